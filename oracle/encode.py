@@ -1,0 +1,27 @@
+"""encode = concatenation over fragments of BPE(fragment bytes): the two-stage
+tokenizer F = E* . G (TokTier, Appendix A.1), with no normaliser, special
+tokens, truncation, padding or dropout (the assumptions listed there).
+decode concatenates token bytes."""
+from .bpe import bpe_heap
+from .pretokenize import pretokenize
+from .utf8 import decode_utf8
+
+
+def pretoken_byte_spans(data, pattern_id):
+    """Fragments as (start_byte, end_byte) spans of the UTF-8 input."""
+    cps, offs = decode_utf8(data)
+    return [(offs[a], offs[b]) for a, b in pretokenize(cps, pattern_id)]
+
+
+def encode(data, vocab, pattern_id, bpe=bpe_heap):
+    data = bytes(data)
+    ids = []
+    mm = vocab.merge_map
+    bid = vocab.byte_id
+    for a, b in pretoken_byte_spans(data, pattern_id):
+        ids.extend(bpe([bid[x] for x in data[a:b]], mm))
+    return ids
+
+
+def decode(ids, vocab):
+    return b"".join(vocab.token_bytes[i] for i in ids)

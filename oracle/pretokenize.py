@@ -1,0 +1,77 @@
+"""Pre-tokenization G: split the text into fragments with a GPT-style regex,
+left to right (TokTier, Sections 3.2 and 4.1: the serial regex pass whose
+every match start depends on where the previous match ended).
+
+The pages name the tokenizer families but print no pattern.  The two
+patterns here are the GPT-2 pattern and the cl100k-style pattern (case-
+insensitive contractions, digit groups of at most three, newline-aware
+whitespace), written as ASTs for regex_engine in the same order as their
+usual regex text:
+
+GPT-2:
+  's|'t|'re|'ve|'m|'ll|'d| ?\\p{L}+| ?\\p{N}+| ?[^\\s\\p{L}\\p{N}]+|\\s+(?!\\S)|\\s+
+
+cl100k-style:
+  (?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\\r\\n\\p{L}\\p{N}]?\\p{L}+|\\p{N}{1,3}
+  | ?[^\\s\\p{L}\\p{N}]+[\\r\\n]*|\\s*[\\r\\n]+|\\s+(?!\\S)|\\s+
+"""
+from .regex_engine import Alt, Cls, INF, Lit, NotAhead, Rep, Seq, match_at
+from .ucd import class_array
+
+PATTERN_GPT2 = 0
+PATTERN_CL100K = 1
+
+_L = Cls(lambda cp, c: c == "L", r"\p{L}")
+_N = Cls(lambda cp, c: c == "N", r"\p{N}")
+_S = Cls(lambda cp, c: c == "W", r"\s")
+_NOT_S = Cls(lambda cp, c: c != "W", r"\S")
+_NOT_SLN = Cls(lambda cp, c: c == "O", r"[^\s\p{L}\p{N}]")
+_NOT_CRLF_L_N = Cls(lambda cp, c: cp not in (10, 13) and c not in ("L", "N"), r"[^\r\n\p{L}\p{N}]")
+_CRLF = Cls(lambda cp, c: cp in (10, 13), r"[\r\n]")
+_SP = Lit(" ")
+
+
+def _contractions(icase):
+    return [Seq(*[Lit(ch, icase) for ch in "'" + tail]) for tail in ("s", "t", "re", "ve", "m", "ll", "d")]
+
+
+GPT2 = Alt(
+    *_contractions(False),
+    Seq(Rep(_SP, 0, 1), Rep(_L, 1, INF)),
+    Seq(Rep(_SP, 0, 1), Rep(_N, 1, INF)),
+    Seq(Rep(_SP, 0, 1), Rep(_NOT_SLN, 1, INF)),
+    Seq(Rep(_S, 1, INF), NotAhead(_NOT_S)),
+    Rep(_S, 1, INF),
+)
+
+CL100K = Alt(
+    Alt(*_contractions(True)),
+    Seq(Rep(_NOT_CRLF_L_N, 0, 1), Rep(_L, 1, INF)),
+    Rep(_N, 1, 3),
+    Seq(Rep(_SP, 0, 1), Rep(_NOT_SLN, 1, INF), Rep(_CRLF, 0, INF)),
+    Seq(Rep(_S, 0, INF), Rep(_CRLF, 1, INF)),
+    Seq(Rep(_S, 1, INF), NotAhead(_NOT_S)),
+    Rep(_S, 1, INF),
+)
+
+PATTERNS = {PATTERN_GPT2: GPT2, PATTERN_CL100K: CL100K}
+
+
+def pretokenize(cps, pattern_id, cls=None):
+    """Fragments of a code point sequence as (start, end) code point spans.
+
+    Matches are taken left to right: each starts where the previous one
+    ended.  Every alternative consumes at least one code point and every
+    class is covered, so the spans partition the text."""
+    pat = PATTERNS[pattern_id]
+    if cls is None:
+        cls = class_array(cps)
+    spans = []
+    i, n = 0, len(cps)
+    while i < n:
+        j = match_at(pat, cps, cls, i)
+        if j is None or j <= i:
+            raise AssertionError("pattern failed to match at %d" % i)
+        spans.append((i, j))
+        i = j
+    return spans

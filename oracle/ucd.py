@@ -1,0 +1,50 @@
+"""Code point classes used by the pre-tokenizer patterns.
+
+L  = \\p{L}  (General_Category Lu, Ll, Lt, Lm, Lo)
+N  = \\p{N}  (General_Category Nd, Nl, No)
+W  = \\s     (the White_Space property: 25 code points)
+O  = everything else (marks, symbols, punctuation, controls, unassigned)
+
+The range data in data/unicode_classes.txt was written by
+gen_unicode_classes.py from a Unicode regex engine.  TokTier, Section 5.2
+(key findings) reports that a Unicode-table version mismatch between two
+implementations mis-split about 9,700 code points; the version the data
+comes from is recorded in the file's first line.
+"""
+import bisect
+import os
+
+_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "data", "unicode_classes.txt")
+
+_starts, _ends, _cls = [], [], []
+with open(_PATH) as _f:
+    for _line in _f:
+        if _line.startswith("#"):
+            continue
+        _a, _b, _c = _line.split()
+        _starts.append(int(_a, 16))
+        _ends.append(int(_b, 16))
+        _cls.append(_c)
+
+VERSION_LINE = open(_PATH).readline().strip()
+
+
+def classify(cp):
+    """Class letter of one code point."""
+    k = bisect.bisect_right(_starts, cp) - 1
+    if k >= 0 and cp <= _ends[k]:
+        return _cls[k]
+    return "O"
+
+
+def class_array(cps):
+    """Class letters of a sequence of code points (memoised per code point)."""
+    memo = {}
+    out = []
+    for cp in cps:
+        c = memo.get(cp)
+        if c is None:
+            c = classify(cp)
+            memo[cp] = c
+        out.append(c)
+    return out

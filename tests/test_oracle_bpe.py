@@ -1,0 +1,131 @@
+"""Pins for the oracle's BPE (E): the pages' worked non-concatenation example,
+agreement of three independent loops, the fixpoint invariant, degenerate
+vocabularies and hand-worked tie-breaks."""
+import random
+
+from oracle.bpe import bpe_heap, bpe_rounds, bpe_textbook
+from oracle.encode import decode, encode
+from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2
+from oracle.vocab import Vocab
+
+
+def _vocab_from_strings(merge_strings):
+    """Byte tokens 0..255 and merges given as (left bytes, right bytes)."""
+    toks = [bytes([b]) for b in range(256)]
+    idx = {t: i for i, t in enumerate(toks)}
+    merges = []
+    for a, b in merge_strings:
+        a, b = a.encode(), b.encode()
+        if a + b not in idx:
+            idx[a + b] = len(toks)
+            toks.append(a + b)
+        merges.append((idx[a], idx[b]))
+    return Vocab(toks, merges), idx
+
+
+def test_pipe_line_pipeline_example():
+    # TokTier, Sections 1.2 and 3.2: "pipe" alone is one token; appending
+    # "line" yields the single token "pipeline", so tok(pipe) + tok(line) is
+    # not tok(pipeline).
+    v, idx = _vocab_from_strings([("p", "i"), ("p", "e"), ("pi", "pe"), ("l", "i"), ("n", "e"),
+                                  ("li", "ne"), ("pipe", "line")])
+    for pat in (PATTERN_GPT2, PATTERN_CL100K):
+        assert encode(b"pipe", v, pat) == [idx[b"pipe"]]
+        assert encode(b"line", v, pat) == [idx[b"line"]]
+        assert encode(b"pipeline", v, pat) == [idx[b"pipeline"]]
+        assert encode(b"pipe", v, pat) + encode(b"line", v, pat) != encode(b"pipeline", v, pat)
+        assert encode(b"pipe line", v, pat) == [idx[b"pipe"], 32, idx[b"line"]]
+
+
+def test_zero_merges_is_bytes():
+    v = Vocab.from_merges([])
+    data = "héllo 世界 1234\n".encode()
+    assert encode(data, v, PATTERN_GPT2) == list(data)
+    assert encode(data, v, PATTERN_CL100K) == list(data)
+
+
+def test_leftmost_tie_break_and_rank_order():
+    v, idx = _vocab_from_strings([("a", "a")])
+    mm = v.merge_map
+    aa = idx[b"aa"]
+    for f in (bpe_textbook, bpe_rounds, bpe_heap):
+        assert f([97, 97, 97], mm) == [aa, 97]
+        assert f([97, 97, 97, 97], mm) == [aa, aa]
+        assert f([98, 97, 97, 97, 98], mm) == [98, aa, 97, 98]
+    # lower rank wins wherever it is: (b,c) rank 0 beats (a,b) rank 1
+    v2, i2 = _vocab_from_strings([("b", "c"), ("a", "b")])
+    for f in (bpe_textbook, bpe_rounds, bpe_heap):
+        assert f([97, 98, 99], v2.merge_map) == [97, i2[b"bc"]]
+
+
+def test_local_minima_are_not_enough():
+    # ranks AB=3, BC=5, CD=1 plus BX=2 where X=CD: merging both local minima
+    # (AB and CD) at once gives (AB)(CD); the rule gives A(B(CD)).
+    v, idx = _vocab_from_strings([("x", "y"), ("c", "d"), ("b", "cd"), ("a", "b"), ("q", "r"), ("b", "c")])
+    mm = v.merge_map
+    want = [97, idx[b"bcd"]]
+    for f in (bpe_textbook, bpe_rounds, bpe_heap):
+        assert f([97, 98, 99, 100], mm) == want
+
+
+def _random_vocab(rnd, alphabet, n_merges):
+    toks = [bytes([b]) for b in range(256)]
+    idx = {t: i for i, t in enumerate(toks)}
+    live = [ord(c) for c in alphabet]
+    merges = []
+    seen = set()
+    tries = 0
+    while len(merges) < n_merges and tries < 10 * n_merges:
+        tries += 1
+        a, b = rnd.choice(live), rnd.choice(live)
+        if (a, b) in seen or len(toks[a]) + len(toks[b]) > 6:
+            continue
+        seen.add((a, b))
+        t = toks[a] + toks[b]
+        if t not in idx:
+            idx[t] = len(toks)
+            toks.append(t)
+            live.append(idx[t])
+        merges.append((a, b))
+    return Vocab(toks, merges)
+
+
+def test_three_loops_agree_on_random_vocabs():
+    rnd = random.Random(3)
+    n_mono = 0
+    for trial in range(300):
+        v = _random_vocab(rnd, "abc", rnd.randint(1, 25))
+        mono = v.monotone()
+        n_mono += mono
+        for _ in range(20):
+            w = [rnd.choice(b"abc") for _ in range(rnd.randint(0, 24))]
+            t = bpe_textbook(w, v.merge_map)
+            assert bpe_heap(w, v.merge_map) == t
+            if mono:
+                assert bpe_rounds(w, v.merge_map) == t
+            # fixpoint: no adjacent output pair is a merge
+            assert all((x, y) not in v.merge_map for x, y in zip(t, t[1:]))
+            assert b"".join(v.token_bytes[i] for i in t) == bytes(w)
+    assert n_mono > 50
+
+
+def test_heap_matches_textbook_on_long_words():
+    rnd = random.Random(9)
+    v = _random_vocab(rnd, "ab ", 60)
+    for n in (200, 1000):
+        w = [rnd.choice(b"ab ") for _ in range(n)]
+        assert bpe_heap(w, v.merge_map) == bpe_textbook(w, v.merge_map)
+
+
+def test_decode_roundtrip_and_vocab_checks():
+    v, _ = _vocab_from_strings([("h", "e"), ("l", "l"), ("he", "ll"), (" ", "w")])
+    data = "hello world héllo\r\n".encode()
+    assert decode(encode(data, v, PATTERN_GPT2), v) == data
+    import pytest
+    from oracle.vocab import VocabError
+    with pytest.raises(VocabError):
+        Vocab([bytes([b]) for b in range(255)], [])
+    with pytest.raises(VocabError):
+        Vocab([bytes([b]) for b in range(256)], [(97, 97), (97, 97)])
+    with pytest.raises(VocabError):
+        Vocab([bytes([b]) for b in range(256)], [(97, 98)])  # result bytes missing

@@ -1,0 +1,76 @@
+"""Pins for the oracle's pre-tokenizer (G): the committed split examples, the
+third-party `regex` module on every short string over an adversarial
+alphabet and on generated text, and the partition invariant."""
+import itertools
+import json
+import os
+import random
+
+import pytest
+
+import textgen
+from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2, pretokenize
+from oracle.utf8 import decode_utf8
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+GPT2_RE = r"""'s|'t|'re|'ve|'m|'ll|'d| ?\p{L}+| ?\p{N}+| ?[^\s\p{L}\p{N}]+|\s+(?!\S)|\s+"""
+CL100K_RE = (r"""(?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\r\n\p{L}\p{N}]?\p{L}+|\p{N}{1,3}"""
+             r"""| ?[^\s\p{L}\p{N}]+[\r\n]*|\s*[\r\n]+|\s+(?!\S)|\s+""")
+
+ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ"
+
+
+def split(s, pat):
+    cps, _ = decode_utf8(s.encode())
+    return [s[a:b] for a, b in pretokenize(cps, pat)]
+
+
+def test_pinned_examples():
+    n = 0
+    with open(os.path.join(HERE, "golden", "pretoken_pins.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            s, g, c = json.loads(line)
+            assert split(s, PATTERN_GPT2) == g, s
+            assert split(s, PATTERN_CL100K) == c, s
+            n += 1
+    assert n >= 20
+
+
+def test_partition_and_empty():
+    assert pretokenize([], PATTERN_GPT2) == []
+    s = textgen.mixed_c2(4000, 3)
+    for pat in (PATTERN_GPT2, PATTERN_CL100K):
+        parts = split(s, pat)
+        assert "".join(parts) == s and all(parts)
+
+
+def _regex_split(rx, s):
+    return rx.findall(s)
+
+
+def test_brute_force_against_regex_module():
+    regex = pytest.importorskip("regex")
+    rg, rc = regex.compile(GPT2_RE), regex.compile(CL100K_RE)
+    for n in range(1, 4):
+        for t in itertools.product(ALPHABET, repeat=n):
+            s = "".join(t)
+            assert split(s, PATTERN_GPT2) == rg.findall(s), repr(s)
+            assert split(s, PATTERN_CL100K) == rc.findall(s), repr(s)
+    rnd = random.Random(11)
+    for _ in range(5000):
+        s = "".join(rnd.choice(ALPHABET) for _ in range(rnd.randint(4, 16)))
+        assert split(s, PATTERN_GPT2) == rg.findall(s), repr(s)
+        assert split(s, PATTERN_CL100K) == rc.findall(s), repr(s)
+
+
+def test_generated_text_against_regex_module():
+    regex = pytest.importorskip("regex")
+    rg, rc = regex.compile(GPT2_RE), regex.compile(CL100K_RE)
+    texts = [textgen.code_ascii(8000, 1), textgen.mixed_c2(20000, 2), textgen.agentic_session(20000, 3)]
+    texts += textgen.adversarial_pieces(5, scale=0.002)
+    for s in texts:
+        assert split(s, PATTERN_GPT2) == rg.findall(s)
+        assert split(s, PATTERN_CL100K) == rc.findall(s)
