@@ -1,0 +1,587 @@
+// Host side of the C ABI declared in include/tok.h.
+//
+// A handle owns the device-side vocabulary (merge hash table, per-token
+// lengths and operand-length bounds), a workspace that grows to the largest
+// input seen and is then reused (no per-call allocation after warm-up), a
+// stream, and a pinned status buffer.  A host request costs two host
+// synchronisations: one to read the status and id count, one for the ids
+// ("TokTier: exact stateful tokenization for agentic LLM serving", Section
+// 4.3, cuts a request from eight host syncs to two).
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/tok.h"
+#include "tok_common.cuh"
+
+using namespace tokgb;
+
+namespace {
+
+constexpr int N_STAGES = 6;
+const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_bpe_short",
+                                     "k_bpe_med",     "k_bpe_long",   "k_emit"};
+
+thread_local std::string g_load_error;
+
+struct ByteStringHash {
+  size_t operator()(const std::string& s) const { return std::hash<std::string>()(s); }
+};
+
+}  // namespace
+
+struct tok_handle {
+  int dev = 0;
+  int n_sms = 1;
+  int pattern = 0;
+  cudaStream_t stream = nullptr;
+  DevVocab v{};
+  // device allocations of the vocabulary
+  MergeEntry* d_table = nullptr;
+  int32_t* d_byte_id = nullptr;
+  uint16_t* d_tok_len = nullptr;
+  uint16_t* d_max_left = nullptr;
+  uint16_t* d_max_right = nullptr;
+  uint64_t hash = 0;
+  // workspace
+  Workspace ws{};
+  int32_t* d_out = nullptr;           // ids of host-side calls
+  long long* d_items = nullptr;       // item starts of host-side batch calls
+  long long* d_item_off = nullptr;
+  uint64_t cap_items = 0;
+  DevStatus* h_status = nullptr;      // pinned
+  long long* h_items = nullptr;       // pinned
+  uint64_t cap_h_items = 0;
+  uint32_t epoch = 0;
+  std::string err;
+  int64_t err_off = -1;
+  uint64_t launches = 0;
+  bool timing = false;
+  cudaEvent_t ev[N_STAGES + 1] = {};
+  float stage_ms[N_STAGES] = {};
+  bool have_times = false;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+    else prev = -1;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+int fail(tok_handle* h, int code, const std::string& msg) {
+  if (h) h->err = msg;
+  else g_load_error = msg;
+  return code;
+}
+
+int cuda_fail(tok_handle* h, cudaError_t e, const char* what) {
+  return fail(h, TOK_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+uint64_t fnv1a(uint64_t h, const void* p, size_t n) {
+  const uint8_t* b = static_cast<const uint8_t*>(p);
+  for (size_t i = 0; i < n; ++i) {
+    h ^= b[i];
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+template <class T>
+cudaError_t dalloc(T** p, size_t count) {
+  return cudaMalloc(reinterpret_cast<void**>(p), std::max<size_t>(count, 1) * sizeof(T));
+}
+
+void free_workspace(tok_handle* h) {
+  Workspace& w = h->ws;
+  void* ptrs[] = {w.text, w.csum, w.pstart, w.tstart, w.sid, w.medq, w.longq, w.lb, w.st,
+                  w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1], w.e_kr[0], w.e_kr[1], w.e_fl, w.e_rs,
+                  h->d_out};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  w = Workspace{};
+  h->d_out = nullptr;
+}
+
+// Grow the workspace to hold n bytes (no-op when it already does).
+int ensure_workspace(tok_handle* h, uint64_t n) {
+  if (h->ws.st && n <= h->ws.cap_bytes) return TOK_OK;
+  uint64_t cap = std::max<uint64_t>(n + n / 4, 1 << 16);
+  cap = (cap + CHUNK - 1) / CHUNK * CHUNK;
+  free_workspace(h);
+  Workspace& w = h->ws;
+  const uint64_t nch = cap / CHUNK;
+  const uint64_t pad = 256;
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+  chk(dalloc(&w.text, cap + pad));
+  chk(dalloc(&w.csum, nch + 2));
+  chk(dalloc(&w.pstart, cap / 32 + pad));
+  chk(dalloc(&w.tstart, cap + pad));
+  chk(dalloc(&w.sid, cap + pad));
+  chk(dalloc(&w.medq, cap / (SHORT_MAX + 1) + pad));
+  chk(dalloc(&w.longq, cap / (MED_MAX + 1) + cap / BPE_CHUNK + pad));
+  chk(dalloc(&w.lb, nch + 2));
+  chk(dalloc(&w.st, 1));
+  for (int b = 0; b < 2; ++b) {
+    chk(dalloc(&w.e_sym[b], cap + pad));
+    chk(dalloc(&w.e_len[b], cap + pad));
+    chk(dalloc(&w.e_kr[b], cap + pad));
+  }
+  chk(dalloc(&w.e_fl, cap + pad));
+  chk(dalloc(&w.e_rs, cap + pad));
+  chk(dalloc(&h->d_out, cap + pad));
+  if (e == cudaSuccess) e = cudaMemset(w.lb, 0, (nch + 2) * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(w.pstart, 0, (cap / 32 + pad) * sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    free_workspace(h);
+    cudaGetLastError();
+    return fail(h, TOK_ENOMEM, std::string("workspace allocation failed: ") + cudaGetErrorString(e));
+  }
+  w.cap_bytes = cap;
+  w.cap_chunks = nch;
+  return TOK_OK;
+}
+
+int ensure_items(tok_handle* h, uint64_t n_items) {
+  if (n_items + 1 <= h->cap_items && n_items + 1 <= h->cap_h_items) return TOK_OK;
+  const uint64_t cap = std::max<uint64_t>(n_items + 1, 64) * 2;
+  if (h->d_items) cudaFree(h->d_items);
+  if (h->d_item_off) cudaFree(h->d_item_off);
+  if (h->h_items) cudaFreeHost(h->h_items);
+  h->d_items = nullptr; h->d_item_off = nullptr; h->h_items = nullptr;
+  cudaError_t e = dalloc(&h->d_items, cap);
+  if (e == cudaSuccess) e = dalloc(&h->d_item_off, cap);
+  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&h->h_items), cap * sizeof(long long));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    h->cap_items = h->cap_h_items = 0;
+    return fail(h, TOK_ENOMEM, "item buffer allocation failed");
+  }
+  h->cap_items = h->cap_h_items = cap;
+  return TOK_OK;
+}
+
+// Enqueue the whole chain for one call.
+int run_chain(tok_handle* h, Call c, cudaStream_t s) {
+  c.pattern = h->pattern;
+  c.epoch = ++h->epoch;
+  if (h->epoch >= 0x3FFFFFFFu) h->epoch = 0;
+  if (c.n == 0) {
+    launch_status_only(c, h->ws, s);
+    h->launches += 1;
+    h->have_times = false;
+  } else {
+    const bool tm = h->timing;
+    if (tm) cudaEventRecord(h->ev[0], s);
+    launch_run_summary(c, h->ws, s);
+    if (tm) cudaEventRecord(h->ev[1], s);
+    launch_boundaries(c, h->ws, s);
+    if (tm) cudaEventRecord(h->ev[2], s);
+    launch_bpe_short(c, h->ws, h->v, s);
+    if (tm) cudaEventRecord(h->ev[3], s);
+    launch_bpe_med(c, h->ws, h->v, h->n_sms, s);
+    if (tm) cudaEventRecord(h->ev[4], s);
+    launch_bpe_long(c, h->ws, h->v, h->n_sms, s);
+    if (tm) cudaEventRecord(h->ev[5], s);
+    launch_emit(c, h->ws, s);
+    if (tm) cudaEventRecord(h->ev[6], s);
+    h->launches += N_STAGES;
+    h->have_times = tm;
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  return TOK_OK;
+}
+
+void collect_times(tok_handle* h) {
+  if (!h->have_times) return;
+  for (int k = 0; k < N_STAGES; ++k) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, h->ev[k], h->ev[k + 1]) == cudaSuccess) h->stage_ms[k] = ms;
+  }
+}
+
+// Read the status after the chain; sync 1 of a host request.
+int read_status(tok_handle* h, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(h->h_status, h->ws.st, sizeof(DevStatus), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "status read");
+  collect_times(h);
+  h->err_off = -1;
+  if (h->h_status->err_off != ~0ull) {
+    h->err_off = (int64_t)h->h_status->err_off;
+    char buf[96];
+    snprintf(buf, sizeof buf, "invalid UTF-8 at byte %lld", (long long)h->err_off);
+    return fail(h, TOK_EUTF8, buf);
+  }
+  if (h->h_status->code == ST_ETIMEOUT) return fail(h, TOK_ETIMEOUT, "device-side wait gave up");
+  if (h->h_status->code != ST_OK) return fail(h, TOK_ECUDA, "device-side internal error");
+  return TOK_OK;
+}
+
+Call base_call(tok_handle* h, const uint8_t* d_text, uint64_t n) {
+  Call c{};
+  c.text = d_text;
+  c.n = (long long)n;
+  c.item = nullptr;
+  c.n_items = 1;
+  c.pattern = h->pattern;
+  return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_vocab, const uint32_t* merges,
+             uint32_t n_merges, int pattern_id, tok_handle** out) {
+  if (!out) return fail(nullptr, TOK_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (pattern_id != TOK_PAT_GPT2 && pattern_id != TOK_PAT_CL100K_STYLE)
+    return fail(nullptr, TOK_EINVAL, "unknown pattern id");
+  if (!vocab_bytes || !vocab_off || (n_merges && !merges)) return fail(nullptr, TOK_EINVAL, "NULL vocabulary");
+  if (n_vocab < 256 || n_vocab >= (1u << 20)) return fail(nullptr, TOK_EMERGES, "n_vocab out of range");
+  // tokens
+  std::unordered_map<std::string, uint32_t, ByteStringHash> index;
+  index.reserve(n_vocab * 2);
+  std::vector<uint16_t> tok_len(n_vocab);
+  for (uint32_t t = 0; t < n_vocab; ++t) {
+    if (vocab_off[t + 1] < vocab_off[t]) return fail(nullptr, TOK_EMERGES, "vocab offsets not increasing");
+    const uint64_t len = vocab_off[t + 1] - vocab_off[t];
+    if (len == 0 || len > 65535) return fail(nullptr, TOK_EMERGES, "token length out of range");
+    tok_len[t] = (uint16_t)len;
+    std::string s(reinterpret_cast<const char*>(vocab_bytes + vocab_off[t]), len);
+    if (!index.emplace(std::move(s), t).second) return fail(nullptr, TOK_EMERGES, "duplicate token bytes");
+  }
+  std::vector<int32_t> byte_id(256);
+  for (int b = 0; b < 256; ++b) {
+    auto it = index.find(std::string(1, (char)b));
+    if (it == index.end()) return fail(nullptr, TOK_EMERGES, "a single byte has no token");
+    byte_id[b] = (int32_t)it->second;
+  }
+  // merges -> hash table
+  uint32_t bits = 10;
+  while ((1ull << bits) < 2ull * n_merges) ++bits;
+  std::vector<MergeEntry> table(1ull << bits, MergeEntry{EMPTY_KEY, 0, 0});
+  std::vector<uint16_t> max_left(n_vocab, 0), max_right(n_vocab, 0);
+  std::vector<int64_t> last_made(n_vocab, -1), first_used(n_vocab, INT64_MAX);
+  const uint32_t mask = (1u << bits) - 1u;
+  for (uint32_t r = 0; r < n_merges; ++r) {
+    const uint32_t a = merges[2 * r], b = merges[2 * r + 1];
+    if (a >= n_vocab || b >= n_vocab) return fail(nullptr, TOK_EMERGES, "merge id out of range");
+    std::string s(reinterpret_cast<const char*>(vocab_bytes + vocab_off[a]), tok_len[a]);
+    s.append(reinterpret_cast<const char*>(vocab_bytes + vocab_off[b]), tok_len[b]);
+    auto it = index.find(s);
+    if (it == index.end()) return fail(nullptr, TOK_EMERGES, "merge result not in vocabulary");
+    const uint32_t res = it->second;
+    const unsigned long long key = ((unsigned long long)a << 32) | b;
+    uint32_t slot = merge_slot(key, bits);
+    while (table[slot].key != EMPTY_KEY) {
+      if (table[slot].key == key) return fail(nullptr, TOK_EMERGES, "duplicate merge pair");
+      slot = (slot + 1) & mask;
+    }
+    table[slot] = MergeEntry{key, r, res};
+    max_left[b] = std::max(max_left[b], tok_len[a]);
+    max_right[a] = std::max(max_right[a], tok_len[b]);
+    last_made[res] = std::max<int64_t>(last_made[res], r);
+    first_used[a] = std::min<int64_t>(first_used[a], r);
+    first_used[b] = std::min<int64_t>(first_used[b], r);
+  }
+  bool monotone = true;
+  for (uint32_t t = 0; t < n_vocab && monotone; ++t)
+    if (last_made[t] >= 0 && first_used[t] != INT64_MAX && first_used[t] <= last_made[t]) monotone = false;
+
+  tok_handle* h = new tok_handle();
+  h->pattern = pattern_id;
+  cudaError_t e = cudaGetDevice(&h->dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, h->dev);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = dalloc(&h->d_table, table.size());
+  if (e == cudaSuccess) e = dalloc(&h->d_byte_id, 256);
+  if (e == cudaSuccess) e = dalloc(&h->d_tok_len, n_vocab);
+  if (e == cudaSuccess) e = dalloc(&h->d_max_left, n_vocab);
+  if (e == cudaSuccess) e = dalloc(&h->d_max_right, n_vocab);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->d_table, table.data(), table.size() * sizeof(MergeEntry), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->d_byte_id, byte_id.data(), 256 * sizeof(int32_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->d_tok_len, tok_len.data(), n_vocab * 2, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->d_max_left, max_left.data(), n_vocab * 2, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(h->d_max_right, max_right.data(), n_vocab * 2, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&h->h_status), sizeof(DevStatus));
+  for (int k = 0; k <= N_STAGES && e == cudaSuccess; ++k) e = cudaEventCreate(&h->ev[k]);
+  if (e != cudaSuccess) {
+    const int code = (e == cudaErrorMemoryAllocation) ? TOK_ENOMEM : TOK_ECUDA;
+    std::string msg = std::string("tok_load: ") + cudaGetErrorString(e);
+    cudaGetLastError();
+    tok_free(h);
+    return fail(nullptr, code, msg);
+  }
+  h->v.table = h->d_table;
+  h->v.bits = bits;
+  h->v.n_vocab = n_vocab;
+  h->v.byte_id = h->d_byte_id;
+  h->v.tok_len = h->d_tok_len;
+  h->v.max_left = h->d_max_left;
+  h->v.max_right = h->d_max_right;
+  h->v.monotone = monotone ? 1 : 0;
+  uint64_t hh = 1469598103934665603ull;
+  hh = fnv1a(hh, &pattern_id, sizeof pattern_id);
+  for (uint32_t t = 0; t < n_vocab; ++t) {
+    const uint32_t l = tok_len[t];
+    hh = fnv1a(hh, &l, sizeof l);
+    hh = fnv1a(hh, vocab_bytes + vocab_off[t], l);
+  }
+  hh = fnv1a(hh, merges, (size_t)n_merges * 2 * sizeof(uint32_t));
+  h->hash = hh;
+  *out = h;
+  return TOK_OK;
+}
+
+void tok_free(tok_handle* h) {
+  if (!h) return;
+  DeviceGuard g(h->dev);
+  if (h->stream) cudaStreamSynchronize(h->stream);
+  free_workspace(h);
+  void* ptrs[] = {h->d_table, h->d_byte_id, h->d_tok_len, h->d_max_left, h->d_max_right, h->d_items, h->d_item_off};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  if (h->h_status) cudaFreeHost(h->h_status);
+  if (h->h_items) cudaFreeHost(h->h_items);
+  for (int k = 0; k <= N_STAGES; ++k)
+    if (h->ev[k]) cudaEventDestroy(h->ev[k]);
+  if (h->stream) cudaStreamDestroy(h->stream);
+  delete h;
+}
+
+const char* tok_last_error(tok_handle* h) { return h ? h->err.c_str() : g_load_error.c_str(); }
+
+int64_t tok_error_offset(tok_handle* h) { return h ? h->err_off : -1; }
+
+uint64_t tok_content_hash(tok_handle* h) { return h ? h->hash : 0; }
+
+uint64_t tok_launch_count(tok_handle* h) { return h ? h->launches : 0; }
+
+int tok_set_timing(tok_handle* h, int enable) {
+  if (!h) return TOK_EINVAL;
+  h->timing = enable != 0;
+  return TOK_OK;
+}
+
+int tok_stage_times(tok_handle* h, float* ms, const char** names, int cap) {
+  if (!h) return TOK_EINVAL;
+  if (!h->have_times) return 0;
+  DeviceGuard g(h->dev);
+  collect_times(h);
+  const int n = std::min(cap, N_STAGES);
+  for (int k = 0; k < n; ++k) {
+    if (ms) ms[k] = h->stage_ms[k];
+    if (names) names[k] = kStageNames[k];
+  }
+  return n;
+}
+
+int tok_encode(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, uint64_t cap, uint64_t* n_ids) {
+  if (!h || !n_ids || (len && !text)) return fail(h, TOK_EINVAL, "bad argument");
+  DeviceGuard g(h->dev);
+  *n_ids = 0;
+  int rc = ensure_workspace(h, len);
+  if (rc) return rc;
+  cudaStream_t s = h->stream;
+  if (len) {
+    const cudaError_t e = cudaMemcpyAsync(h->ws.text, text, len, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
+  }
+  Call c = base_call(h, h->ws.text, len);
+  c.out = h->d_out;
+  rc = run_chain(h, c, s);
+  if (rc) return rc;
+  rc = read_status(h, s);
+  if (rc) return rc;
+  const uint64_t n = h->h_status->n_ids;
+  *n_ids = n;
+  if (n > cap) return fail(h, TOK_EBUF, "output buffer too small");
+  if (n) {
+    if (!ids) return fail(h, TOK_EINVAL, "ids is NULL");
+    cudaError_t e = cudaMemcpyAsync(ids, h->d_out, n * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "id copy");
+  }
+  return TOK_OK;
+}
+
+int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t* lens, uint32_t n, int32_t* ids,
+                     uint64_t cap, uint64_t* item_off) {
+  if (!h || (n && (!texts || !lens)) || !item_off) return fail(h, TOK_EINVAL, "bad argument");
+  DeviceGuard g(h->dev);
+  uint64_t total = 0;
+  for (uint32_t k = 0; k < n; ++k) {
+    if (lens[k] && !texts[k]) return fail(h, TOK_EINVAL, "NULL item");
+    total += lens[k];
+  }
+  int rc = ensure_workspace(h, total);
+  if (rc) return rc;
+  rc = ensure_items(h, n);
+  if (rc) return rc;
+  cudaStream_t s = h->stream;
+  uint64_t pos = 0;
+  for (uint32_t k = 0; k < n; ++k) {
+    h->h_items[k] = (long long)pos;
+    if (lens[k]) {
+      const cudaError_t e = cudaMemcpyAsync(h->ws.text + pos, texts[k], lens[k], cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
+    }
+    pos += lens[k];
+  }
+  h->h_items[n] = (long long)total;
+  cudaError_t e = cudaMemcpyAsync(h->d_items, h->h_items, (n + 1) * sizeof(long long), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "item copy");
+  Call c = base_call(h, h->ws.text, total);
+  c.item = h->d_items;
+  c.n_items = (int)n;
+  c.out = h->d_out;
+  c.item_off = h->d_item_off;
+  rc = run_chain(h, c, s);
+  if (rc) return rc;
+  rc = read_status(h, s);
+  if (rc) return rc;
+  const uint64_t nid = h->h_status->n_ids;
+  if (nid > cap) {
+    item_off[n] = nid;
+    return fail(h, TOK_EBUF, "output buffer too small");
+  }
+  if (nid && !ids) return fail(h, TOK_EINVAL, "ids is NULL");
+  if (nid) e = cudaMemcpyAsync(ids, h->d_out, nid * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(h->h_items, h->d_item_off, (n + 1) * sizeof(long long),
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "id copy");
+  for (uint32_t k = 0; k <= n; ++k) item_off[k] = (uint64_t)h->h_items[k];
+  return TOK_OK;
+}
+
+int tok_encode_device(tok_handle* h, const uint8_t* d_text, uint64_t len, int32_t* d_ids, uint64_t cap,
+                      int64_t* d_status, void* stream) {
+  if (!h || !d_status || (len && (!d_text || !d_ids))) return fail(h, TOK_EINVAL, "bad argument");
+  if (cap < len) return fail(h, TOK_EBUF, "cap must be >= len");
+  DeviceGuard g(h->dev);
+  int rc = ensure_workspace(h, len);
+  if (rc) return rc;
+  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : h->stream;
+  Call c = base_call(h, d_text, len);
+  c.out = d_ids;
+  c.user_status = reinterpret_cast<long long*>(d_status);
+  return run_chain(h, c, s);
+}
+
+int tok_encode_batch_device(tok_handle* h, const uint8_t* d_text, uint64_t len, const int64_t* d_item_start,
+                            uint32_t n, int32_t* d_ids, uint64_t cap, int64_t* d_item_off, int64_t* d_status,
+                            void* stream) {
+  if (!h || !d_status || !d_item_start || !d_item_off || n == 0 || (len && (!d_text || !d_ids)))
+    return fail(h, TOK_EINVAL, "bad argument");
+  if (cap < len) return fail(h, TOK_EBUF, "cap must be >= len");
+  DeviceGuard g(h->dev);
+  int rc = ensure_workspace(h, len);
+  if (rc) return rc;
+  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : h->stream;
+  Call c = base_call(h, d_text, len);
+  c.item = reinterpret_cast<const long long*>(d_item_start);
+  c.n_items = (int)n;
+  c.out = d_ids;
+  c.item_off = reinterpret_cast<long long*>(d_item_off);
+  c.user_status = reinterpret_cast<long long*>(d_status);
+  return run_chain(h, c, s);
+}
+
+// Pre-tokenizer only, over items packed back to back (items == nullptr: one
+// item).  Fragment starts are offsets into the concatenation.
+static int pretokenize_impl(tok_handle* h, uint64_t len, uint32_t n_items, bool batch, int64_t* starts,
+                            uint64_t cap, uint64_t* n) {
+  cudaStream_t s = h->stream;
+  Call c = base_call(h, h->ws.text, len);
+  if (batch) {
+    c.item = h->d_items;
+    c.n_items = (int)n_items;
+  }
+  c.epoch = ++h->epoch;
+  launch_run_summary(c, h->ws, s);
+  launch_boundaries(c, h->ws, s);
+  h->launches += 2;
+  h->have_times = false;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  int rc = read_status(h, s);
+  if (rc) return rc;
+  const uint64_t nw = (len + 31) / 32;
+  std::vector<uint32_t> bits(nw);
+  e = cudaMemcpy(bits.data(), h->ws.pstart, nw * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "bitmask copy");
+  uint64_t cnt = 0;
+  for (uint64_t w = 0; w < nw; ++w) {
+    uint32_t v = bits[w];
+    while (v) {
+      const int b = __builtin_ctz(v);
+      v &= v - 1;
+      const uint64_t p = w * 32 + (uint64_t)b;
+      if (p >= len) break;
+      if (cnt < cap && starts) starts[cnt] = (int64_t)p;
+      ++cnt;
+    }
+  }
+  *n = cnt;
+  if (cnt > cap) return fail(h, TOK_EBUF, "starts buffer too small");
+  return TOK_OK;
+}
+
+int tok_pretokenize(tok_handle* h, const uint8_t* text, uint64_t len, int64_t* starts, uint64_t cap, uint64_t* n) {
+  if (!h || !n || (len && !text)) return fail(h, TOK_EINVAL, "bad argument");
+  DeviceGuard g(h->dev);
+  *n = 0;
+  int rc = ensure_workspace(h, len);
+  if (rc) return rc;
+  if (len == 0) return TOK_OK;
+  const cudaError_t e = cudaMemcpyAsync(h->ws.text, text, len, cudaMemcpyHostToDevice, h->stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
+  return pretokenize_impl(h, len, 1, false, starts, cap, n);
+}
+
+int tok_pretokenize_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t* lens, uint32_t n_items,
+                          int64_t* starts, uint64_t cap, uint64_t* n) {
+  if (!h || !n || (n_items && (!texts || !lens))) return fail(h, TOK_EINVAL, "bad argument");
+  DeviceGuard g(h->dev);
+  *n = 0;
+  uint64_t total = 0;
+  for (uint32_t k = 0; k < n_items; ++k) total += lens[k];
+  int rc = ensure_workspace(h, total);
+  if (rc) return rc;
+  rc = ensure_items(h, n_items);
+  if (rc) return rc;
+  if (total == 0) return TOK_OK;
+  cudaStream_t s = h->stream;
+  uint64_t pos = 0;
+  for (uint32_t k = 0; k < n_items; ++k) {
+    h->h_items[k] = (long long)pos;
+    if (lens[k]) {
+      const cudaError_t e = cudaMemcpyAsync(h->ws.text + pos, texts[k], lens[k], cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
+    }
+    pos += lens[k];
+  }
+  h->h_items[n_items] = (long long)total;
+  const cudaError_t e =
+      cudaMemcpyAsync(h->d_items, h->h_items, (n_items + 1) * sizeof(long long), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "item copy");
+  return pretokenize_impl(h, total, n_items, true, starts, cap, n);
+}
+
+}  // extern "C"

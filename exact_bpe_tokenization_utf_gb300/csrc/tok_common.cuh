@@ -1,0 +1,172 @@
+// Shared definitions of the GB300 exact BPE tokenizer library.
+//
+// Pipeline (one pass over a text or a packed batch; "TokTier: exact stateful
+// tokenization for agentic LLM serving", Section 4):
+//   K1 run_summary   per 4 KiB chunk: the chunk's effect on three run states
+//                    (digit-run offset mod 3, "CR/LF-only since an O-run"
+//                    whitespace prefix, "CR/LF later in this whitespace run")
+//   K2 boundaries    UTF-8 validation + per-code-point class + run
+//                    decomposition rules -> fragment-start bitmask (Section 4.1)
+//   K3 bpe_short     fragments <= 16 bytes: one thread each, registers;
+//                    longer fragments are queued (Section 4.2 tiering)
+//   K4 bpe_sweep     queued fragments: a warp (<= 256 bytes) or a CTA (longer)
+//                    each, merging every pair that is certified safe per sweep
+//   K5 emit          token-start flags -> compacted ids (decoupled look-back)
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tokgb {
+
+constexpr int CHUNK = 4096;        // bytes per pre-tokenizer / emit CTA
+constexpr int CHUNK_THREADS = 256; // 16 bytes per thread
+constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
+constexpr int BPE_CHUNK = 1024;    // bytes per short-tier CTA
+constexpr int BPE_THREADS = 256;
+constexpr int SHORT_MAX = 16;      // thread tier
+constexpr int MED_MAX = 256;       // warp tier (shared memory); longer -> CTA tier
+constexpr int MED_WARPS = 4;       // warps per warp-tier CTA
+constexpr int LONG_THREADS = 512;  // CTA tier
+constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
+constexpr unsigned long long EMPTY_KEY = ~0ull;
+
+// code point classes of the pre-tokenizer patterns
+enum : uint32_t { CLS_O = 0, CLS_L = 1, CLS_N = 2, CLS_W = 3 };
+
+// status codes mirrored from tok.h
+enum : int32_t { ST_OK = 0, ST_EUTF8 = -2, ST_EBUF = -5, ST_ETIMEOUT = -6, ST_EINTERNAL = -4 };
+
+// merge table entry: key = left << 32 | right; rank = merge index; result id
+struct __align__(16) MergeEntry {
+  unsigned long long key;
+  uint32_t rank;
+  uint32_t result;
+};
+
+struct DevVocab {
+  const MergeEntry* table;
+  uint32_t bits;              // log2(capacity)
+  uint32_t n_vocab;
+  const int32_t* byte_id;     // 256 entries: initial symbol of each byte value
+  const uint16_t* tok_len;    // byte length of every token
+  const uint16_t* max_left;   // longest left operand of any merge whose right operand is t
+  const uint16_t* max_right;  // longest right operand of any merge whose left operand is t
+  int monotone;               // every merge that uses a token comes after every merge making it
+};
+
+// one queued fragment
+struct Frag {
+  long long start;
+  long long len;  // -1: end not yet known
+};
+
+// device-side per-call status and work counters
+struct DevStatus {
+  int32_t code;
+  uint32_t epoch;
+  unsigned long long err_off;   // first malformed UTF-8 byte (atomicMin), ~0 if none
+  unsigned long long n_ids;
+  uint32_t med_count, med_taken;
+  uint32_t long_count, long_taken;
+  uint32_t emit_ticket, emit_done;
+  uint32_t pad[6];
+};
+
+struct Workspace {
+  uint8_t* text;            // device copy of host input (host entry points)
+  uint32_t* csum;           // K1 chunk summaries
+  uint32_t* pstart;         // fragment-start bitmask
+  uint8_t* tstart;          // 1 at the first byte of every token
+  int32_t* sid;             // token id at token-start bytes
+  Frag* medq;               // warp-tier queue
+  Frag* longq;              // CTA-tier queue
+  unsigned long long* lb;   // K5 look-back words
+  DevStatus* st;
+  // CTA-tier engine storage, indexed by byte position of the fragment
+  uint32_t* e_sym[2];
+  uint16_t* e_len[2];
+  unsigned long long* e_kr[2];
+  uint8_t* e_fl;
+  int32_t* e_rs;
+  uint64_t cap_bytes;       // capacity in bytes of the per-byte arrays
+  uint64_t cap_chunks;
+};
+
+struct Call {
+  const uint8_t* text;        // device
+  long long n;                // bytes
+  const long long* item;      // device item starts, n_items + 1 entries
+  int n_items;
+  int pattern;
+  uint32_t epoch;
+  int32_t* out;               // device ids
+  long long* item_off;        // device, n_items + 1 (batch) or nullptr
+  long long* user_status;     // device int64[4] or nullptr
+};
+
+__host__ __device__ inline uint32_t merge_slot(unsigned long long key, uint32_t bits) {
+  return (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> (64 - bits));
+}
+
+#ifdef __CUDACC__
+// Probe the merge table for (a, b): returns (rank << 32 | result), or ~0 when
+// the pair is not a merge.  Linear probing over a table at most half full,
+// so an empty slot always ends the probe; the loop is bounded anyway.
+__device__ __forceinline__ unsigned long long merge_lookup(const DevVocab& v, uint32_t a, uint32_t b) {
+  const unsigned long long key = ((unsigned long long)a << 32) | b;
+  const uint32_t mask = (1u << v.bits) - 1u;
+  uint32_t s = merge_slot(key, v.bits);
+  for (uint32_t probe = 0; probe <= mask; ++probe) {
+    const uint4 e = __ldg(reinterpret_cast<const uint4*>(v.table + s));
+    const unsigned long long k = ((unsigned long long)e.y << 32) | e.x;
+    if (k == key) return ((unsigned long long)e.z << 32) | e.w;
+    if (k == EMPTY_KEY) break;
+    s = (s + 1u) & mask;
+  }
+  return ~0ull;
+}
+
+__device__ __forceinline__ uint32_t kr_rank(unsigned long long kr) { return (uint32_t)(kr >> 32); }
+__device__ __forceinline__ uint32_t kr_result(unsigned long long kr) { return (uint32_t)kr; }
+
+// Strict UTF-8 (RFC 3629, Section 4): length of the well-formed sequence at
+// s[0..avail), or 0 if it is malformed or truncated.  *cp receives the value.
+__device__ __forceinline__ int utf8_decode(const uint8_t* s, int avail, uint32_t* cp) {
+  const uint32_t b0 = s[0];
+  if (b0 < 0x80u) { *cp = b0; return 1; }
+  int need;
+  uint32_t lo = 0x80u, hi = 0xBFu;
+  if (b0 >= 0xC2u && b0 <= 0xDFu) need = 1;
+  else if (b0 == 0xE0u) { need = 2; lo = 0xA0u; }
+  else if ((b0 >= 0xE1u && b0 <= 0xECu) || b0 == 0xEEu || b0 == 0xEFu) need = 2;
+  else if (b0 == 0xEDu) { need = 2; hi = 0x9Fu; }
+  else if (b0 == 0xF0u) { need = 3; lo = 0x90u; }
+  else if (b0 >= 0xF1u && b0 <= 0xF3u) need = 3;
+  else if (b0 == 0xF4u) { need = 3; hi = 0x8Fu; }
+  else return 0;
+  if (need >= avail) return 0;
+  const uint32_t b1 = s[1];
+  if (b1 < lo || b1 > hi) return 0;
+  uint32_t v = (b0 & (0x7Fu >> (need + 1))) << 6 | (b1 & 0x3Fu);
+  for (int k = 2; k <= need; ++k) {
+    const uint32_t bk = s[k];
+    if ((bk & 0xC0u) != 0x80u) return 0;
+    v = (v << 6) | (bk & 0x3Fu);
+  }
+  *cp = v;
+  return need + 1;
+}
+#endif
+
+// host-side launchers (defined in the kernel translation units)
+void launch_run_summary(const Call& c, const Workspace& w, cudaStream_t s);
+void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
+void launch_bpe_short(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
+void launch_bpe_med(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
+void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
+void launch_emit(const Call& c, const Workspace& w, cudaStream_t s);
+void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);
+
+__host__ __device__ inline long long n_chunks(long long n) { return (n + CHUNK - 1) / CHUNK; }
+
+}  // namespace tokgb

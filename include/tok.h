@@ -1,0 +1,167 @@
+/*
+ * tok.h -- C ABI of the GB300 exact byte-level BPE tokenizer.
+ *
+ * The operation is the fresh-session GPU path of "TokTier: exact stateful
+ * tokenization for agentic LLM serving" (Section 4, "exact GPU
+ * tokenization"): bytes in, token ids out, identical to the serial reference
+ * tokenizer.  The tokenizer is the two-stage map F = E* . G of Appendix A.1:
+ * G splits the UTF-8 text into fragments with a GPT-style pre-tokenizer
+ * regex (Section 4.1 recasts that serial regex as a parallel decomposition
+ * into runs of letter / digit / whitespace / other code points), then E
+ * encodes every fragment on its own with BPE merges in rank order (Section
+ * 4.2).  No normaliser, special tokens, truncation or dropout (the
+ * assumptions of Appendix A.1).  Output is an id array only, no byte offsets
+ * (Section 4.4).  Section 4.3 packages the whole bytes -> ids chain with
+ * pre-bucketed buffers so a request needs two host synchronisations; the
+ * host entry points below follow that shape.
+ *
+ * Conventions for every function:
+ *   - Return 0 (TOK_OK) or a negative TOK_E* code.  Nothing traps or aborts.
+ *   - A handle is not reentrant: calls on one handle must not overlap.
+ *   - "host" pointers are ordinary CPU memory (pageable or pinned); "device"
+ *     pointers are CUDA global memory of the handle's device.
+ *   - The library copies everything tok_load is given; all other buffers are
+ *     borrowed for the duration of the call only.
+ *   - Outputs are undefined when a call fails; tok_last_error() says why.
+ */
+#ifndef TOK_H
+#define TOK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tok_handle tok_handle;
+
+enum {
+  TOK_OK = 0,
+  TOK_EINVAL = -1,   /* bad argument (null pointer, bad pattern id, ...)      */
+  TOK_EUTF8 = -2,    /* input is not well-formed UTF-8 (RFC 3629)             */
+  TOK_ENOMEM = -3,   /* a device or pinned host allocation failed             */
+  TOK_ECUDA = -4,    /* a CUDA runtime call failed                            */
+  TOK_EBUF = -5,     /* the output buffer is too small                        */
+  TOK_ETIMEOUT = -6, /* a bounded device-side wait gave up (no hang)          */
+  TOK_EMERGES = -7   /* vocabulary / merges failed validation                 */
+};
+
+/* Pre-tokenizer patterns.  The pages name the cl100k / o200k / DeepSeek
+ * families (Section 4.1) without printing them; these are the GPT-2 pattern
+ * and the cl100k-style pattern:
+ *   GPT-2:  's|'t|'re|'ve|'m|'ll|'d| ?\p{L}+| ?\p{N}+| ?[^\s\p{L}\p{N}]+|\s+(?!\S)|\s+
+ *   cl100k: (?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\r\n\p{L}\p{N}]?\p{L}+|\p{N}{1,3}
+ *           | ?[^\s\p{L}\p{N}]+[\r\n]*|\s*[\r\n]+|\s+(?!\S)|\s+                */
+enum { TOK_PAT_GPT2 = 0, TOK_PAT_CL100K_STYLE = 1 };
+
+/* tok_load -- build a tokenizer on the current CUDA device.
+ *
+ * vocab_bytes / vocab_off: token t has bytes vocab_bytes[vocab_off[t] ..
+ *   vocab_off[t+1]) (host, n_vocab+1 offsets).  Each of the 256 single bytes
+ *   must be exactly one token; no two tokens may have equal bytes; tokens are
+ *   at most 65535 bytes; n_vocab < 2^20.
+ * merges: host array of n_merges (left_id, right_id) pairs in rank order
+ *   (rank = index).  The result of a merge is the token whose bytes are
+ *   bytes(left) || bytes(right); it must exist.  No pair may repeat.
+ *   (Section 4.2: BPE merges applied lowest rank first.)
+ * pattern_id: TOK_PAT_GPT2 or TOK_PAT_CL100K_STYLE.
+ * out: receives the handle; free it with tok_free.
+ * Errors: TOK_EINVAL, TOK_EMERGES (validation, message in tok_last_error(NULL)),
+ *   TOK_ENOMEM, TOK_ECUDA.
+ */
+int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_vocab,
+             const uint32_t* merges, uint32_t n_merges, int pattern_id, tok_handle** out);
+
+/* tok_encode -- encode one text (host in, host out), Section 4.3's request:
+ * copies text[0..len) to the device, runs the whole bytes -> ids chain on the
+ * handle's stream and copies the ids back.
+ * ids: host array of capacity cap.  cap >= len always suffices (a token has
+ *   at least one byte).  *n_ids receives the number of ids.
+ * Errors: TOK_EUTF8 (tok_error_offset() = offset of the first malformed
+ *   byte sequence), TOK_EBUF (*n_ids = the required capacity), TOK_ECUDA,
+ *   TOK_ENOMEM, TOK_ETIMEOUT.  Empty input gives 0 ids.
+ */
+int tok_encode(tok_handle* h, const uint8_t* text, uint64_t len,
+               int32_t* ids, uint64_t cap, uint64_t* n_ids);
+
+/* tok_encode_batch -- encode n independent texts in one pass (host in, host
+ * out).  Item k is texts[k][0..lens[k]); items never interact: every item
+ * starts and ends a fragment exactly as a separate tok_encode call would.
+ * ids: host array of capacity cap (cap >= sum(lens) suffices), filled with
+ *   the items' ids back to back; item_off: host array of n+1 entries, item k's
+ *   ids are ids[item_off[k] .. item_off[k+1]).
+ * Errors: as tok_encode; TOK_EUTF8 reports the offset within the
+ *   concatenation of all items.
+ */
+int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t* lens, uint32_t n,
+                     int32_t* ids, uint64_t cap, uint64_t* item_off);
+
+/* tok_encode_device -- the same chain on device-resident buffers, enqueued on
+ * `stream` (a cudaStream_t; NULL = the handle's own stream) without any host
+ * synchronisation.
+ * d_text: device, len bytes.  d_ids: device, cap >= len int32 (required).
+ * d_status: device int64[4], written when the chain finishes:
+ *   [0] = TOK_OK or a negative code, [1] = number of ids,
+ *   [2] = offset of the first malformed UTF-8 sequence (or -1), [3] = reserved.
+ * Returns TOK_EINVAL / TOK_EBUF / TOK_ENOMEM / TOK_ECUDA for launch-time
+ * problems; data-dependent errors appear in d_status only.
+ */
+int tok_encode_device(tok_handle* h, const uint8_t* d_text, uint64_t len,
+                      int32_t* d_ids, uint64_t cap, int64_t* d_status, void* stream);
+
+/* tok_encode_batch_device -- device-resident batch.  d_text holds the items
+ * back to back; d_item_start (device, n+1 int64) gives item k's bytes as
+ * d_text[d_item_start[k] .. d_item_start[k+1]), with d_item_start[0] == 0
+ * and d_item_start[n] == total length.  d_item_off (device, n+1 int64)
+ * receives the id offsets of the items; d_status as tok_encode_device.
+ * total = d_item_start[n] must be passed as `len` (host value).
+ */
+int tok_encode_batch_device(tok_handle* h, const uint8_t* d_text, uint64_t len,
+                            const int64_t* d_item_start, uint32_t n, int32_t* d_ids, uint64_t cap,
+                            int64_t* d_item_off, int64_t* d_status, void* stream);
+
+/* tok_pretokenize -- the pre-tokenizer G alone (Section 4.1): writes the byte
+ * offset of every fragment start of text[0..len) (host in, host out) to
+ * starts (capacity cap; cap >= len suffices) and the count to *n.
+ * Errors: as tok_encode.
+ */
+int tok_pretokenize(tok_handle* h, const uint8_t* text, uint64_t len,
+                    int64_t* starts, uint64_t cap, uint64_t* n);
+
+/* tok_pretokenize_batch -- tok_pretokenize over n independent texts packed
+ * back to back (as tok_encode_batch packs them); starts are byte offsets into
+ * that concatenation.  Every item starts a fragment. */
+int tok_pretokenize_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t* lens, uint32_t n,
+                          int64_t* starts, uint64_t cap, uint64_t* n_starts);
+
+/* tok_last_error -- message of the last failure on h (or of the last failed
+ * tok_load when h is NULL).  The string is owned by the library and valid
+ * until the next call on h. */
+const char* tok_last_error(tok_handle* h);
+
+/* tok_error_offset -- byte offset of the first malformed UTF-8 sequence seen
+ * by the last host-side call on h that returned TOK_EUTF8, else -1. */
+int64_t tok_error_offset(tok_handle* h);
+
+/* tok_content_hash -- 64-bit FNV-1a hash over the pattern id, the token bytes
+ * and the merges (Section 3.1: tokenizers are registered by content hash). */
+uint64_t tok_content_hash(tok_handle* h);
+
+/* tok_stage_times -- per-kernel device times of the most recent call made
+ * with timing enabled (tok_set_timing).  Writes up to cap entries of
+ * milliseconds to ms and the matching kernel names (static strings) to names;
+ * returns the number of entries, or a negative code. */
+int tok_set_timing(tok_handle* h, int enable);
+int tok_stage_times(tok_handle* h, float* ms, const char** names, int cap);
+
+/* tok_launch_count -- number of kernels this handle has launched so far. */
+uint64_t tok_launch_count(tok_handle* h);
+
+/* tok_free -- release the handle and its device memory.  NULL is ignored. */
+void tok_free(tok_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOK_H */

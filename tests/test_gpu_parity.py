@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA library through its C ABI against the oracle.
+
+Integer work, so the bar is bit-exact: every fragment start and every token
+id must equal the oracle's.  Full-size comparisons where the oracle finishes
+in seconds (the 16 KiB, 1 MiB and 1M-character workloads); at the batch and
+adversarial sizes, every fragment start of a scaled copy plus the full-size
+text's round trip, fixpoint property and a sample of fragments re-encoded by
+the oracle."""
+import itertools
+import os
+import random
+
+import numpy as np
+import pytest
+
+import textgen
+from oracle.bpe import bpe_heap
+from oracle.encode import decode, encode, pretoken_byte_spans
+from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2
+from oracle.utf8 import Utf8Error
+from oracle.vocab import Vocab
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+VOC = os.path.join(ROOT, "data", "vocabs")
+
+ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ"
+
+
+@pytest.fixture(scope="session")
+def pkg():
+    from exact_bpe_tokenization_utf_gb300 import _build
+    _build.build()
+    import exact_bpe_tokenization_utf_gb300 as p
+    return p
+
+
+_cache = {}
+
+
+def pair(pkg, name, pattern):
+    """(oracle vocabulary, GPU tokenizer) for a committed vocabulary."""
+    key = (name, pattern)
+    if key not in _cache:
+        path = os.path.join(VOC, name + ".merges")
+        if not os.path.exists(path):
+            pytest.skip("vocabulary %s not built" % name)
+        _cache[key] = (Vocab.load_merges(path), pkg.Tokenizer.from_merges_file(path, pattern))
+    return _cache[key]
+
+
+def oracle_starts(data, pattern):
+    return [a for a, _ in pretoken_byte_spans(data, pattern)]
+
+
+# --- pre-tokenizer ----------------------------------------------------------
+
+@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+def test_pretokenize_brute_force(pkg, pattern):
+    tok = pkg.Tokenizer.from_merges([], pattern)
+    items = ["".join(t) for n in range(1, 4) for t in itertools.product(ALPHABET, repeat=n)]
+    rnd = random.Random(pattern)
+    items += ["".join(rnd.choice(ALPHABET) for _ in range(rnd.randint(4, 40))) for _ in range(4000)]
+    enc = [s.encode() for s in items]
+    got = tok.pretokenize_batch(enc)
+    for s, b, g in zip(items, enc, got):
+        assert g == oracle_starts(b, pattern), repr(s)
+
+
+@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+def test_pretokenize_runs_across_chunks(pkg, pattern):
+    # runs far longer than a 4 KiB chunk: whitespace, digits, letters, CR/LF
+    tok = pkg.Tokenizer.from_merges([], pattern)
+    text = textgen.adversarial(600_000, 1005, scale=0.05).encode()
+    assert list(tok.pretokenize(text)) == oracle_starts(text, pattern)
+    parts = [b"x;" + b"\n" * 9000 + b" " * 5000 + b"\n" * 3 + b"  y",
+             b"a" + b"\r\n" * 5000 + b" " * 3,
+             b"1" * 12347 + b"z" + b"2" * 8191,
+             b" " * 8192,
+             b"'s" * 3000 + b"'" + b" " * 4095 + b"'ll"]
+    for p in parts:
+        assert list(tok.pretokenize(p)) == oracle_starts(p, pattern)
+    got = tok.pretokenize_batch(parts)
+    for p, g in zip(parts, got):
+        assert g == oracle_starts(p, pattern)
+
+
+# --- whole encode at full size -------------------------------------------
+
+def test_encode_code_16k_1k_merges(pkg):
+    v, tok = pair(pkg, "gpt2_code_1k", PATTERN_GPT2)
+    data = textgen.code_ascii(16384, 1001).encode()
+    assert tok.encode(data).tolist() == encode(data, v, PATTERN_GPT2)
+
+
+def test_encode_mixed_1mib_50k_merges(pkg):
+    v, tok = pair(pkg, "gpt2_mixed_50k", PATTERN_GPT2)
+    data = textgen.mixed_c2(1 << 20, 1002).encode()
+    assert tok.encode(data).tolist() == encode(data, v, PATTERN_GPT2)
+
+
+def test_encode_session_1m_chars_100k_merges(pkg):
+    v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
+    data = textgen.agentic_session(1_000_000, 1003).encode()
+    assert tok.encode(data).tolist() == encode(data, v, PATTERN_CL100K)
+
+
+# --- batch ---------------------------------------------------------------
+
+def _token_starts(ids, v):
+    lens = np.array([len(v.token_bytes[i]) for i in ids], dtype=np.int64)
+    return np.concatenate([[0], np.cumsum(lens)])
+
+
+def test_encode_batch_64_sessions(pkg):
+    v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
+    items = [s.encode() for s in textgen.session_batch(64, 1004)]
+    ids, off = tok.encode_batch(items)
+    assert off[0] == 0 and off[-1] == len(ids) and np.all(np.diff(off) >= 0)
+    rnd = random.Random(4)
+    order = sorted(range(64), key=lambda k: len(items[k]))
+    check = set(order[:8]) | set(rnd.sample(range(64), 3))
+    for k, it in enumerate(items):
+        got = ids[off[k]:off[k + 1]].tolist()
+        assert decode(got, v) == it
+        if k in check:
+            assert got == encode(it, v, PATTERN_CL100K), k
+    # batch == singles
+    for k in list(check)[:4]:
+        assert tok.encode(items[k]).tolist() == ids[off[k]:off[k + 1]].tolist()
+
+
+# --- adversarial ---------------------------------------------------------
+
+@pytest.mark.parametrize("name,pattern", [("gpt2_session_100k", PATTERN_GPT2),
+                                          ("cl100k_session_100k", PATTERN_CL100K)])
+def test_adversarial_scaled_exact(pkg, name, pattern):
+    v, tok = pair(pkg, name, pattern)
+    data = textgen.adversarial(400_000, 1005, scale=0.02).encode()
+    assert tok.encode(data).tolist() == encode(data, v, pattern)
+    pieces = [p.encode() for p in textgen.adversarial_pieces(1005, scale=0.02)]
+    ids, off = tok.encode_batch(pieces)
+    for k, p in enumerate(pieces):
+        assert ids[off[k]:off[k + 1]].tolist() == encode(p, v, pattern), k
+
+
+@pytest.mark.parametrize("name,pattern", [("gpt2_session_100k", PATTERN_GPT2),
+                                          ("cl100k_session_100k", PATTERN_CL100K)])
+def test_adversarial_8mib_sampled(pkg, name, pattern):
+    v, tok = pair(pkg, name, pattern)
+    data = textgen.adversarial(8 << 20, 1005).encode()
+    ids = tok.encode(data).tolist()
+    assert decode(ids, v) == data
+    starts = tok.pretokenize(data)
+    ends = np.append(starts[1:], len(data))
+    tstart = _token_starts(ids, v)
+    pos = {int(p): k for k, p in enumerate(tstart)}
+    # every fragment start is a token start; a fragment's tokens are BPE(fragment)
+    lens = ends - starts
+    rnd = random.Random(pattern)
+    idx = set(np.argsort(lens)[-6:].tolist()) | set(rnd.sample(range(len(starts)), 300))
+    for k in idx:
+        a, b = int(starts[k]), int(ends[k])
+        assert a in pos and b in pos
+        got = ids[pos[a]:pos[b]]
+        want = bpe_heap([v.byte_id[x] for x in data[a:b]], v.merge_map)
+        assert got == want, (k, a, b)
+
+
+# --- edge cases ------------------------------------------------------------
+
+def test_empty_and_tiny(pkg):
+    v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
+    assert tok.encode(b"").tolist() == []
+    for b in range(128):
+        d = bytes([b])
+        assert tok.encode(d).tolist() == encode(d, v, PATTERN_CL100K)
+    ids, off = tok.encode_batch([b"", b"a", b"", b" ", b""])
+    assert off.tolist() == [0, 0, 1, 1, 2, 2]
+
+
+@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+def test_ragged_sizes_and_tier_edges(pkg, pattern):
+    name = "gpt2_session_100k" if pattern == PATTERN_GPT2 else "cl100k_session_100k"
+    v, tok = pair(pkg, name, pattern)
+    base = textgen.agentic_session_bytes(20000, 77).encode()
+    for n in (1, 15, 16, 17, 255, 256, 257, 1023, 1024, 1025, 4095, 4096, 4097, 8191, 8193, 12289):
+        d = base[:n]
+        while d and (d[-1] & 0xC0) == 0x80:
+            d = d[:-1]
+        assert tok.encode(d).tolist() == encode(d, v, pattern), n
+    rnd = random.Random(5)
+    for n in (16, 17, 255, 256, 257, 300, 1000, 5000, 20000):
+        for alpha in ("abcdefghij", "0123456789", "=", " ", "ab"):
+            d = ("x " + "".join(rnd.choice(alpha) for _ in range(n)) + " y").encode()
+            assert tok.encode(d).tolist() == encode(d, v, pattern), (n, alpha)
+
+
+def test_invalid_utf8_offsets(pkg):
+    _, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
+    cases = [b"abc\xe4\xb8", b"\x80abc", b"ab\xc0\xafcd", b"x\xed\xa0\x80y", b"\xf4\x90\x80\x80", b"ok \xff",
+             b"a" * 5000 + b"\xe2\x82", b"a" * 4094 + b"\xe4\xb8\xad\x80" + b"b" * 10]
+    for d in cases:
+        with pytest.raises(Utf8Error) as ref:
+            encode(d, Vocab.from_merges([]), 0)
+        with pytest.raises(pkg.TokError) as e:
+            tok.encode(d)
+        assert e.value.code == pkg.TOK_EUTF8 and e.value.offset == ref.value.offset, d[:20]
+    # batch items are validated on their own: a sequence may not span items
+    with pytest.raises(pkg.TokError) as e:
+        tok.encode_batch([b"ab\xe4\xb8", b"\xadcd"])
+    assert e.value.code == pkg.TOK_EUTF8 and e.value.offset == 2
+
+
+def test_non_monotone_vocabulary_falls_back_exactly(pkg):
+    # "abc" is made by (ab,c) at rank 1 and again by (a,bc) at rank 4, after
+    # (abc,d) used it at rank 2: merges can create lower-rank pairs
+    toks = [bytes([b]) for b in range(256)] + [b"ab", b"abc", b"abcd", b"bc", b"cd", b"dd"]
+    ix = {t: i for i, t in enumerate(toks)}
+    merges = [(ix[b"a"], ix[b"b"]), (ix[b"ab"], ix[b"c"]), (ix[b"abc"], ix[b"d"]), (ix[b"b"], ix[b"c"]),
+              (ix[b"a"], ix[b"bc"]), (ix[b"c"], ix[b"d"]), (ix[b"d"], ix[b"d"])]
+    v = Vocab(toks, merges)
+    assert not v.monotone()
+    tok = pkg.Tokenizer(toks, merges, PATTERN_GPT2)
+    rnd = random.Random(6)
+    words = ["".join(rnd.choice("abcd") for _ in range(n)) for n in (3, 10, 16, 17, 40, 200, 256, 300, 2000)]
+    data = " ".join(words).encode()
+    assert tok.encode(data).tolist() == encode(data, v, PATTERN_GPT2)
+
+
+def test_device_entry_points(pkg):
+    import torch
+    v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
+    data = textgen.agentic_session(200_000, 11).encode()
+    want = tok.encode(data)
+    d_text = torch.frombuffer(bytearray(data), dtype=torch.uint8).cuda()
+    d_ids = torch.empty(len(data), dtype=torch.int32, device="cuda")
+    d_st = torch.zeros(4, dtype=torch.int64, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    tok.encode_device(d_text.data_ptr(), len(data), d_ids.data_ptr(), len(data), d_st.data_ptr(), stream)
+    torch.cuda.synchronize()
+    st = d_st.cpu().tolist()
+    assert st[0] == 0 and st[2] == -1
+    assert d_ids[:st[1]].cpu().numpy().tolist() == want.tolist()
+    # batch on the device
+    items = [data[:5000], data[5000:5000], data[5000:70001], data[70001:]]
+    items = [it for it in items]
+    starts = np.cumsum([0] + [len(x) for x in items]).astype(np.int64)
+    d_items = torch.from_numpy(starts).cuda()
+    d_off = torch.zeros(len(items) + 1, dtype=torch.int64, device="cuda")
+    tok.encode_batch_device(d_text.data_ptr(), len(data), d_items.data_ptr(), len(items), d_ids.data_ptr(),
+                            len(data), d_off.data_ptr(), d_st.data_ptr(), stream)
+    torch.cuda.synchronize()
+    ids_h, off_h = tok.encode_batch(items)
+    assert d_off.cpu().tolist() == off_h.tolist()
+    assert d_ids[:int(off_h[-1])].cpu().numpy().tolist() == ids_h.tolist()
