@@ -223,8 +223,10 @@ class Tokenizer:
 
     # --- device in, device out (torch tensors or raw pointers) ---------
     def encode_device(self, d_text, n_bytes, d_ids, cap, d_status, stream=0):
-        """Enqueue an encode of device bytes; no host sync.  Pointers are ints
-        (e.g. tensor.data_ptr()); d_status is a device int64[4]."""
+        """Enqueue an encode of device bytes on `stream` (a cudaStream_t as an
+        int, e.g. torch.cuda.current_stream().cuda_stream; 0 = the default
+        stream); no host sync.  Pointers are ints (e.g. tensor.data_ptr());
+        d_status is a device int64[4]."""
         self._check(self._L.tok_encode_device(self._h, d_text, n_bytes, d_ids, cap, d_status, stream or None))
 
     def encode_batch_device(self, d_text, n_bytes, d_item_start, n_items, d_ids, cap, d_item_off, d_status,

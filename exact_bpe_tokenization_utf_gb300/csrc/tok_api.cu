@@ -477,7 +477,7 @@ int tok_encode_device(tok_handle* h, const uint8_t* d_text, uint64_t len, int32_
   DeviceGuard g(h->dev);
   int rc = ensure_workspace(h, len);
   if (rc) return rc;
-  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : h->stream;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);  // NULL: the CUDA default stream
   Call c = base_call(h, d_text, len);
   c.out = d_ids;
   c.user_status = reinterpret_cast<long long*>(d_status);
@@ -493,7 +493,7 @@ int tok_encode_batch_device(tok_handle* h, const uint8_t* d_text, uint64_t len, 
   DeviceGuard g(h->dev);
   int rc = ensure_workspace(h, len);
   if (rc) return rc;
-  cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : h->stream;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);  // NULL: the CUDA default stream
   Call c = base_call(h, d_text, len);
   c.item = reinterpret_cast<const long long*>(d_item_start);
   c.n_items = (int)n;

@@ -97,8 +97,8 @@ int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t*
                      int32_t* ids, uint64_t cap, uint64_t* item_off);
 
 /* tok_encode_device -- the same chain on device-resident buffers, enqueued on
- * `stream` (a cudaStream_t; NULL = the handle's own stream) without any host
- * synchronisation.
+ * `stream` (a cudaStream_t of the handle's device; NULL = the CUDA default
+ * stream) without any host synchronisation.
  * d_text: device, len bytes.  d_ids: device, cap >= len int32 (required).
  * d_status: device int64[4], written when the chain finishes:
  *   [0] = TOK_OK or a negative code, [1] = number of ids,
