@@ -33,7 +33,7 @@ _NAMES = {0: "TOK_OK", -1: "TOK_EINVAL", -2: "TOK_EUTF8", -3: "TOK_ENOMEM", -4: 
 # every symbol include/tok.h declares
 SYMBOLS = ["tok_load", "tok_encode", "tok_encode_batch", "tok_encode_device", "tok_encode_batch_device",
            "tok_pretokenize", "tok_pretokenize_batch", "tok_last_error", "tok_error_offset", "tok_content_hash", "tok_set_timing",
-           "tok_stage_times", "tok_launch_count", "tok_free"]
+           "tok_stage_times", "tok_launch_count", "tok_free", "tok_pretokenize_device_noalloc"]
 
 
 class TokError(RuntimeError):
@@ -67,6 +67,8 @@ def lib():
     L.tok_encode_batch_device.argtypes = [P, P, U64, P, U32, P, U64, P, P, P]
     L.tok_pretokenize.argtypes = [P, U8P, U64, I64P, U64, U64P]
     L.tok_pretokenize_batch.argtypes = [P, ctypes.POINTER(U8P), U64P, U32, I64P, U64, U64P]
+    L.tok_pretokenize_device_noalloc.argtypes = [ctypes.c_int, P, U64, P, P, P]
+    L.tok_pretokenize_device_noalloc.restype = ctypes.c_int
     L.tok_last_error.argtypes = [P]
     L.tok_last_error.restype = ctypes.c_char_p
     L.tok_error_offset.argtypes = [P]

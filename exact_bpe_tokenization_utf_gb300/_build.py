@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libtokgb.so")
-SOURCES = ["tok_pretok.cu", "tok_bpe.cu", "tok_emit.cu", "tok_api.cu"]
+SOURCES = ["tok_pretok.cu", "tok_bpe.cu", "tok_emit.cu", "tok_api.cu", "tok_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 

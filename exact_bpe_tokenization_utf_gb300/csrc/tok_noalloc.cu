@@ -1,0 +1,89 @@
+// tok_pretokenize_device_noalloc: the pre-tokenizer for callers that cannot
+// allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all: code that runs inside another
+// framework's memory pool or arena (where a stray cudaMalloc fragments or
+// breaks the pool's accounting), code that must not synchronise the device
+// (cudaMalloc/cudaFree can serialise with in-flight work), and hosts that run
+// with a fixed, pre-reserved memory budget.  This entry point takes device
+// input and output buffers from the caller and keeps the only scratch it
+// needs (the per-chunk run-state summaries and a status block) in a
+// file-scope __device__ array of fixed size, which every GPU that loads the
+// library holds until the process exits.
+#include "../../include/tok.h"
+#include "tok_common.cuh"
+
+using namespace tokgb;
+
+namespace {
+
+// Longest text one call accepts (64 MiB); the scratch holds one summary word
+// per pre-tokenizer chunk of that text plus the status block.
+constexpr uint64_t kNoAllocMaxBytes = 64ull << 20;
+constexpr uint64_t kNoAllocSummaryWords = kNoAllocMaxBytes / CHUNK + 2;
+
+struct NoAllocScratch {
+  DevStatus st;
+  uint32_t csum[kNoAllocSummaryWords];
+};
+
+static __device__ __align__(256) NoAllocScratch g_noalloc_scratch;
+
+// Host-side stand-in for g_noalloc_scratch is not a device address: the
+// device address is looked up once per device with cudaGetSymbolAddress.
+constexpr int kMaxDevices = 64;
+NoAllocScratch* g_scratch_addr[kMaxDevices] = {};
+
+__global__ void k_noalloc_status(const NoAllocScratch* s, long long* d_status) {
+  const unsigned long long eo = s->st.err_off;
+  d_status[0] = eo != ~0ull ? TOK_EUTF8 : TOK_OK;
+  d_status[1] = eo != ~0ull ? (long long)eo : -1;
+}
+
+}  // namespace
+
+extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_text, uint64_t len,
+                                              uint32_t* d_start_bits, int64_t* d_status, void* stream) {
+  if (pattern_id != TOK_PAT_GPT2 && pattern_id != TOK_PAT_CL100K_STYLE) return TOK_EINVAL;
+  if (!d_status || (len && (!d_text || !d_start_bits))) return TOK_EINVAL;
+  if (len > kNoAllocMaxBytes) return TOK_EBUF;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TOK_ECUDA;
+  if (!g_scratch_addr[dev]) {
+    // once per device, with that device current; the first call on a device
+    // should therefore come before any stream capture
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return TOK_ECUDA;
+    }
+    g_scratch_addr[dev] = static_cast<NoAllocScratch*>(p);
+  }
+  NoAllocScratch* scratch = g_scratch_addr[dev];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Workspace w{};
+  w.csum = scratch->csum;
+  w.st = &scratch->st;
+  w.pstart = d_start_bits;
+  Call c{};
+  c.text = d_text;
+  c.n = (long long)len;
+  c.item = nullptr;
+  c.n_items = 1;
+  c.pattern = pattern_id;
+  c.epoch = 1;
+  if (len) {
+    // the summary kernel also resets the status block before anything reads it
+    launch_run_summary(c, w, s);
+    launch_boundaries(c, w, s);
+    k_noalloc_status<<<1, 1, 0, s>>>(scratch, reinterpret_cast<long long*>(d_status));
+  } else {
+    const long long ok[2] = {TOK_OK, -1};
+    if (cudaMemcpyAsync(d_status, ok, sizeof ok, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+      cudaGetLastError();
+      return TOK_ECUDA;
+    }
+    if (cudaStreamSynchronize(s) != cudaSuccess) return TOK_ECUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? TOK_OK : TOK_ECUDA;
+}

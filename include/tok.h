@@ -134,6 +134,32 @@ int tok_pretokenize(tok_handle* h, const uint8_t* text, uint64_t len,
 int tok_pretokenize_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t* lens, uint32_t n,
                           int64_t* starts, uint64_t cap, uint64_t* n_starts);
 
+/* tok_pretokenize_device_noalloc -- the pre-tokenizer G on device buffers for
+ * callers that cannot allocate device memory (code inside another framework's
+ * memory pool or arena, code that must not trigger the device-wide
+ * synchronisation cudaMalloc/cudaFree can cause, hosts with a fixed memory
+ * budget).  The paper has no counterpart: it is an integration entry point of
+ * this library, not a step of the method.
+ * Needs no handle and allocates nothing: its scratch (per-chunk run-state
+ * summaries and a status block) lives in a fixed __device__ array of this
+ * library that every GPU loading it holds until exit, sized for texts of at
+ * most 64 MiB; longer texts return TOK_EBUF.  The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress, with the device
+ * current); make that first call before any stream capture.
+ * d_text: device, len bytes.  d_start_bits: device uint32 words, at least
+ *   ceil(len / 4096) * 128 of them; bit p % 32 of word p / 32 is set iff a
+ *   fragment starts at byte p (bits at p >= len are 0).
+ * d_status: device int64[2]: [0] = TOK_OK or TOK_EUTF8, [1] = offset of the
+ *   first malformed UTF-8 sequence or -1.
+ * Enqueued on `stream` (NULL = the CUDA default stream) with no host sync.
+ * Every call shares the one scratch array: calls that overlap on the GPU (on
+ * different streams or devices' shared contexts) race and must be serialised
+ * by the caller.
+ * Errors: TOK_EINVAL, TOK_EBUF (len > 64 MiB), TOK_ECUDA.
+ */
+int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_text, uint64_t len,
+                                   uint32_t* d_start_bits, int64_t* d_status, void* stream);
+
 /* tok_last_error -- message of the last failure on h (or of the last failed
  * tok_load when h is NULL).  The string is owned by the library and valid
  * until the next call on h. */
