@@ -21,9 +21,8 @@ using namespace tokgb;
 
 namespace {
 
-constexpr int N_STAGES = 6;
-const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_bpe_short",
-                                     "k_bpe_med",     "k_bpe_long",   "k_emit"};
+constexpr int N_STAGES = 5;
+const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_bpe_chunk", "k_bpe_long", "k_emit"};
 
 thread_local std::string g_load_error;
 
@@ -104,9 +103,9 @@ cudaError_t dalloc(T** p, size_t count) {
 
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
-  void* ptrs[] = {w.text, w.csum, w.pstart, w.tstart, w.sid, w.medq, w.longq, w.lb, w.st,
-                  w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1], w.e_kr[0], w.e_kr[1], w.e_fl, w.e_rs,
-                  h->d_out};
+  void* ptrs[] = {w.text, w.csum, w.pstart, w.tok, w.cm_first, w.cm_count, w.cm_long, w.cm_long_count,
+                  w.longq, w.lb, w.st, w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1], w.e_kr[0], w.e_kr[1],
+                  w.e_fl, w.e_rs, h->d_out};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   w = Workspace{};
@@ -127,10 +126,12 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.text, cap + pad));
   chk(dalloc(&w.csum, nch + 2));
   chk(dalloc(&w.pstart, cap / 32 + pad));
-  chk(dalloc(&w.tstart, cap + pad));
-  chk(dalloc(&w.sid, cap + pad));
-  chk(dalloc(&w.medq, cap / (SHORT_MAX + 1) + pad));
-  chk(dalloc(&w.longq, cap / (MED_MAX + 1) + cap / BPE_CHUNK + pad));
+  chk(dalloc(&w.tok, cap + pad));
+  chk(dalloc(&w.cm_first, nch + 2));
+  chk(dalloc(&w.cm_count, nch + 2));
+  chk(dalloc(&w.cm_long, nch + 2));
+  chk(dalloc(&w.cm_long_count, nch + 2));
+  chk(dalloc(&w.longq, nch + 2));
   chk(dalloc(&w.lb, nch + 2));
   chk(dalloc(&w.st, 1));
   for (int b = 0; b < 2; ++b) {
@@ -188,14 +189,12 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
     if (tm) cudaEventRecord(h->ev[1], s);
     launch_boundaries(c, h->ws, s);
     if (tm) cudaEventRecord(h->ev[2], s);
-    launch_bpe_short(c, h->ws, h->v, s);
+    launch_bpe_chunk(c, h->ws, h->v, s);
     if (tm) cudaEventRecord(h->ev[3], s);
-    launch_bpe_med(c, h->ws, h->v, h->n_sms, s);
-    if (tm) cudaEventRecord(h->ev[4], s);
     launch_bpe_long(c, h->ws, h->v, h->n_sms, s);
-    if (tm) cudaEventRecord(h->ev[5], s);
+    if (tm) cudaEventRecord(h->ev[4], s);
     launch_emit(c, h->ws, s);
-    if (tm) cudaEventRecord(h->ev[6], s);
+    if (tm) cudaEventRecord(h->ev[5], s);
     h->launches += N_STAGES;
     h->have_times = tm;
   }
@@ -259,7 +258,7 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   for (uint32_t t = 0; t < n_vocab; ++t) {
     if (vocab_off[t + 1] < vocab_off[t]) return fail(nullptr, TOK_EMERGES, "vocab offsets not increasing");
     const uint64_t len = vocab_off[t + 1] - vocab_off[t];
-    if (len == 0 || len > 65535) return fail(nullptr, TOK_EMERGES, "token length out of range");
+    if (len == 0 || len > 32767) return fail(nullptr, TOK_EMERGES, "token length out of range");
     tok_len[t] = (uint16_t)len;
     std::string s(reinterpret_cast<const char*>(vocab_bytes + vocab_off[t]), len);
     if (!index.emplace(std::move(s), t).second) return fail(nullptr, TOK_EMERGES, "duplicate token bytes");

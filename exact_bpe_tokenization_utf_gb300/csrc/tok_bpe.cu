@@ -1,528 +1,476 @@
 // Per-fragment BPE, E ("TokTier: exact stateful tokenization for agentic LLM
 // serving", Section 4.2): every fragment is encoded on its own by merging the
 // lowest-rank adjacent pair (leftmost on ties) until no adjacent pair is a
-// merge.  The pages tier fragments by length (one thread, one warp, one
-// block); the tiers here are this library's own:
+// merge.  The pages tier fragments by length (one thread, one warp, one block
+// per fragment); here one CTA encodes all fragments of a 1 KiB chunk at once,
+// and only fragments longer than that get a CTA each.
 //
-//   thread tier (<= 16 bytes)  the rule itself, symbols in registers
-//   warp tier   (<= 256 bytes) the sweep engine below, arrays in shared memory
-//   CTA tier    (longer)       the sweep engine, arrays in global memory
-//
-// Sweep engine.  Let k be the rank of pair j = (s_j, s_{j+1}).  When every
-// merge that uses a token comes after every merge that produces it (the
-// vocabulary is "monotone", checked at load), the textbook loop merges in
-// non-decreasing rank order, and pair j is merged exactly as it stands unless
-// s_j or s_{j+1} is absorbed by a lower-rank merge first.  That can only be
+// Sweep engine.  The symbols of many fragments sit in one array; the pair
+// between two fragments is a "wall" that never merges.  Let k be the rank of
+// pair j = (s_j, s_{j+1}).  When every merge that uses a token comes after
+// every merge that produces it (the vocabulary is "monotone", checked at
+// load), the rule merges in non-decreasing rank order, and pair j is merged
+// exactly as it stands unless s_j or s_{j+1} is absorbed by a lower-rank merge
+// first.  That can only be
 //   - pair j-1 or j+1 having a lower rank now, or
 //   - a token Y grown from a lower-rank pair further left that ends at s_{j-1}
 //     and then merges with s_j, which needs |Y| <= the longest left operand of
-//     any merge with right operand s_j (and the mirror image on the right):
-//     every merge inside the window between that lower-rank pair and j must
-//     involve the growing token, so Y covers all symbols in between.
-// A pair that none of these can reach is "safe"; equal-rank pairs that
-// overlap (runs of one symbol x with the merge (x,x)) pair up from the left
-// end of the run, which must itself be safe.  Every sweep merges all safe
-// pairs at once; the leftmost minimum pair is always safe, so each sweep makes
-// progress, and the result equals the textbook loop.  For other vocabularies
-// the engine falls back to merging only the leftmost minimum pair per sweep,
-// which is the textbook loop itself.
+//     any merge whose right operand is s_j (and the mirror image on the
+//     right): every merge between that lower-rank pair and j must involve the
+//     growing token, so Y covers all symbols in between; a wall stops it.
+// A pair none of these can reach is "safe".  Equal-rank pairs that overlap
+// (runs of one symbol x with the merge (x,x)) pair up from the left end of
+// the run, which must itself be safe.  Every sweep merges all safe pairs; the
+// leftmost minimum pair of each fragment is always safe, so every sweep makes
+// progress, and the result equals the rule.  For other vocabularies a sweep
+// merges only the leftmost minimum pair of the whole array, which is the
+// rule itself applied fragment after fragment.
 #include "tok_common.cuh"
 
 namespace tokgb {
 
-constexpr unsigned long long KR_NONE = ~0ull;
-constexpr unsigned long long KR_NEED = ~0ull - 1ull;  // key to be looked up
-constexpr uint32_t SYM_MASK = 0xFFFFFu;
+// pair keys: rank << 32 | result
+constexpr uint32_t RANK_NONE = 0xFFFFFFFFu;  // not a merge (may become one when a symbol changes)
+constexpr uint32_t RANK_WALL = 0xFFFFFFFEu;  // between fragments, or past the last symbol: never merges
+constexpr uint32_t RANK_NEED = 0xFFFFFFFDu;  // to be looked up
+constexpr unsigned long long KR_WALL = (unsigned long long)RANK_WALL << 32;
+constexpr unsigned long long KR_NEED = (unsigned long long)RANK_NEED << 32;
+constexpr uint16_t LEN_MASK = 0x7FFF;        // symbol byte length; bit 15: symbol starts a fragment
+constexpr uint16_t FRAG_START = 0x8000;
 
-// ---------------------------------------------------------------------------
-// thread tier
+__device__ __forceinline__ bool mergeable(uint32_t rank) { return rank < RANK_NEED; }
 
-__device__ __forceinline__ void bpe_thread(const DevVocab& V, const int32_t* s_byte_id, const uint8_t* text,
-                                           long long a, int len, int32_t* sid, uint8_t* tstart) {
-  // s: symbol (bits 0-19) | byte length (bits 20-27); r: rank; x: result
-  uint32_t s[SHORT_MAX], r[SHORT_MAX], x[SHORT_MAX];
-#pragma unroll
-  for (int k = 0; k < SHORT_MAX; ++k) s[k] = k < len ? ((uint32_t)s_byte_id[text[a + k]] | (1u << 20)) : 0u;
-#pragma unroll
-  for (int k = 0; k < SHORT_MAX; ++k) {
-    r[k] = NO_RANK;
-    x[k] = 0;
-    if (k + 1 < len) {
-      const unsigned long long e = merge_lookup(V, s[k] & SYM_MASK, s[k + 1] & SYM_MASK);
-      r[k] = kr_rank(e);
-      x[k] = kr_result(e);
-    }
-  }
-  int m = len;
-  for (int it = 0; it < SHORT_MAX; ++it) {
-    uint32_t best = r[0];
-    int j = 0;
-#pragma unroll
-    for (int k = 1; k < SHORT_MAX - 1; ++k)
-      if (r[k] < best) { best = r[k]; j = k; }
-    if (best == NO_RANK) break;
-    uint32_t sj = 0, sj1 = 0, xj = 0;
-#pragma unroll
-    for (int k = 0; k < SHORT_MAX; ++k) {
-      if (k == j) { sj = s[k]; xj = x[k]; }
-      if (k == j + 1) sj1 = s[k];
-    }
-    const uint32_t merged = xj | ((((sj >> 20) + (sj1 >> 20))) << 20);
-#pragma unroll
-    for (int k = 0; k < SHORT_MAX; ++k) {
-      const uint32_t nxt_s = k + 1 < SHORT_MAX ? s[k + 1] : 0u;
-      const uint32_t nxt_r = k + 1 < SHORT_MAX ? r[k + 1] : NO_RANK;
-      const uint32_t nxt_x = k + 1 < SHORT_MAX ? x[k + 1] : 0u;
-      if (k == j) s[k] = merged;
-      else if (k > j) { s[k] = nxt_s; r[k] = nxt_r; x[k] = nxt_x; }
-    }
-    --m;
-    // neighbours of the new symbol
-    uint32_t left = 0, right = 0;
-#pragma unroll
-    for (int k = 0; k < SHORT_MAX; ++k) {
-      if (k == j - 1) left = s[k];
-      if (k == j + 1) right = s[k];
-    }
-    unsigned long long el = KR_NONE, er = KR_NONE;
-    if (j > 0) el = merge_lookup(V, left & SYM_MASK, merged & SYM_MASK);
-    if (j + 1 < m) er = merge_lookup(V, merged & SYM_MASK, right & SYM_MASK);
-#pragma unroll
-    for (int k = 0; k < SHORT_MAX; ++k) {
-      if (k == j - 1) { r[k] = kr_rank(el); x[k] = kr_result(el); }
-      if (k == j) { r[k] = kr_rank(er); x[k] = kr_result(er); }
-    }
-  }
-  // outputs: token id at each token's first byte, token-start flags
-  uint32_t starts = 0;
-  int off = 0;
-#pragma unroll
-  for (int k = 0; k < SHORT_MAX; ++k) {
-    if (k < m) {
-      sid[a + off] = (int32_t)(s[k] & SYM_MASK);
-      starts |= 1u << off;
-      off += (int)(s[k] >> 20);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < SHORT_MAX; ++k)
-    if (k < len) tstart[a + k] = (uint8_t)((starts >> k) & 1u);
-}
-
-// K3: enumerate the fragments that start in this CTA's 1 KiB range, encode
-// the short ones, queue the others
-__global__ void __launch_bounds__(BPE_THREADS) k_bpe_short(Call c, Workspace ws, DevVocab V) {
-  constexpr int WORDS = BPE_CHUNK / 32;
-  constexpr int EXT = MED_MAX / 32 + 2;  // words scanned past the range for the last fragment's end
-  __shared__ uint32_t words[WORDS];
-  __shared__ uint16_t starts[BPE_CHUNK + 1];
-  __shared__ int32_t s_byte_id[256];
-  __shared__ int wsum[BPE_THREADS / 32];
-  __shared__ long long s_last_end;
-  const int tid = threadIdx.x;
-  const long long r0 = (long long)blockIdx.x * BPE_CHUNK;
-  const long long r1 = min(r0 + BPE_CHUNK, c.n);
-  s_byte_id[tid] = V.byte_id[tid];
-  if (tid < WORDS) words[tid] = (r0 + tid * 32 < c.n) ? ws.pstart[(r0 >> 5) + tid] : 0u;
-  if (tid == 0) {
-    // end of the last fragment: next start at or after r1, the text end, or unknown
-    long long e = -1;
-    if (r1 >= c.n) e = c.n;
-    else {
-      for (int q = 0; q < EXT && e < 0; ++q) {
-        const long long wi = (r1 >> 5) + q;
-        if (wi * 32 >= c.n) { e = c.n; break; }
-        uint32_t wv = ws.pstart[wi];
-        if (q == 0) wv &= ~0u << (r1 & 31);
-        if (wv) e = min(wi * 32 + __ffs(wv) - 1, c.n);
-      }
-    }
-    s_last_end = e;
-  }
-  __syncthreads();
-  // positions of starts: thread t scans bits [4t, 4t+4)
-  const uint32_t nib = (words[tid >> 3] >> ((tid & 7) * 4)) & 0xFu;
-  const int cnt = __popc(nib);
-  // block exclusive sum
-  const int lane = tid & 31, warp = tid >> 5;
-  int inc = cnt;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += o;
-  }
-  if (lane == 31) wsum[warp] = inc;
-  __syncthreads();
-  int wpre = 0, total = 0;
-  for (int k = 0; k < BPE_THREADS / 32; ++k) {
-    if (k < warp) wpre += wsum[k];
-    total += wsum[k];
-  }
-  int pos = wpre + inc - cnt;
-  for (int q = 0; q < 4; ++q)
-    if ((nib >> q) & 1u) starts[pos++] = (uint16_t)(tid * 4 + q);
-  __syncthreads();
-  for (int k = tid; k < total; k += BPE_THREADS) {
-    const long long a = r0 + starts[k];
-    const long long e = (k + 1 < total) ? r0 + starts[k + 1] : s_last_end;
-    const long long len = e < 0 ? -1 : e - a;
-    if (len >= 1 && len <= SHORT_MAX) {
-      bpe_thread(V, s_byte_id, c.text, a, (int)len, ws.sid, ws.tstart);
-    } else if (len >= 1 && len <= MED_MAX) {
-      const uint32_t q = atomicAdd(&ws.st->med_count, 1u);
-      ws.medq[q] = Frag{a, len};
-    } else {
-      const uint32_t q = atomicAdd(&ws.st->long_count, 1u);
-      ws.longq[q] = Frag{a, len};
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// groups for the sweep engine
-
-struct WarpGroup {
-  __device__ int rank() const { return threadIdx.x & 31; }
-  __device__ int size() const { return 32; }
-  __device__ void sync() const { __syncwarp(); }
-  __device__ bool any(bool p) const { return __any_sync(0xffffffffu, p); }
-  __device__ int excl_sum(int v, int* total) const {
-    const int lane = threadIdx.x & 31;
-    int inc = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, inc, off);
-      if (lane >= off) inc += o;
-    }
-    *total = __shfl_sync(0xffffffffu, inc, 31);
-    return inc - v;
-  }
-  __device__ int excl_max(int v) const {
-    const int lane = threadIdx.x & 31;
-    int inc = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, inc, off);
-      if (lane >= off) inc = max(inc, o);
-    }
-    const int ex = __shfl_up_sync(0xffffffffu, inc, 1);
-    return lane == 0 ? -1 : ex;
-  }
-  __device__ unsigned long long min_u64(unsigned long long v) const {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, off);
-      v = o < v ? o : v;
-    }
-    return v;
-  }
-};
-
-// whole-CTA group; `sh` is shared scratch of at least 2 * (blockDim/32) + 2 words
-struct BlockGroup {
-  long long* sh;
-  __device__ int rank() const { return threadIdx.x; }
-  __device__ int size() const { return blockDim.x; }
-  __device__ void sync() const { __syncthreads(); }
-  __device__ bool any(bool p) const { return __syncthreads_or(p) != 0; }
-  __device__ int excl_sum(int v, int* total) const {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int inc = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, inc, off);
-      if (lane >= off) inc += o;
-    }
-    __syncthreads();
-    if (lane == 31) sh[warp] = inc;
-    __syncthreads();
-    long long pre = 0, tot = 0;
-    for (int k = 0; k < nw; ++k) {
-      if (k < warp) pre += sh[k];
-      tot += sh[k];
-    }
-    *total = (int)tot;
-    __syncthreads();
-    return (int)pre + inc - v;
-  }
-  __device__ int excl_max(int v) const {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int inc = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, inc, off);
-      if (lane >= off) inc = max(inc, o);
-    }
-    __syncthreads();
-    if (lane == 31) sh[warp] = inc;
-    __syncthreads();
-    int pre = -1;
-    for (int k = 0; k < warp; ++k) pre = max(pre, (int)sh[k]);
-    const int ex = __shfl_up_sync(0xffffffffu, inc, 1);
-    __syncthreads();
-    return lane == 0 ? pre : max(pre, ex);
-  }
-  __device__ unsigned long long min_u64(unsigned long long v) const {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, off);
-      v = o < v ? o : v;
-    }
-    __syncthreads();
-    if (lane == 0) sh[warp] = (long long)v;
-    __syncthreads();
-    unsigned long long r = ~0ull;
-    for (int k = 0; k < nw; ++k) {
-      const unsigned long long o = (unsigned long long)sh[k];
-      r = o < r ? o : r;
-    }
-    __syncthreads();
-    return r;
-  }
-};
-
-struct EngineArrays {
-  uint32_t* sym[2];
-  uint16_t* len[2];
-  unsigned long long* kr[2];
-  uint8_t* fl;   // bit 0: pair merges this sweep
-  int32_t* rs;   // start of the run of equal-rank pairs containing this pair
-};
-
-// Is pair i (rank k) safe to merge now?  See the file comment.
+// Is pair i (rank k) safe to merge now?  rs[i] is the first pair of the run
+// of equal-rank pairs that contains i.  See the file comment.
+template <class RS>
 __device__ __forceinline__ bool pair_safe(const DevVocab& V, const uint32_t* S, const uint16_t* L,
-                                          const unsigned long long* K, const int32_t* rs, int m, int i,
-                                          uint32_t k) {
-  const int u = rs[i];
-  if ((i - u) & 1) return false;  // overlapping equal pairs pair up from the run start
+                                          const unsigned long long* K, const RS* rs, int m, int i, uint32_t k) {
+  const int u = (int)rs[i];
+  if ((i - u) & 1) return false;
   if (u > 0) {
-    if (kr_rank(K[u - 1]) < k) return false;
-    const int lim = V.max_left[S[u]];
-    int cum = L[u - 1];
-    for (int q = u - 2; q >= 0; --q) {
-      cum += L[q];
-      if (cum > lim) break;
-      if (kr_rank(K[q]) < k) return false;
+    const uint32_t kl = kr_rank(K[u - 1]);
+    if (kl != RANK_WALL) {
+      if (kl < k) return false;
+      const int lim = V.max_left[S[u]];
+      int cum = L[u - 1] & LEN_MASK;
+      for (int q = u - 2; q >= 0; --q) {
+        const uint32_t kq = kr_rank(K[q]);
+        if (kq == RANK_WALL) break;
+        cum += L[q] & LEN_MASK;
+        if (cum > lim) break;
+        if (kq < k) return false;
+      }
     }
   }
   if (i + 1 < m - 1) {
-    if (kr_rank(K[i + 1]) < k) return false;
-    const int lim = V.max_right[S[i + 1]];
-    int cum = L[i + 2];
-    for (int q = i + 2; q < m - 1; ++q) {
-      cum += L[q + 1];
-      if (cum > lim) break;
-      if (kr_rank(K[q]) < k) return false;
+    const uint32_t kr = kr_rank(K[i + 1]);
+    if (kr != RANK_WALL) {
+      if (kr < k) return false;
+      const int lim = V.max_right[S[i + 1]];
+      int cum = L[i + 2] & LEN_MASK;
+      for (int q = i + 2; q < m - 1; ++q) {
+        const uint32_t kq = kr_rank(K[q]);
+        if (kq == RANK_WALL) break;
+        cum += L[q + 1] & LEN_MASK;
+        if (cum > lim) break;
+        if (kq < k) return false;
+      }
     }
   }
   return true;
 }
 
-// Encode the fragment text[a .. a+m0) with group g.  Arrays hold >= m0
-// elements.  Writes sid / tstart for the fragment's bytes.
-template <class G>
-__device__ void sweep_engine(const G& g, const DevVocab& V, const uint8_t* text, long long a, int m0,
-                             const EngineArrays& A, int32_t* sid, uint8_t* tstart, int32_t* err) {
-  const int t = g.rank(), GS = g.size();
-  int m = m0;
-  for (int i = t; i < m; i += GS) {
-    A.sym[0][i] = (uint32_t)V.byte_id[text[a + i]];
-    A.len[0][i] = 1;
+// block-wide scans for blockDim.x a multiple of 32; `sh` holds >= blockDim/32 words
+__device__ __forceinline__ int block_excl_sum(int v, int* total, int* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
   }
-  g.sync();
-  for (int i = t; i < m; i += GS)
-    A.kr[0][i] = (i + 1 < m) ? merge_lookup(V, A.sym[0][i], A.sym[0][i + 1]) : KR_NONE;
-  g.sync();
-  int cur = 0;
-  for (int sweep = 0; sweep <= m0; ++sweep) {
-    const uint32_t* S = A.sym[cur];
-    const uint16_t* L = A.len[cur];
-    const unsigned long long* K = A.kr[cur];
-    const int np = m - 1;  // pairs
-    // 1. run starts of equal-rank pairs, contiguous blocks per thread
-    const int E = (np + GS - 1) / GS;
-    const int lo = min(t * E, np), hi = min(lo + E, np);
-    int last = -1;
-    for (int i = lo; i < hi; ++i)
-      if (i == 0 || kr_rank(K[i - 1]) != kr_rank(K[i])) last = i;
-    int run = g.excl_max(last);
-    for (int i = lo; i < hi; ++i) {
-      if (i == 0 || kr_rank(K[i - 1]) != kr_rank(K[i])) run = i;
-      A.rs[i] = run;
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  int pre = 0, tot = 0;
+  for (int k = 0; k < nw; ++k) {
+    const int x = sh[k];
+    pre += k < warp ? x : 0;
+    tot += x;
+  }
+  *total = tot;
+  __syncthreads();
+  return pre + inc - v;
+}
+
+__device__ __forceinline__ int block_excl_max(int v, int* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc = max(inc, o);
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  int pre = -1;
+  for (int k = 0; k < warp; ++k) pre = max(pre, sh[k]);
+  const int ex = __shfl_up_sync(0xffffffffu, inc, 1);
+  __syncthreads();
+  return lane == 0 ? pre : max(pre, ex);
+}
+
+__device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v, unsigned long long* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = o < v ? o : v;
+  }
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  unsigned long long r = ~0ull;
+  for (int k = 0; k < nw; ++k) r = sh[k] < r ? sh[k] : r;
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ bool bit_at(const uint32_t* bits, int p) { return (bits[p >> 5] >> (p & 31)) & 1u; }
+
+// ---------------------------------------------------------------------------
+// K3: the fragments that start in one 1 KiB chunk, in shared memory
+
+struct ChunkEngine {
+  uint32_t sym[ENG_CAP];
+  unsigned long long kr[ENG_CAP];
+  uint16_t len[ENG_CAP];
+  uint16_t rs[ENG_CAP];
+  uint8_t fl[ENG_CAP];
+  uint32_t bits[ENG_CAP / 32];
+  int scan[ENG_THREADS / 32];
+  unsigned long long scan64[ENG_THREADS / 32];
+  int32_t byte_id[256];
+  long long first, end, last, longfrag;
+};
+
+__global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws, DevVocab V) {
+  __shared__ ChunkEngine E;
+  const int tid = threadIdx.x, T = ENG_THREADS;
+  const long long chunk = blockIdx.x;
+  const long long r0 = chunk * CHUNK;
+  const long long r1 = min(r0 + CHUNK, c.n);
+  const long long lim = min(r0 + ENG_CAP, c.n);
+  E.byte_id[tid] = V.byte_id[tid];
+  for (int w = tid; w < ENG_CAP / 32; w += T) {
+    const long long p = r0 + 32ll * w;
+    uint32_t v = 0;
+    if (p < lim) {
+      v = ws.pstart[(r0 >> 5) + w];
+      if (lim - p < 32) v &= (1u << (lim - p)) - 1u;
     }
-    g.sync();
-    // 2. safe pairs
-    bool any_pair = false, any_safe = false;
+    E.bits[w] = v;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // first and last fragment start in [r0, r1); first start in [r1, lim)
+    const int lane = tid;
+    const uint32_t w0 = E.bits[lane];  // CHUNK / 32 == 32 words
+    const uint32_t nz = __ballot_sync(0xffffffffu, w0 != 0u);
+    const uint32_t w1 = E.bits[32 + lane];
+    const uint32_t nz1 = __ballot_sync(0xffffffffu, w1 != 0u);
+    if (lane == 0) {
+      long long first = -1, last = -1, end = -1;
+      if (nz) {
+        const int a = __ffs(nz) - 1, b = 31 - __clz(nz);
+        first = r0 + 32ll * a + (__ffs(E.bits[a]) - 1);
+        last = r0 + 32ll * b + (31 - __clz(E.bits[b]));
+      }
+      if (r1 >= c.n) end = c.n;
+      else if (nz1) { const int a = __ffs(nz1) - 1; end = r1 + 32ll * a + (__ffs(E.bits[32 + a]) - 1); }
+      else if (lim >= c.n) end = c.n;
+      long long lf = -1;
+      if (first >= 0 && end < 0) {  // the last fragment runs past lim: queue it
+        lf = last;
+        end = last;
+        const uint32_t q = atomicAdd(&ws.st->long_count, 1u);
+        ws.longq[q] = Frag{last, chunk};
+      }
+      E.first = first;
+      E.end = end;
+      E.longfrag = lf;
+    }
+  }
+  __syncthreads();
+  const long long fs = E.first;
+  if (fs < 0) {  // no fragment starts here (the chunk lies inside a long fragment)
+    if (tid == 0) {
+      ws.cm_first[chunk] = -1;
+      ws.cm_count[chunk] = 0;
+      ws.cm_long[chunk] = -1;
+    }
+    return;
+  }
+  const int m0 = (int)(E.end - fs);
+  for (int i = tid; i < m0; i += T) {
+    const int p = (int)(fs - r0) + i;
+    E.sym[i] = (uint32_t)E.byte_id[c.text[fs + i]];
+    E.len[i] = (uint16_t)(1u | (bit_at(E.bits, p) ? FRAG_START : 0u));
+  }
+  __syncthreads();
+  for (int i = tid; i < m0; i += T)
+    E.kr[i] = (i + 1 >= m0 || (E.len[i + 1] & FRAG_START)) ? KR_WALL : merge_lookup(V, E.sym[i], E.sym[i + 1]);
+  __syncthreads();
+
+  int m = m0;
+  for (int sweep = 0; sweep <= m0; ++sweep) {
+    const int B = (m + T - 1) / T;
+    const int lo = min(tid * B, m), hi = min(lo + B, m);
+    // A: any mergeable pair left?  run starts of equal-rank pairs
+    bool anyk = false;
+    int lastrun = -1;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t k = kr_rank(E.kr[i]);
+      anyk |= mergeable(k);
+      if (i == 0 || kr_rank(E.kr[i - 1]) != k) lastrun = i;
+    }
+    if (!__syncthreads_or(anyk)) break;
+    int run = block_excl_max(lastrun, E.scan);
+    for (int i = lo; i < hi; ++i) {
+      if (i == 0 || kr_rank(E.kr[i - 1]) != kr_rank(E.kr[i])) run = i;
+      E.rs[i] = (uint16_t)run;
+    }
+    __syncthreads();
+    // B: safe pairs
     if (V.monotone) {
       for (int i = lo; i < hi; ++i) {
-        const uint32_t k = kr_rank(K[i]);
-        uint8_t f = 0;
-        if (k != NO_RANK) {
-          any_pair = true;
-          if (pair_safe(V, S, L, K, A.rs, m, i, k)) { f = 1; any_safe = true; }
-        }
-        A.fl[i] = f;
+        const uint32_t k = kr_rank(E.kr[i]);
+        E.fl[i] = (mergeable(k) && pair_safe(V, E.sym, E.len, E.kr, E.rs, m, i, k)) ? 1 : 0;
       }
     } else {
       unsigned long long best = ~0ull;
       for (int i = lo; i < hi; ++i) {
-        const uint32_t k = kr_rank(K[i]);
-        if (k != NO_RANK) {
+        const uint32_t k = kr_rank(E.kr[i]);
+        if (mergeable(k)) {
           const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
           best = key < best ? key : best;
         }
       }
-      best = g.min_u64(best);
-      any_pair = best != ~0ull;
-      any_safe = any_pair;
-      for (int i = lo; i < hi; ++i) A.fl[i] = (any_pair && (uint32_t)best == (uint32_t)i) ? 1 : 0;
+      best = block_min_u64(best, E.scan64);
+      for (int i = lo; i < hi; ++i) E.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
     }
-    if (t == 0 && m > 0) A.fl[m - 1] = 0;
-    g.sync();
-    any_pair = g.any(any_pair);
-    any_safe = g.any(any_safe);
-    if (!any_pair) break;
-    if (!any_safe) {  // cannot happen: the leftmost minimum pair is always safe
-      if (t == 0) atomicExch(err, ST_EINTERNAL);
-      break;
-    }
-    // 3. merge and compact into the other buffer
-    const int E2 = (m + GS - 1) / GS;
-    const int lo2 = min(t * E2, m), hi2 = min(lo2 + E2, m);
-    int keep = 0;
-    for (int i = lo2; i < hi2; ++i) keep += !(i > 0 && A.fl[i - 1]);
-    int newm = 0;
-    int p = g.excl_sum(keep, &newm);
-    uint32_t* S2 = A.sym[cur ^ 1];
-    uint16_t* L2 = A.len[cur ^ 1];
-    unsigned long long* K2 = A.kr[cur ^ 1];
-    for (int i = lo2; i < hi2; ++i) {
-      if (i > 0 && A.fl[i - 1]) continue;  // absorbed into its left neighbour
-      const bool mg = A.fl[i] != 0;
-      if (mg) {
-        S2[p] = kr_result(K[i]);
-        L2[p] = (uint16_t)(L[i] + L[i + 1]);
-      } else {
-        S2[p] = S[i];
-        L2[p] = L[i];
+    __syncthreads();
+    // C: merge and compact, through registers
+    uint32_t nsym[ENG_EPT];
+    uint16_t nlen[ENG_EPT];
+    unsigned long long nkr[ENG_EPT];
+    uint32_t keep = 0;
+#pragma unroll
+    for (int j = 0; j < ENG_EPT; ++j) {
+      const int i = lo + j;
+      nsym[j] = 0; nlen[j] = 0; nkr[j] = 0;
+      if (i < hi && !(i > 0 && E.fl[i - 1])) {
+        keep |= 1u << j;
+        const bool mg = E.fl[i] != 0;
+        if (mg) {
+          nsym[j] = kr_result(E.kr[i]);
+          nlen[j] = (uint16_t)(((E.len[i] & LEN_MASK) + (E.len[i + 1] & LEN_MASK)) | (E.len[i] & FRAG_START));
+        } else {
+          nsym[j] = E.sym[i];
+          nlen[j] = E.len[i];
+        }
+        // an unchanged pair keeps its key; pairs touching a new symbol are looked up
+        nkr[j] = (!mg && i + 1 < m && !E.fl[i + 1]) ? E.kr[i] : KR_NEED;
       }
-      // an unchanged pair keeps its rank; pairs touching a new symbol are looked up
-      K2[p] = (!mg && i + 1 < m && !A.fl[i + 1]) ? K[i] : KR_NEED;
-      ++p;
     }
-    g.sync();
-    for (int q = t; q < newm; q += GS) {
-      if (q + 1 >= newm) K2[q] = KR_NONE;
-      else if (K2[q] == KR_NEED) K2[q] = merge_lookup(V, S2[q], S2[q + 1]);
+    int newm = 0;
+    const int base = block_excl_sum(__popc(keep), &newm, E.scan);
+#pragma unroll
+    for (int j = 0; j < ENG_EPT; ++j) {
+      if ((keep >> j) & 1u) {
+        const int p = base + __popc(keep & ((1u << j) - 1u));
+        E.sym[p] = nsym[j];
+        E.len[p] = nlen[j];
+        E.kr[p] = nkr[j];
+      }
     }
-    g.sync();
-    cur ^= 1;
+    __syncthreads();
+    // D: keys of pairs that touch a new symbol
+    const int cnt = __popc(keep);
+    for (int p = base; p < base + cnt; ++p) {
+      if (kr_rank(E.kr[p]) == RANK_NEED) {
+        if (p + 1 >= newm || (E.len[p + 1] & FRAG_START)) E.kr[p] = KR_WALL;
+        else E.kr[p] = merge_lookup(V, E.sym[p], E.sym[p + 1]);
+      }
+    }
     m = newm;
+    __syncthreads();
+    if (sweep == m0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
   }
-  // outputs
-  const int E3 = (m + GS - 1) / GS;
-  const int lo3 = min(t * E3, m), hi3 = min(lo3 + E3, m);
-  int bytes = 0;
-  for (int i = lo3; i < hi3; ++i) bytes += A.len[cur][i];
-  int tot = 0;
-  int off = g.excl_sum(bytes, &tot);
-  for (int i = lo3; i < hi3; ++i) {
-    const int l = A.len[cur][i];
-    sid[a + off] = (int32_t)A.sym[cur][i];
-    tstart[a + off] = 1;
-    for (int q = 1; q < l; ++q) tstart[a + off + q] = 0;
-    off += l;
+  // ids of this chunk's fragments, compacted at the chunk's first fragment start
+  for (int i = tid; i < m; i += T) ws.tok[fs + i] = (int32_t)E.sym[i];
+  if (tid == 0) {
+    ws.cm_first[chunk] = fs;
+    ws.cm_count[chunk] = m;
+    ws.cm_long[chunk] = E.longfrag;
   }
-  g.sync();
-}
-
-// K4a: warp tier, fragments of 17..256 bytes, arrays in shared memory
-struct WarpArrays {
-  uint32_t sym[2][MED_MAX];
-  unsigned long long kr[2][MED_MAX];
-  uint16_t len[2][MED_MAX];
-  int32_t rs[MED_MAX];
-  uint8_t fl[MED_MAX];
-};
-
-__global__ void __launch_bounds__(MED_WARPS * 32) k_bpe_med(Call c, Workspace ws, DevVocab V) {
-  __shared__ WarpArrays wa[MED_WARPS];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  WarpArrays& W = wa[warp];
-  EngineArrays A;
-  A.sym[0] = W.sym[0]; A.sym[1] = W.sym[1];
-  A.len[0] = W.len[0]; A.len[1] = W.len[1];
-  A.kr[0] = W.kr[0]; A.kr[1] = W.kr[1];
-  A.fl = W.fl; A.rs = W.rs;
-  WarpGroup g;
-  const uint32_t count = *(volatile uint32_t*)&ws.st->med_count;
-  while (true) {
-    uint32_t idx = 0;
-    if (lane == 0) idx = atomicAdd(&ws.st->med_taken, 1u);
-    idx = __shfl_sync(0xffffffffu, idx, 0);
-    if (idx >= count) break;
-    const Frag f = ws.medq[idx];
-    sweep_engine(g, V, c.text, f.start, (int)f.len, A, ws.sid, ws.tstart, &ws.st->code);
+  // batch: ids before each item start in this chunk (K5 adds the chunk's offset)
+  if (c.item_off) {
+    const int B = (m + T - 1) / T;
+    const int lo = min(tid * B, m), hi = min(lo + B, m);
+    int bytes = 0;
+    for (int i = lo; i < hi; ++i) bytes += E.len[i] & LEN_MASK;
+    int tot = 0;
+    int off = block_excl_sum(bytes, &tot, E.scan);
+    for (int i = lo; i < hi; ++i) {
+      E.rs[i] = (uint16_t)off;  // byte offset of symbol i from fs
+      off += E.len[i] & LEN_MASK;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int a = 0, b = c.n_items + 1;  // first item start >= r0
+      while (a < b) {
+        const int mid = (a + b) >> 1;
+        if (c.item[mid] < r0) a = mid + 1; else b = mid;
+      }
+      E.last = a;
+    }
+    __syncthreads();
+    for (int k = (int)E.last + tid; k <= c.n_items; k += T) {
+      const long long x = c.item[k];
+      if (x >= r1) break;
+      int a = 0, b = m;  // first symbol at or after x
+      while (a < b) {
+        const int mid = (a + b) >> 1;
+        if (fs + E.rs[mid] < x) a = mid + 1; else b = mid;
+      }
+      c.item_off[k] = a;
+    }
   }
 }
 
-// K4b: CTA tier, fragments longer than 256 bytes (or of unknown length),
-// arrays in global memory at the fragment's byte offsets
+// ---------------------------------------------------------------------------
+// K4: fragments longer than a chunk engine holds, one CTA each, in global
+// memory at the fragment's byte offsets (double-buffered)
+
 __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws, DevVocab V) {
-  __shared__ long long sh[2 * (LONG_THREADS / 32) + 4];
+  __shared__ int sh[LONG_THREADS / 32];
+  __shared__ unsigned long long sh64[LONG_THREADS / 32];
   __shared__ uint32_t s_idx;
-  __shared__ long long s_end;
-  BlockGroup g{sh};
+  __shared__ unsigned long long s_end;
+  const int tid = threadIdx.x, T = blockDim.x;
   const uint32_t count = *(volatile uint32_t*)&ws.st->long_count;
   while (true) {
-    if (threadIdx.x == 0) s_idx = atomicAdd(&ws.st->long_taken, 1u);
+    if (tid == 0) s_idx = atomicAdd(&ws.st->long_taken, 1u);
     __syncthreads();
     const uint32_t idx = s_idx;
     __syncthreads();
     if (idx >= count) break;
     const Frag f = ws.longq[idx];
-    long long len = f.len;
-    if (len < 0) {
-      // find the next fragment start after f.start (first set bit), bounded by n
-      if (threadIdx.x == 0) s_end = c.n;
-      __syncthreads();
-      const long long w0 = (f.start + 1) >> 5;
-      const long long wn = (c.n + 31) >> 5;
-      for (long long base = w0; base < wn; base += blockDim.x) {
-        const long long wi = base + threadIdx.x;
-        if (wi < wn) {
-          uint32_t wv = ws.pstart[wi];
-          if (wi == w0) wv &= ~0u << ((f.start + 1) & 31);
-          if (wv) atomicMin((unsigned long long*)&s_end, (unsigned long long)min(wi * 32 + __ffs(wv) - 1, c.n));
-        }
-        __syncthreads();
-        const long long e = s_end;
-        __syncthreads();
-        if (e < c.n || base + blockDim.x >= wn) break;
+    // end: the next fragment start after f.start, or the text end
+    if (tid == 0) s_end = (unsigned long long)c.n;
+    __syncthreads();
+    const long long w0 = (f.start + 1) >> 5, wn = (c.n + 31) >> 5;
+    for (long long base = w0; base < wn; base += T) {
+      const long long wi = base + tid;
+      if (wi < wn) {
+        uint32_t wv = ws.pstart[wi];
+        if (wi == w0) wv &= ~0u << ((f.start + 1) & 31);
+        if (wi * 32 + 32 > c.n) wv &= (c.n - wi * 32 >= 32) ? ~0u : ((1u << (c.n - wi * 32)) - 1u);
+        if (wv) atomicMin(&s_end, (unsigned long long)(wi * 32 + __ffs(wv) - 1));
       }
-      len = s_end - f.start;
       __syncthreads();
+      const bool found = s_end < (unsigned long long)c.n;
+      __syncthreads();
+      if (found) break;
     }
-    EngineArrays A;
-    for (int b = 0; b < 2; ++b) {
-      A.sym[b] = ws.e_sym[b] + f.start;
-      A.len[b] = ws.e_len[b] + f.start;
-      A.kr[b] = ws.e_kr[b] + f.start;
+    const long long a = f.start;
+    const int m0 = (int)((long long)s_end - a);
+    uint32_t* S0 = ws.e_sym[0] + a;
+    uint32_t* S1 = ws.e_sym[1] + a;
+    uint16_t* L0 = ws.e_len[0] + a;
+    uint16_t* L1 = ws.e_len[1] + a;
+    unsigned long long* K0 = ws.e_kr[0] + a;
+    unsigned long long* K1 = ws.e_kr[1] + a;
+    uint8_t* FL = ws.e_fl + a;
+    int32_t* RS = ws.e_rs + a;
+    for (int i = tid; i < m0; i += T) {
+      S0[i] = (uint32_t)V.byte_id[c.text[a + i]];
+      L0[i] = 1;
     }
-    A.fl = ws.e_fl + f.start;
-    A.rs = ws.e_rs + f.start;
-    sweep_engine(g, V, c.text, f.start, (int)len, A, ws.sid, ws.tstart, &ws.st->code);
+    __syncthreads();
+    for (int i = tid; i < m0; i += T) K0[i] = (i + 1 < m0) ? merge_lookup(V, S0[i], S0[i + 1]) : KR_WALL;
+    __syncthreads();
+    int m = m0, cur = 0;
+    for (int sweep = 0; sweep <= m0; ++sweep) {
+      uint32_t* S = cur ? S1 : S0;
+      uint16_t* L = cur ? L1 : L0;
+      unsigned long long* K = cur ? K1 : K0;
+      uint32_t* S2 = cur ? S0 : S1;
+      uint16_t* L2 = cur ? L0 : L1;
+      unsigned long long* K2 = cur ? K0 : K1;
+      const int B = (m + T - 1) / T;
+      const int lo = min(tid * B, m), hi = min(lo + B, m);
+      bool anyk = false;
+      int lastrun = -1;
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t k = kr_rank(K[i]);
+        anyk |= mergeable(k);
+        if (i == 0 || kr_rank(K[i - 1]) != k) lastrun = i;
+      }
+      if (!__syncthreads_or(anyk)) break;
+      int run = block_excl_max(lastrun, sh);
+      for (int i = lo; i < hi; ++i) {
+        if (i == 0 || kr_rank(K[i - 1]) != kr_rank(K[i])) run = i;
+        RS[i] = run;
+      }
+      __syncthreads();
+      if (V.monotone) {
+        for (int i = lo; i < hi; ++i) {
+          const uint32_t k = kr_rank(K[i]);
+          FL[i] = (mergeable(k) && pair_safe(V, S, L, K, RS, m, i, k)) ? 1 : 0;
+        }
+      } else {
+        unsigned long long best = ~0ull;
+        for (int i = lo; i < hi; ++i) {
+          const uint32_t k = kr_rank(K[i]);
+          if (mergeable(k)) {
+            const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
+            best = key < best ? key : best;
+          }
+        }
+        best = block_min_u64(best, sh64);
+        for (int i = lo; i < hi; ++i) FL[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
+      }
+      __syncthreads();
+      int keep = 0;
+      for (int i = lo; i < hi; ++i) keep += !(i > 0 && FL[i - 1]);
+      int newm = 0;
+      int p = block_excl_sum(keep, &newm, sh);
+      for (int i = lo; i < hi; ++i) {
+        if (i > 0 && FL[i - 1]) continue;
+        const bool mg = FL[i] != 0;
+        S2[p] = mg ? kr_result(K[i]) : S[i];
+        L2[p] = mg ? (uint16_t)(L[i] + L[i + 1]) : L[i];
+        K2[p] = (!mg && i + 1 < m && !FL[i + 1]) ? K[i] : KR_NEED;
+        ++p;
+      }
+      __syncthreads();
+      for (int q = tid; q < newm; q += T) {
+        if (kr_rank(K2[q]) == RANK_NEED) K2[q] = (q + 1 >= newm) ? KR_WALL : merge_lookup(V, S2[q], S2[q + 1]);
+      }
+      __syncthreads();
+      cur ^= 1;
+      m = newm;
+      if (sweep == m0 && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);
+    }
+    const uint32_t* S = cur ? S1 : S0;
+    for (int i = tid; i < m; i += T) ws.tok[a + i] = (int32_t)S[i];
+    if (tid == 0) ws.cm_long_count[f.chunk] = m;
+    __syncthreads();
   }
 }
 
-void launch_bpe_short(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
-  const long long nb = (c.n + BPE_CHUNK - 1) / BPE_CHUNK;
-  k_bpe_short<<<(unsigned)nb, BPE_THREADS, 0, s>>>(c, w, v);
-}
-
-void launch_bpe_med(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
-  k_bpe_med<<<n_sms * 4, MED_WARPS * 32, 0, s>>>(c, w, v);
+void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
+  k_bpe_chunk<<<(unsigned)n_chunks(c.n), ENG_THREADS, 0, s>>>(c, w, v);
 }
 
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {

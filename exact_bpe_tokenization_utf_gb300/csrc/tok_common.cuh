@@ -1,32 +1,33 @@
 // Shared definitions of the GB300 exact BPE tokenizer library.
 //
 // Pipeline (one pass over a text or a packed batch; "TokTier: exact stateful
-// tokenization for agentic LLM serving", Section 4):
-//   K1 run_summary   per 4 KiB chunk: the chunk's effect on three run states
-//                    (digit-run offset mod 3, "CR/LF-only since an O-run"
-//                    whitespace prefix, "CR/LF later in this whitespace run")
+// tokenization for agentic LLM serving", Section 4), all on 1 KiB chunks:
+//   K1 run_summary   the chunk's effect on three run states (digit-run offset
+//                    mod 3, "CR/LF-only since an O-run" whitespace prefix,
+//                    "CR/LF later in this whitespace run")
 //   K2 boundaries    UTF-8 validation + per-code-point class + run
 //                    decomposition rules -> fragment-start bitmask (Section 4.1)
-//   K3 bpe_short     fragments <= 16 bytes: one thread each, registers;
-//                    longer fragments are queued (Section 4.2 tiering)
-//   K4 bpe_sweep     queued fragments: a warp (<= 256 bytes) or a CTA (longer)
-//                    each, merging every pair that is certified safe per sweep
-//   K5 emit          token-start flags -> compacted ids (decoupled look-back)
+//   K3 bpe_chunk     every fragment that starts in the chunk (and fits in
+//                    ENG_CAP symbols with its neighbours) is encoded by one CTA
+//                    in shared memory, merging all certified-safe pairs per
+//                    sweep; a longer last fragment is queued (Section 4.2)
+//   K4 bpe_long      queued fragments, one CTA each, arrays in global memory
+//   K5 emit          per-chunk token counts -> offsets (decoupled look-back),
+//                    coalesced copy of the ids
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
 
 namespace tokgb {
 
-constexpr int CHUNK = 4096;        // bytes per pre-tokenizer / emit CTA
-constexpr int CHUNK_THREADS = 256; // 16 bytes per thread
+constexpr int CHUNK = 1024;        // bytes per chunk (every per-chunk kernel)
+constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K1 / K2
+constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
-constexpr int BPE_CHUNK = 1024;    // bytes per short-tier CTA
-constexpr int BPE_THREADS = 256;
-constexpr int SHORT_MAX = 16;      // thread tier
-constexpr int MED_MAX = 256;       // warp tier (shared memory); longer -> CTA tier
-constexpr int MED_WARPS = 4;       // warps per warp-tier CTA
-constexpr int LONG_THREADS = 512;  // CTA tier
+constexpr int ENG_CAP = 2048;      // symbols one K3 CTA holds: its chunk + the tail of its last fragment
+constexpr int ENG_THREADS = 256;
+constexpr int ENG_EPT = ENG_CAP / ENG_THREADS;  // symbols per thread at most
+constexpr int LONG_THREADS = 1024; // K4
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
 
@@ -54,10 +55,10 @@ struct DevVocab {
   int monotone;               // every merge that uses a token comes after every merge making it
 };
 
-// one queued fragment
+// one queued long fragment: its start; the chunk whose last fragment it is
 struct Frag {
   long long start;
-  long long len;  // -1: end not yet known
+  long long chunk;
 };
 
 // device-side per-call status and work counters
@@ -66,23 +67,24 @@ struct DevStatus {
   uint32_t epoch;
   unsigned long long err_off;   // first malformed UTF-8 byte (atomicMin), ~0 if none
   unsigned long long n_ids;
-  uint32_t med_count, med_taken;
   uint32_t long_count, long_taken;
   uint32_t emit_ticket, emit_done;
-  uint32_t pad[6];
+  uint32_t pad[8];
 };
 
 struct Workspace {
   uint8_t* text;            // device copy of host input (host entry points)
   uint32_t* csum;           // K1 chunk summaries
   uint32_t* pstart;         // fragment-start bitmask
-  uint8_t* tstart;          // 1 at the first byte of every token
-  int32_t* sid;             // token id at token-start bytes
-  Frag* medq;               // warp-tier queue
-  Frag* longq;              // CTA-tier queue
+  int32_t* tok;             // token ids, compacted per chunk at the chunk's first fragment start
+  long long* cm_first;      // per chunk: first fragment start in it, or -1
+  int32_t* cm_count;        // per chunk: ids K3 produced
+  long long* cm_long;       // per chunk: start of its queued long fragment, or -1
+  int32_t* cm_long_count;   // per chunk: ids K4 produced for it
+  Frag* longq;              // K4 queue
   unsigned long long* lb;   // K5 look-back words
   DevStatus* st;
-  // CTA-tier engine storage, indexed by byte position of the fragment
+  // K4 engine storage, indexed by byte position of the fragment
   uint32_t* e_sym[2];
   uint16_t* e_len[2];
   unsigned long long* e_kr[2];
@@ -161,8 +163,7 @@ __device__ __forceinline__ int utf8_decode(const uint8_t* s, int avail, uint32_t
 // host-side launchers (defined in the kernel translation units)
 void launch_run_summary(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
-void launch_bpe_short(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
-void launch_bpe_med(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
+void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
 void launch_emit(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);

@@ -2,8 +2,8 @@
 // exact stateful tokenization for agentic LLM serving", Section 4.3 returns
 // an id array; Section 4.4: ids only, no byte offsets).
 //
-// Each CTA owns a 4 KiB range of bytes and emits the tokens whose first byte
-// lies in it.  The number of tokens before the range comes from a
+// Each CTA owns a 1 KiB chunk and emits the ids of the fragments that start
+// in it (K3 left them compacted; a long last fragment's ids come from K4).  The number of tokens before the range comes from a
 // decoupled look-back over the CTAs' published counts (Merrill and Garland,
 // "Single-pass parallel prefix scan with decoupled look-back", 2016): ranges
 // are taken in ticket order, so a CTA only waits on CTAs that already run;
@@ -33,47 +33,26 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
 
 __global__ void __launch_bounds__(CHUNK_THREADS) k_emit(Call c, Workspace ws) {
   __shared__ uint32_t s_chunk;
-  __shared__ int wsum[CHUNK_THREADS / 32];
   __shared__ unsigned long long s_prefix;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int s_item;
+  const int tid = threadIdx.x;
   const long long nch = n_chunks(c.n);
   DevStatus* st = ws.st;
   if (tid == 0) s_chunk = atomicAdd(&st->emit_ticket, 1u);
   __syncthreads();
   const long long chunk = s_chunk;
-  const long long c0 = chunk * CHUNK;
-  const long long p0 = c0 + tid * 16;
-  // this thread's 16 token-start flags
-  uint32_t mask = 0;
-  if (p0 + 16 <= c.n && ((reinterpret_cast<uintptr_t>(ws.tstart) & 15u) == 0)) {
-    const uint4 v = *reinterpret_cast<const uint4*>(ws.tstart + p0);
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 16; ++q) mask |= ((wv[q >> 2] >> ((q & 3) * 8)) & 1u) << q;
-  } else {
-    for (int q = 0; q < 16; ++q)
-      if (p0 + q < c.n && ws.tstart[p0 + q]) mask |= 1u << q;
-  }
-  const int cnt = __popc(mask);
-  int inc = cnt;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += o;
-  }
-  if (lane == 31) wsum[warp] = inc;
-  __syncthreads();
-  int wpre = 0, total = 0;
-  for (int k = 0; k < CHUNK_THREADS / 32; ++k) {
-    if (k < warp) wpre += wsum[k];
-    total += wsum[k];
-  }
-  const int excl = wpre + inc - cnt;
+  const long long r0 = chunk * CHUNK;
+  const long long r1 = min(r0 + CHUNK, c.n);
+  const long long first = ws.cm_first[chunk];
+  const int n_short = first >= 0 ? ws.cm_count[chunk] : 0;
+  const long long lf = first >= 0 ? ws.cm_long[chunk] : -1;
+  const int n_long = lf >= 0 ? ws.cm_long_count[chunk] : 0;
+  const uint32_t total = (uint32_t)(n_short + n_long);
   if (tid == 0) {
     volatile unsigned long long* lb = ws.lb;
     if (chunk > 0) {
       __threadfence();
-      lb[chunk] = lb_pack(c.epoch, LB_AGG, (uint32_t)total);
+      lb[chunk] = lb_pack(c.epoch, LB_AGG, total);
     }
     unsigned long long prefix = 0;
     bool timed_out = false;
@@ -96,30 +75,24 @@ __global__ void __launch_bounds__(CHUNK_THREADS) k_emit(Call c, Workspace ws) {
     if (chunk == nch - 1) st->n_ids = prefix + total;
   }
   __syncthreads();
-  const unsigned long long base = s_prefix + excl;
-  // ids
-  unsigned long long o = base;
-  for (int q = 0; q < 16; ++q)
-    if ((mask >> q) & 1u) c.out[o++] = ws.sid[p0 + q];
-  // item offsets (batch): ids before each item start in this range
+  const unsigned long long base = s_prefix;
+  // ids: the chunk's fragments, then its long fragment (always its last one)
+  for (int j = tid; j < n_short; j += CHUNK_THREADS) c.out[base + j] = ws.tok[first + j];
+  for (int j = tid; j < n_long; j += CHUNK_THREADS) c.out[base + n_short + j] = ws.tok[lf + j];
+  // batch: K3 stored the ids before each item start relative to its chunk
   if (c.item_off) {
-    __shared__ int s_first;
     if (tid == 0) {
-      int lo = 0, hi = c.n_items + 1;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (c.item[mid] < c0) lo = mid + 1; else hi = mid;
+      int a = 0, b = c.n_items + 1;
+      while (a < b) {
+        const int mid = (a + b) >> 1;
+        if (c.item[mid] < r0) a = mid + 1; else b = mid;
       }
-      s_first = lo;
+      s_item = a;
     }
     __syncthreads();
-    for (int k = s_first + tid; k <= c.n_items; k += CHUNK_THREADS) {
-      const long long x = c.item[k];
-      if (x >= c0 + CHUNK || x >= c.n) break;
-      // ids before x in this range = token-start flags in bytes [c0, x)
-      long long cntb = 0;
-      for (long long y = c0; y < x; ++y) cntb += ws.tstart[y] != 0;
-      c.item_off[k] = (long long)s_prefix + cntb;
+    for (int k = s_item + tid; k <= c.n_items; k += CHUNK_THREADS) {
+      if (c.item[k] >= r1) break;
+      c.item_off[k] += (long long)base;
     }
   }
   // the last CTA to finish completes the status

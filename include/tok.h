@@ -59,7 +59,7 @@ enum { TOK_PAT_GPT2 = 0, TOK_PAT_CL100K_STYLE = 1 };
  * vocab_bytes / vocab_off: token t has bytes vocab_bytes[vocab_off[t] ..
  *   vocab_off[t+1]) (host, n_vocab+1 offsets).  Each of the 256 single bytes
  *   must be exactly one token; no two tokens may have equal bytes; tokens are
- *   at most 65535 bytes; n_vocab < 2^20.
+ *   at most 32767 bytes; n_vocab < 2^20.
  * merges: host array of n_merges (left_id, right_id) pairs in rank order
  *   (rank = index).  The result of a merge is the token whose bytes are
  *   bytes(left) || bytes(right); it must exist.  No pair may repeat.
@@ -147,8 +147,8 @@ int tok_pretokenize_batch(tok_handle* h, const uint8_t* const* texts, const uint
  * looks up that array's device address (cudaGetSymbolAddress, with the device
  * current); make that first call before any stream capture.
  * d_text: device, len bytes.  d_start_bits: device uint32 words, at least
- *   ceil(len / 4096) * 128 of them; bit p % 32 of word p / 32 is set iff a
- *   fragment starts at byte p (bits at p >= len are 0).
+ *   ceil(len / 32) of them; bit p % 32 of word p / 32 is set iff a fragment
+ *   starts at byte p (bits at p >= len are 0).
  * d_status: device int64[2]: [0] = TOK_OK or TOK_EUTF8, [1] = offset of the
  *   first malformed UTF-8 sequence or -1.
  * Enqueued on `stream` (NULL = the CUDA default stream) with no host sync.

@@ -35,7 +35,7 @@ def test_noalloc_pretokenizer_matches_allocating_entry_point():
                  textgen.adversarial(200_003, 60 + pattern, scale=0.02).encode()]
         for data in texts:  # two calls in a row share the scratch array
             n = len(data)
-            words = -(-n // 4096) * 128
+            words = -(-n // 32)
             d_text = torch.frombuffer(bytearray(data), dtype=torch.uint8).cuda()
             d_bits = torch.full((words,), -1, dtype=torch.int32, device="cuda")
             d_st = torch.full((2,), 7, dtype=torch.int64, device="cuda")
@@ -49,7 +49,7 @@ def test_noalloc_pretokenizer_matches_allocating_entry_point():
         # malformed input: same error offset as the allocating entry point
         bad = b"a" * 5000 + b"\xe4\xb8" + b"b" * 10
         d_text = torch.frombuffer(bytearray(bad), dtype=torch.uint8).cuda()
-        d_bits = torch.zeros(-(-len(bad) // 4096) * 128, dtype=torch.int32, device="cuda")
+        d_bits = torch.zeros(-(-len(bad) // 32), dtype=torch.int32, device="cuda")
         d_st = torch.zeros(2, dtype=torch.int64, device="cuda")
         rc = L.tok_pretokenize_device_noalloc(pattern, d_text.data_ptr(), len(bad), d_bits.data_ptr(),
                                               d_st.data_ptr(), ctypes.c_void_p(stream))
