@@ -44,6 +44,10 @@ struct tok_handle {
   uint16_t* d_tok_len = nullptr;
   uint16_t* d_max_left = nullptr;
   uint16_t* d_max_right = nullptr;
+  WholeEntry* d_whole = nullptr;
+  uint8_t* d_vocab_bytes = nullptr;
+  uint32_t* d_vocab_off = nullptr;
+  uint32_t n_whole = 0;
   uint64_t hash = 0;
   // workspace
   Workspace ws{};
@@ -301,6 +305,52 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   for (uint32_t t = 0; t < n_vocab && monotone; ++t)
     if (last_made[t] >= 0 && first_used[t] != INT64_MAX && first_used[t] <= last_made[t]) monotone = false;
 
+  // Self-encoding tokens: BPE (the textbook rule) of a token's own bytes gives
+  // back that token.  A fragment whose bytes equal such a token's encodes to
+  // it, which lets the kernels skip the merge loop for it.
+  std::unordered_map<unsigned long long, std::pair<uint32_t, uint32_t>> mh;
+  mh.reserve(n_merges * 2 + 1);
+  for (uint32_t r = 0; r < n_merges; ++r) {
+    const unsigned long long key = ((unsigned long long)merges[2 * r] << 32) | merges[2 * r + 1];
+    for (uint32_t slot = merge_slot(key, bits);; slot = (slot + 1) & mask)
+      if (table[slot].key == key) { mh.emplace(key, std::make_pair(table[slot].rank, table[slot].result)); break; }
+  }
+  std::vector<uint32_t> whole_tokens;
+  uint32_t max_tok_len = 1;
+  {
+    std::vector<uint32_t> sy;
+    for (uint32_t t = 0; t < n_vocab; ++t) {
+      const uint32_t len = tok_len[t];
+      max_tok_len = std::max(max_tok_len, len);
+      if (len < 2) continue;
+      sy.assign(len, 0);
+      for (uint32_t i = 0; i < len; ++i) sy[i] = (uint32_t)byte_id[vocab_bytes[vocab_off[t] + i]];
+      while (sy.size() > 1) {
+        uint32_t best = UINT32_MAX, bi = 0, br = 0;
+        for (uint32_t i = 0; i + 1 < sy.size(); ++i) {
+          auto it = mh.find(((unsigned long long)sy[i] << 32) | sy[i + 1]);
+          if (it != mh.end() && it->second.first < best) { best = it->second.first; bi = i; br = it->second.second; }
+        }
+        if (best == UINT32_MAX) break;
+        sy[bi] = br;
+        sy.erase(sy.begin() + bi + 1);
+      }
+      if (sy.size() == 1 && sy[0] == t) whole_tokens.push_back(t);
+    }
+  }
+  uint32_t wbits = 10;
+  while ((1ull << wbits) < 2ull * whole_tokens.size()) ++wbits;
+  std::vector<WholeEntry> whole(1ull << wbits, WholeEntry{0, 0, 0});
+  for (uint32_t t : whole_tokens) {
+    const unsigned long long hv = bytes_hash(vocab_bytes + vocab_off[t], tok_len[t]);
+    uint32_t slot = (uint32_t)(hv >> (64 - wbits));
+    while (whole[slot].len != 0) slot = (slot + 1) & ((1u << wbits) - 1u);
+    whole[slot] = WholeEntry{hv, t, tok_len[t]};
+  }
+  std::vector<uint32_t> off32(n_vocab + 1);
+  for (uint32_t t = 0; t <= n_vocab; ++t) off32[t] = (uint32_t)(vocab_off[t] - vocab_off[0]);
+  if (vocab_off[n_vocab] - vocab_off[0] >= (1ull << 32)) return fail(nullptr, TOK_EMERGES, "vocabulary too large");
+
   tok_handle* h = new tok_handle();
   h->pattern = pattern_id;
   cudaError_t e = cudaGetDevice(&h->dev);
@@ -311,6 +361,15 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   if (e == cudaSuccess) e = dalloc(&h->d_tok_len, n_vocab);
   if (e == cudaSuccess) e = dalloc(&h->d_max_left, n_vocab);
   if (e == cudaSuccess) e = dalloc(&h->d_max_right, n_vocab);
+  if (e == cudaSuccess) e = dalloc(&h->d_whole, whole.size());
+  if (e == cudaSuccess) e = dalloc(&h->d_vocab_bytes, off32[n_vocab] + 16);
+  if (e == cudaSuccess) e = dalloc(&h->d_vocab_off, n_vocab + 1);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->d_whole, whole.data(), whole.size() * sizeof(WholeEntry), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->d_vocab_bytes, vocab_bytes + vocab_off[0], off32[n_vocab], cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->d_vocab_off, off32.data(), (n_vocab + 1) * sizeof(uint32_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_table, table.data(), table.size() * sizeof(MergeEntry), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->d_byte_id, byte_id.data(), 256 * sizeof(int32_t), cudaMemcpyHostToDevice);
@@ -334,6 +393,12 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   h->v.max_left = h->d_max_left;
   h->v.max_right = h->d_max_right;
   h->v.monotone = monotone ? 1 : 0;
+  h->v.whole = h->d_whole;
+  h->v.whole_bits = wbits;
+  h->v.max_tok_len = max_tok_len;
+  h->v.vocab_bytes = h->d_vocab_bytes;
+  h->v.vocab_off = h->d_vocab_off;
+  h->n_whole = (uint32_t)whole_tokens.size();
   uint64_t hh = 1469598103934665603ull;
   hh = fnv1a(hh, &pattern_id, sizeof pattern_id);
   for (uint32_t t = 0; t < n_vocab; ++t) {
@@ -352,7 +417,8 @@ void tok_free(tok_handle* h) {
   DeviceGuard g(h->dev);
   if (h->stream) cudaStreamSynchronize(h->stream);
   free_workspace(h);
-  void* ptrs[] = {h->d_table, h->d_byte_id, h->d_tok_len, h->d_max_left, h->d_max_right, h->d_items, h->d_item_off};
+  void* ptrs[] = {h->d_table,  h->d_byte_id,     h->d_tok_len,     h->d_max_left, h->d_max_right,
+                  h->d_whole,  h->d_vocab_bytes, h->d_vocab_off,   h->d_items,    h->d_item_off};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_status) cudaFreeHost(h->h_status);

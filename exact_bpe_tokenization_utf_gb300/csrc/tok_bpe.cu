@@ -137,23 +137,38 @@ __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int p) { return (bits[p >> 5] >> (p & 31)) & 1u; }
 
 // ---------------------------------------------------------------------------
-// K3: the fragments that start in one 1 KiB chunk, in shared memory
+// K3: the fragments that start in one 1 KiB chunk
+//
+// Most fragments need no merge loop: a single byte is its byte token, and a
+// fragment whose bytes equal a token t with BPE(bytes(t)) == [t] (checked for
+// every token at load time) encodes to [t].  One thread per fragment settles
+// those with a hash probe; only the rest enter the sweep engine, in shared
+// memory, with walls between fragments.
 
 struct ChunkEngine {
   uint32_t sym[ENG_CAP];
   unsigned long long kr[ENG_CAP];
   uint16_t len[ENG_CAP];
   uint16_t rs[ENG_CAP];
+  uint16_t fidx[ENG_CAP];      // fragment of each engine symbol
   uint8_t fl[ENG_CAP];
+  uint8_t text[ENG_CAP];       // bytes [first, end)
   uint32_t bits[ENG_CAP / 32];
+  uint16_t fstart[CHUNK + 1];  // fragment starts relative to `first`, then `end`
+  int32_t ftok[CHUNK];         // settled token, or -1: goes through the engine
+  int32_t fcnt[CHUNK];         // ids of each fragment
+  uint16_t fout[CHUNK];        // first id of each fragment (relative)
+  uint16_t feng[CHUNK];        // first engine symbol of each fragment
   int scan[ENG_THREADS / 32];
   unsigned long long scan64[ENG_THREADS / 32];
   int32_t byte_id[256];
-  long long first, end, last, longfrag;
+  long long first, end, longfrag, item0;
+  int nf;
 };
 
 __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws, DevVocab V) {
-  __shared__ ChunkEngine E;
+  extern __shared__ __align__(16) uint8_t dsm[];
+  ChunkEngine& E = *reinterpret_cast<ChunkEngine*>(dsm);
   const int tid = threadIdx.x, T = ENG_THREADS;
   const long long chunk = blockIdx.x;
   const long long r0 = chunk * CHUNK;
@@ -173,10 +188,8 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
   if (tid < 32) {
     // first and last fragment start in [r0, r1); first start in [r1, lim)
     const int lane = tid;
-    const uint32_t w0 = E.bits[lane];  // CHUNK / 32 == 32 words
-    const uint32_t nz = __ballot_sync(0xffffffffu, w0 != 0u);
-    const uint32_t w1 = E.bits[32 + lane];
-    const uint32_t nz1 = __ballot_sync(0xffffffffu, w1 != 0u);
+    const uint32_t nz = __ballot_sync(0xffffffffu, E.bits[lane] != 0u);  // CHUNK / 32 == 32 words
+    const uint32_t nz1 = __ballot_sync(0xffffffffu, E.bits[32 + lane] != 0u);
     if (lane == 0) {
       long long first = -1, last = -1, end = -1;
       if (nz) {
@@ -209,11 +222,51 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
     }
     return;
   }
-  const int m0 = (int)(E.end - fs);
-  for (int i = tid; i < m0; i += T) {
-    const int p = (int)(fs - r0) + i;
-    E.sym[i] = (uint32_t)E.byte_id[c.text[fs + i]];
-    E.len[i] = (uint16_t)(1u | (bit_at(E.bits, p) ? FRAG_START : 0u));
+  const int span = (int)(E.end - fs);  // bytes of the fragments handled here
+  const int rel = (int)(fs - r0);
+  for (int i = tid; i < span; i += T) E.text[i] = c.text[fs + i];
+  // fragment starts in [fs, min(r1, end)): thread t looks at 4 bit positions
+  {
+    const int q0 = tid * 4;  // positions relative to r0
+    const uint32_t nib = (E.bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
+    uint32_t mine = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (((nib >> q) & 1u) && r0 + q0 + q < E.end) mine |= 1u << q;
+    int nf = 0;
+    int idx = block_excl_sum(__popc(mine), &nf, E.scan);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if ((mine >> q) & 1u) E.fstart[idx++] = (uint16_t)(q0 + q - rel);
+    if (tid == 0) {
+      E.nf = nf;
+      E.fstart[nf] = (uint16_t)span;
+    }
+  }
+  __syncthreads();
+  const int nf = E.nf;
+  // settle single bytes and whole tokens; contiguous fragments per thread
+  const int FB = (nf + T - 1) / T;
+  const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
+  int eng_bytes = 0;
+  for (int f = flo; f < fhi; ++f) {
+    const int a = E.fstart[f], L = E.fstart[f + 1] - a;
+    int t = L == 1 ? E.byte_id[E.text[a]] : whole_lookup(V, E.text + a, L);
+    E.ftok[f] = t;
+    E.fcnt[f] = t >= 0 ? 1 : 0;
+    if (t < 0) eng_bytes += L;
+  }
+  int m0 = 0;
+  int eo = block_excl_sum(eng_bytes, &m0, E.scan);
+  for (int f = flo; f < fhi; ++f) {
+    if (E.ftok[f] >= 0) continue;
+    const int a = E.fstart[f], L = E.fstart[f + 1] - a;
+    for (int j = 0; j < L; ++j) {
+      E.sym[eo + j] = (uint32_t)E.byte_id[E.text[a + j]];
+      E.len[eo + j] = (uint16_t)(1u | (j == 0 ? FRAG_START : 0u));
+      E.fidx[eo + j] = (uint16_t)f;
+    }
+    eo += L;
   }
   __syncthreads();
   for (int i = tid; i < m0; i += T)
@@ -260,13 +313,13 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
     __syncthreads();
     // C: merge and compact, through registers
     uint32_t nsym[ENG_EPT];
-    uint16_t nlen[ENG_EPT];
+    uint16_t nlen[ENG_EPT], nfi[ENG_EPT];
     unsigned long long nkr[ENG_EPT];
     uint32_t keep = 0;
 #pragma unroll
     for (int j = 0; j < ENG_EPT; ++j) {
       const int i = lo + j;
-      nsym[j] = 0; nlen[j] = 0; nkr[j] = 0;
+      nsym[j] = 0; nlen[j] = 0; nkr[j] = 0; nfi[j] = 0;
       if (i < hi && !(i > 0 && E.fl[i - 1])) {
         keep |= 1u << j;
         const bool mg = E.fl[i] != 0;
@@ -277,6 +330,7 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
           nsym[j] = E.sym[i];
           nlen[j] = E.len[i];
         }
+        nfi[j] = E.fidx[i];
         // an unchanged pair keeps its key; pairs touching a new symbol are looked up
         nkr[j] = (!mg && i + 1 < m && !E.fl[i + 1]) ? E.kr[i] : KR_NEED;
       }
@@ -290,6 +344,7 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
         E.sym[p] = nsym[j];
         E.len[p] = nlen[j];
         E.kr[p] = nkr[j];
+        E.fidx[p] = nfi[j];
       }
     }
     __syncthreads();
@@ -303,46 +358,55 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
     }
     m = newm;
     __syncthreads();
-    if (sweep == m0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
+    if (sweep == m0 && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
   }
-  // ids of this chunk's fragments, compacted at the chunk's first fragment start
-  for (int i = tid; i < m; i += T) ws.tok[fs + i] = (int32_t)E.sym[i];
+  // ids per fragment, then the fragments' first ids
+  for (int i = tid; i < m; i += T) {
+    const int f = E.fidx[i];
+    if (E.len[i] & FRAG_START) E.feng[f] = (uint16_t)i;
+    atomicAdd(&E.fcnt[f], 1);
+  }
+  __syncthreads();
+  int ids = 0;
+  for (int f = flo; f < fhi; ++f) ids += E.fcnt[f];
+  int total = 0;
+  int oo = block_excl_sum(ids, &total, E.scan);
+  for (int f = flo; f < fhi; ++f) {
+    E.fout[f] = (uint16_t)oo;
+    oo += E.fcnt[f];
+  }
+  __syncthreads();
+  for (int f = tid; f < nf; f += T)
+    if (E.ftok[f] >= 0) ws.tok[fs + E.fout[f]] = E.ftok[f];
+  for (int i = tid; i < m; i += T) {
+    const int f = E.fidx[i];
+    ws.tok[fs + E.fout[f] + (i - E.feng[f])] = (int32_t)E.sym[i];
+  }
   if (tid == 0) {
     ws.cm_first[chunk] = fs;
-    ws.cm_count[chunk] = m;
+    ws.cm_count[chunk] = total;
     ws.cm_long[chunk] = E.longfrag;
   }
   // batch: ids before each item start in this chunk (K5 adds the chunk's offset)
   if (c.item_off) {
-    const int B = (m + T - 1) / T;
-    const int lo = min(tid * B, m), hi = min(lo + B, m);
-    int bytes = 0;
-    for (int i = lo; i < hi; ++i) bytes += E.len[i] & LEN_MASK;
-    int tot = 0;
-    int off = block_excl_sum(bytes, &tot, E.scan);
-    for (int i = lo; i < hi; ++i) {
-      E.rs[i] = (uint16_t)off;  // byte offset of symbol i from fs
-      off += E.len[i] & LEN_MASK;
-    }
-    __syncthreads();
     if (tid == 0) {
       int a = 0, b = c.n_items + 1;  // first item start >= r0
       while (a < b) {
         const int mid = (a + b) >> 1;
         if (c.item[mid] < r0) a = mid + 1; else b = mid;
       }
-      E.last = a;
+      E.item0 = a;
     }
     __syncthreads();
-    for (int k = (int)E.last + tid; k <= c.n_items; k += T) {
+    for (int k = (int)E.item0 + tid; k <= c.n_items; k += T) {
       const long long x = c.item[k];
       if (x >= r1) break;
-      int a = 0, b = m;  // first symbol at or after x
+      int a = 0, b = nf;  // fragment starting at x (or the long fragment after the last)
       while (a < b) {
         const int mid = (a + b) >> 1;
-        if (fs + E.rs[mid] < x) a = mid + 1; else b = mid;
+        if (fs + E.fstart[mid] < x) a = mid + 1; else b = mid;
       }
-      c.item_off[k] = a;
+      c.item_off[k] = a < nf ? E.fout[a] : total;
     }
   }
 }
@@ -470,7 +534,14 @@ __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws,
 }
 
 void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
-  k_bpe_chunk<<<(unsigned)n_chunks(c.n), ENG_THREADS, 0, s>>>(c, w, v);
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaFuncSetAttribute(k_bpe_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ChunkEngine));
+    attr_set[dev] = true;
+  }
+  k_bpe_chunk<<<(unsigned)n_chunks(c.n), ENG_THREADS, sizeof(ChunkEngine), s>>>(c, w, v);
 }
 
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {

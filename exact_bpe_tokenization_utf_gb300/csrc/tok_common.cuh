@@ -44,10 +44,23 @@ struct __align__(16) MergeEntry {
   uint32_t result;
 };
 
+// whole-token table entry: a token whose own bytes encode to itself, keyed by
+// a hash of those bytes; len == 0 marks an empty slot
+struct __align__(16) WholeEntry {
+  unsigned long long hash;
+  uint32_t token;
+  uint32_t len;
+};
+
 struct DevVocab {
   const MergeEntry* table;
   uint32_t bits;              // log2(capacity)
   uint32_t n_vocab;
+  const WholeEntry* whole;    // tokens t with BPE(bytes(t)) == [t], length >= 2
+  uint32_t whole_bits;        // log2(capacity)
+  uint32_t max_tok_len;
+  const uint8_t* vocab_bytes; // token bytes back to back
+  const uint32_t* vocab_off;  // n_vocab + 1 offsets
   const int32_t* byte_id;     // 256 entries: initial symbol of each byte value
   const uint16_t* tok_len;    // byte length of every token
   const uint16_t* max_left;   // longest left operand of any merge whose right operand is t
@@ -110,6 +123,21 @@ __host__ __device__ inline uint32_t merge_slot(unsigned long long key, uint32_t 
   return (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> (64 - bits));
 }
 
+// 64-bit hash of a byte string (FNV-1a, then the splitmix64 finaliser)
+__host__ __device__ inline unsigned long long bytes_hash(const uint8_t* s, int len) {
+  unsigned long long h = 1469598103934665603ull;
+  for (int i = 0; i < len; ++i) {
+    h ^= s[i];
+    h *= 1099511628211ull;
+  }
+  h ^= h >> 30;
+  h *= 0xBF58476D1CE4E5B9ull;
+  h ^= h >> 27;
+  h *= 0x94D049BB133111EBull;
+  h ^= h >> 31;
+  return h;
+}
+
 #ifdef __CUDACC__
 // Probe the merge table for (a, b): returns (rank << 32 | result), or ~0 when
 // the pair is not a merge.  Linear probing over a table at most half full,
@@ -126,6 +154,27 @@ __device__ __forceinline__ unsigned long long merge_lookup(const DevVocab& v, ui
     s = (s + 1u) & mask;
   }
   return ~0ull;
+}
+
+// Token whose bytes equal s[0..len) and whose own bytes encode to itself,
+// or -1.  The hash only selects candidates; the bytes are compared.
+__device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s, int len) {
+  if (len < 2 || len > (int)v.max_tok_len) return -1;
+  const unsigned long long h = bytes_hash(s, len);
+  const uint32_t mask = (1u << v.whole_bits) - 1u;
+  uint32_t slot = (uint32_t)(h >> (64 - v.whole_bits));
+  for (uint32_t probe = 0; probe <= mask; ++probe) {
+    const uint4 e = __ldg(reinterpret_cast<const uint4*>(v.whole + slot));
+    if (e.w == 0u) return -1;
+    if (e.w == (uint32_t)len && (((unsigned long long)e.y << 32) | e.x) == h) {
+      const uint8_t* t = v.vocab_bytes + __ldg(v.vocab_off + e.z);
+      bool eq = true;
+      for (int i = 0; i < len && eq; ++i) eq = __ldg(t + i) == s[i];
+      if (eq) return (int)e.z;
+    }
+    slot = (slot + 1u) & mask;
+  }
+  return -1;
 }
 
 __device__ __forceinline__ uint32_t kr_rank(unsigned long long kr) { return (uint32_t)(kr >> 32); }

@@ -48,31 +48,45 @@ __global__ void __launch_bounds__(CHUNK_THREADS) k_emit(Call c, Workspace ws) {
   const long long lf = first >= 0 ? ws.cm_long[chunk] : -1;
   const int n_long = lf >= 0 ? ws.cm_long_count[chunk] : 0;
   const uint32_t total = (uint32_t)(n_short + n_long);
-  if (tid == 0) {
+  if (tid < 32) {
+    // warp 0: publish this chunk's count, then look back 32 predecessors at a
+    // time until one has published its inclusive prefix
+    const int lane = tid;
     volatile unsigned long long* lb = ws.lb;
-    if (chunk > 0) {
+    const uint32_t ep = c.epoch & 0x3FFFFFFFu;
+    if (lane == 0 && chunk > 0) {
       __threadfence();
       lb[chunk] = lb_pack(c.epoch, LB_AGG, total);
     }
     unsigned long long prefix = 0;
     bool timed_out = false;
-    for (long long j = chunk - 1; j >= 0; --j) {
-      unsigned long long v = lb[j];
+    for (long long top = chunk - 1; top >= 0; top -= 32) {
+      const long long j = top - lane;
+      unsigned long long v = j >= 0 ? lb[j] : lb_pack(c.epoch, LB_INC, 0u);
       int spins = 0;
-      while ((uint32_t)(v >> 34) != (c.epoch & 0x3FFFFFFFu)) {
+      while (true) {
+        const bool ready = (uint32_t)(v >> 34) == ep;
+        if (__all_sync(0xffffffffu, ready)) break;
         if (++spins > LB_SPIN_LIMIT) { timed_out = true; break; }
         __nanosleep(64);
-        v = lb[j];
+        if (!ready) v = lb[j];
       }
       if (timed_out) break;
-      prefix += (uint32_t)v;
-      if (((v >> 32) & 3ull) == LB_INC) break;
+      const uint32_t inc = __ballot_sync(0xffffffffu, ((v >> 32) & 3ull) == LB_INC);
+      const int stop = inc ? __ffs(inc) - 1 : 31;  // nearest predecessor with an inclusive prefix
+      unsigned long long x = lane <= stop ? (uint32_t)v : 0ull;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      prefix += x;
+      if (inc) break;
     }
-    if (timed_out) atomicExch(&st->code, ST_ETIMEOUT);
-    __threadfence();
-    lb[chunk] = lb_pack(c.epoch, LB_INC, (uint32_t)(prefix + total));
-    s_prefix = prefix;
-    if (chunk == nch - 1) st->n_ids = prefix + total;
+    if (lane == 0) {
+      if (timed_out) atomicExch(&st->code, ST_ETIMEOUT);
+      __threadfence();
+      lb[chunk] = lb_pack(c.epoch, LB_INC, (uint32_t)(prefix + total));
+      s_prefix = prefix;
+      if (chunk == nch - 1) st->n_ids = prefix + total;
+    }
   }
   __syncthreads();
   const unsigned long long base = s_prefix;
