@@ -124,6 +124,7 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   free_workspace(h);
   Workspace& w = h->ws;
   const uint64_t nch = cap / CHUNK;
+  const uint64_t nbch = cap / BCHUNK;
   const uint64_t pad = 256;
   cudaError_t e = cudaSuccess;
   auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
@@ -131,12 +132,12 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.csum, nch + 2));
   chk(dalloc(&w.pstart, cap / 32 + pad));
   chk(dalloc(&w.tok, cap + pad));
-  chk(dalloc(&w.cm_first, nch + 2));
-  chk(dalloc(&w.cm_count, nch + 2));
-  chk(dalloc(&w.cm_long, nch + 2));
-  chk(dalloc(&w.cm_long_count, nch + 2));
-  chk(dalloc(&w.longq, nch + 2));
-  chk(dalloc(&w.lb, nch + 2));
+  chk(dalloc(&w.cm_first, nbch + 2));
+  chk(dalloc(&w.cm_count, nbch + 2));
+  chk(dalloc(&w.cm_long, nbch + 2));
+  chk(dalloc(&w.cm_long_count, nbch + 2));
+  chk(dalloc(&w.longq, nbch + 2));
+  chk(dalloc(&w.lb, nbch + 2));
   chk(dalloc(&w.st, 1));
   for (int b = 0; b < 2; ++b) {
     chk(dalloc(&w.e_sym[b], cap + pad));
@@ -146,7 +147,7 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.e_fl, cap + pad));
   chk(dalloc(&w.e_rs, cap + pad));
   chk(dalloc(&h->d_out, cap + pad));
-  if (e == cudaSuccess) e = cudaMemset(w.lb, 0, (nch + 2) * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(w.lb, 0, (nbch + 2) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(w.pstart, 0, (cap / 32 + pad) * sizeof(uint32_t));
   if (e != cudaSuccess) {
     free_workspace(h);
@@ -341,15 +342,17 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   uint32_t wbits = 10;
   while ((1ull << wbits) < 2ull * whole_tokens.size()) ++wbits;
   std::vector<WholeEntry> whole(1ull << wbits, WholeEntry{0, 0, 0});
-  for (uint32_t t : whole_tokens) {
-    const unsigned long long hv = bytes_hash(vocab_bytes + vocab_off[t], tok_len[t]);
-    uint32_t slot = (uint32_t)(hv >> (64 - wbits));
-    while (whole[slot].len != 0) slot = (slot + 1) & ((1u << wbits) - 1u);
-    whole[slot] = WholeEntry{hv, t, tok_len[t]};
-  }
+  if (vocab_off[n_vocab] - vocab_off[0] >= (1ull << 32)) return fail(nullptr, TOK_EMERGES, "vocabulary too large");
   std::vector<uint32_t> off32(n_vocab + 1);
   for (uint32_t t = 0; t <= n_vocab; ++t) off32[t] = (uint32_t)(vocab_off[t] - vocab_off[0]);
-  if (vocab_off[n_vocab] - vocab_off[0] >= (1ull << 32)) return fail(nullptr, TOK_EMERGES, "vocabulary too large");
+  for (uint32_t t : whole_tokens) {
+    // entries carry offset and length so a probe needs one more load to compare bytes
+    if (tok_len[t] > 255 || off32[t] >= (1u << 24)) continue;
+    const unsigned long long hv = bytes_hash(vocab_bytes + vocab_off[t], tok_len[t]);
+    uint32_t slot = (uint32_t)(hv >> (64 - wbits));
+    while (whole[slot].offlen != 0) slot = (slot + 1) & ((1u << wbits) - 1u);
+    whole[slot] = WholeEntry{hv, t, (off32[t] << 8) | tok_len[t]};
+  }
 
   tok_handle* h = new tok_handle();
   h->pattern = pattern_id;

@@ -2,8 +2,8 @@
 // serving", Section 4.2): every fragment is encoded on its own by merging the
 // lowest-rank adjacent pair (leftmost on ties) until no adjacent pair is a
 // merge.  The pages tier fragments by length (one thread, one warp, one block
-// per fragment); here one CTA encodes all fragments of a 1 KiB chunk at once,
-// and only fragments longer than that get a CTA each.
+// per fragment); here one CTA encodes all fragments of a 512-byte chunk at
+// once, and only fragments longer than 512 bytes get a CTA each.
 //
 // Sweep engine.  The symbols of many fragments sit in one array; the pair
 // between two fragments is a "wall" that never merges.  Let k be the rank of
@@ -40,18 +40,19 @@ constexpr uint16_t FRAG_START = 0x8000;
 
 __device__ __forceinline__ bool mergeable(uint32_t rank) { return rank < RANK_NEED; }
 
-// Is pair i (rank k) safe to merge now?  rs[i] is the first pair of the run
-// of equal-rank pairs that contains i.  See the file comment.
-template <class RS>
-__device__ __forceinline__ bool pair_safe(const DevVocab& V, const uint32_t* S, const uint16_t* L,
-                                          const unsigned long long* K, const RS* rs, int m, int i, uint32_t k) {
-  const int u = (int)rs[i];
+// Is pair i (rank k) safe to merge now?  u is the first pair of the run of
+// equal-rank pairs that contains i; ml(x) / mr(x) are the longest left /
+// right operand of any merge whose right / left operand is symbol x.  See the
+// file comment.
+template <class ML, class MR>
+__device__ __forceinline__ bool pair_safe(const uint16_t* L, const unsigned long long* K, int m, int i, int u,
+                                          uint32_t k, ML ml, MR mr) {
   if ((i - u) & 1) return false;
   if (u > 0) {
     const uint32_t kl = kr_rank(K[u - 1]);
     if (kl != RANK_WALL) {
       if (kl < k) return false;
-      const int lim = V.max_left[S[u]];
+      const int lim = ml(u);
       int cum = L[u - 1] & LEN_MASK;
       for (int q = u - 2; q >= 0; --q) {
         const uint32_t kq = kr_rank(K[q]);
@@ -66,7 +67,7 @@ __device__ __forceinline__ bool pair_safe(const DevVocab& V, const uint32_t* S, 
     const uint32_t kr = kr_rank(K[i + 1]);
     if (kr != RANK_WALL) {
       if (kr < k) return false;
-      const int lim = V.max_right[S[i + 1]];
+      const int lim = mr(i + 1);
       int cum = L[i + 2] & LEN_MASK;
       for (int q = i + 2; q < m - 1; ++q) {
         const uint32_t kq = kr_rank(K[q]);
@@ -137,59 +138,78 @@ __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int p) { return (bits[p >> 5] >> (p & 31)) & 1u; }
 
 // ---------------------------------------------------------------------------
-// K3: the fragments that start in one 1 KiB chunk
+// K3: the fragments that start in one 512-byte chunk
 //
 // Most fragments need no merge loop: a single byte is its byte token, and a
 // fragment whose bytes equal a token t with BPE(bytes(t)) == [t] (checked for
 // every token at load time) encodes to [t].  One thread per fragment settles
-// those with a hash probe; only the rest enter the sweep engine, in shared
-// memory, with walls between fragments.
+// those with a hash probe; the rest go through the sweep engine in shared
+// memory, in batches of at most B_CAP symbols, with walls between fragments.
+// Each symbol carries its operand-length bounds, so the safety test reads
+// shared memory only; the merge lookups of a sweep are issued before its
+// compaction scan.
 
 struct ChunkEngine {
-  uint32_t sym[ENG_CAP];
-  unsigned long long kr[ENG_CAP];
-  uint16_t len[ENG_CAP];
-  uint16_t rs[ENG_CAP];
-  uint16_t fidx[ENG_CAP];      // fragment of each engine symbol
-  uint8_t fl[ENG_CAP];
-  uint8_t text[ENG_CAP];       // bytes [first, end)
-  uint32_t bits[ENG_CAP / 32];
-  uint16_t fstart[CHUNK + 1];  // fragment starts relative to `first`, then `end`
-  int32_t ftok[CHUNK];         // settled token, or -1: goes through the engine
-  int32_t fcnt[CHUNK];         // ids of each fragment
-  uint16_t fout[CHUNK];        // first id of each fragment (relative)
-  uint16_t feng[CHUNK];        // first engine symbol of each fragment
-  int scan[ENG_THREADS / 32];
-  unsigned long long scan64[ENG_THREADS / 32];
+  // one engine batch
+  uint32_t sym[B_CAP];
+  unsigned long long kr[B_CAP];
+  uint16_t len[B_CAP];      // byte length | FRAG_START
+  uint16_t rs[B_CAP];       // run start of equal-rank pairs
+  uint16_t fidx[B_CAP];     // fragment of each symbol
+  uint16_t ml[B_CAP];       // longest left operand of merges whose right operand is this symbol
+  uint16_t mr[B_CAP];       // longest right operand of merges whose left operand is this symbol
+  uint8_t fl[B_CAP];        // pair merges this sweep
+  // the CTA's bytes and fragment starts
+  uint8_t text[B_RANGE];
+  uint32_t bits[B_RANGE / 32];
+  // fragments that start in the chunk (at most BCHUNK)
+  uint16_t fstart[BCHUNK + 1];  // relative to `first`; then the span
+  int32_t ftok[BCHUNK];         // settled token, or -1
+  int32_t fcnt[BCHUNK];         // ids of each fragment
+  uint16_t fout[BCHUNK];        // first id of each fragment
+  uint16_t feng[BCHUNK];        // first engine symbol of a fragment in its batch
+  uint16_t feoff[BCHUNK];       // offset of an unresolved fragment among all unresolved bytes
+  uint16_t ulist[BCHUNK];       // unresolved fragments in order
+  uint16_t ueoff[BCHUNK + 1];   // their offsets, then the total
+  uint32_t efinal[B_RANGE];     // engine results at their fragment's feoff
   int32_t byte_id[256];
+  uint16_t byte_ml[256], byte_mr[256];
+  int scan[B_THREADS / 32];
+  unsigned long long scan64[B_THREADS / 32];
   long long first, end, longfrag, item0;
-  int nf;
+  int nf, nu, sflags, batch_end;
 };
 
-__global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws, DevVocab V) {
+__global__ void __launch_bounds__(B_THREADS) k_bpe_chunk(Call c, Workspace ws, DevVocab V) {
   extern __shared__ __align__(16) uint8_t dsm[];
   ChunkEngine& E = *reinterpret_cast<ChunkEngine*>(dsm);
-  const int tid = threadIdx.x, T = ENG_THREADS;
+  const int tid = threadIdx.x, T = B_THREADS, lane = tid & 31;
   const long long chunk = blockIdx.x;
-  const long long r0 = chunk * CHUNK;
-  const long long r1 = min(r0 + CHUNK, c.n);
-  const long long lim = min(r0 + ENG_CAP, c.n);
-  E.byte_id[tid] = V.byte_id[tid];
-  for (int w = tid; w < ENG_CAP / 32; w += T) {
-    const long long p = r0 + 32ll * w;
+  const long long r0 = chunk * BCHUNK;
+  const long long r1 = min(r0 + BCHUNK, c.n);
+  const long long lim = min(r0 + B_RANGE, c.n);
+  for (int b = tid; b < 256; b += T) {
+    const int32_t id = V.byte_id[b];
+    E.byte_id[b] = id;
+    E.byte_ml[b] = V.max_left[id];
+    E.byte_mr[b] = V.max_right[id];
+  }
+  if (tid < B_RANGE / 32) {
+    const long long p = r0 + 32ll * tid;
     uint32_t v = 0;
     if (p < lim) {
-      v = ws.pstart[(r0 >> 5) + w];
+      v = ws.pstart[(r0 >> 5) + tid];
       if (lim - p < 32) v &= (1u << (lim - p)) - 1u;
     }
-    E.bits[w] = v;
+    E.bits[tid] = v;
   }
+  if (tid == 0) E.sflags = 0;
   __syncthreads();
   if (tid < 32) {
-    // first and last fragment start in [r0, r1); first start in [r1, lim)
-    const int lane = tid;
-    const uint32_t nz = __ballot_sync(0xffffffffu, E.bits[lane] != 0u);  // CHUNK / 32 == 32 words
-    const uint32_t nz1 = __ballot_sync(0xffffffffu, E.bits[32 + lane] != 0u);
+    // first and last fragment start in [r0, r1) (words 0..15), first start in [r1, lim) (16..31)
+    const uint32_t w = E.bits[lane];
+    const uint32_t nz = __ballot_sync(0xffffffffu, lane < BCHUNK / 32 && w != 0u);
+    const uint32_t nz1 = __ballot_sync(0xffffffffu, lane >= BCHUNK / 32 && w != 0u) >> (BCHUNK / 32);
     if (lane == 0) {
       long long first = -1, last = -1, end = -1;
       if (nz) {
@@ -198,10 +218,12 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
         last = r0 + 32ll * b + (31 - __clz(E.bits[b]));
       }
       if (r1 >= c.n) end = c.n;
-      else if (nz1) { const int a = __ffs(nz1) - 1; end = r1 + 32ll * a + (__ffs(E.bits[32 + a]) - 1); }
-      else if (lim >= c.n) end = c.n;
+      else if (nz1) {
+        const int a = __ffs(nz1) - 1;
+        end = r1 + 32ll * a + (__ffs(E.bits[BCHUNK / 32 + a]) - 1);
+      } else if (lim >= c.n) end = c.n;
       long long lf = -1;
-      if (first >= 0 && end < 0) {  // the last fragment runs past lim: queue it
+      if (first >= 0 && (end < 0 || end - last > B_CAP)) {  // the last fragment is long: queue it
         lf = last;
         end = last;
         const uint32_t q = atomicAdd(&ws.st->long_count, 1u);
@@ -222,12 +244,11 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
     }
     return;
   }
-  const int span = (int)(E.end - fs);  // bytes of the fragments handled here
+  const int span = (int)(E.end - fs);
   const int rel = (int)(fs - r0);
   for (int i = tid; i < span; i += T) E.text[i] = c.text[fs + i];
-  // fragment starts in [fs, min(r1, end)): thread t looks at 4 bit positions
-  {
-    const int q0 = tid * 4;  // positions relative to r0
+  {  // fragment starts in [fs, min(r1, end)): thread t looks at 4 bit positions
+    const int q0 = tid * 4;
     const uint32_t nib = (E.bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
     uint32_t mine = 0;
 #pragma unroll
@@ -245,128 +266,182 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
   }
   __syncthreads();
   const int nf = E.nf;
-  // settle single bytes and whole tokens; contiguous fragments per thread
+  // settle single bytes and whole tokens (contiguous fragments per thread)
   const int FB = (nf + T - 1) / T;
   const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
-  int eng_bytes = 0;
+  int ubytes = 0, ucount = 0;
   for (int f = flo; f < fhi; ++f) {
     const int a = E.fstart[f], L = E.fstart[f + 1] - a;
-    int t = L == 1 ? E.byte_id[E.text[a]] : whole_lookup(V, E.text + a, L);
+    const int t = L == 1 ? E.byte_id[E.text[a]] : whole_lookup(V, E.text + a, L);
     E.ftok[f] = t;
     E.fcnt[f] = t >= 0 ? 1 : 0;
-    if (t < 0) eng_bytes += L;
+    if (t < 0) { ubytes += L; ++ucount; }
   }
-  int m0 = 0;
-  int eo = block_excl_sum(eng_bytes, &m0, E.scan);
+  int nu = 0, ub_all = 0;
+  int ui = block_excl_sum(ucount, &nu, E.scan);
+  int uo = block_excl_sum(ubytes, &ub_all, E.scan);
   for (int f = flo; f < fhi; ++f) {
     if (E.ftok[f] >= 0) continue;
-    const int a = E.fstart[f], L = E.fstart[f + 1] - a;
-    for (int j = 0; j < L; ++j) {
-      E.sym[eo + j] = (uint32_t)E.byte_id[E.text[a + j]];
-      E.len[eo + j] = (uint16_t)(1u | (j == 0 ? FRAG_START : 0u));
-      E.fidx[eo + j] = (uint16_t)f;
-    }
-    eo += L;
+    E.ulist[ui] = (uint16_t)f;
+    E.ueoff[ui] = (uint16_t)uo;
+    E.feoff[f] = (uint16_t)uo;
+    ++ui;
+    uo += E.fstart[f + 1] - E.fstart[f];
   }
-  __syncthreads();
-  for (int i = tid; i < m0; i += T)
-    E.kr[i] = (i + 1 >= m0 || (E.len[i + 1] & FRAG_START)) ? KR_WALL : merge_lookup(V, E.sym[i], E.sym[i + 1]);
+  if (tid == 0) E.ueoff[nu] = (uint16_t)ub_all;
   __syncthreads();
 
-  int m = m0;
-  for (int sweep = 0; sweep <= m0; ++sweep) {
-    const int B = (m + T - 1) / T;
-    const int lo = min(tid * B, m), hi = min(lo + B, m);
-    // A: any mergeable pair left?  run starts of equal-rank pairs
-    bool anyk = false;
-    int lastrun = -1;
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t k = kr_rank(E.kr[i]);
-      anyk |= mergeable(k);
-      if (i == 0 || kr_rank(E.kr[i - 1]) != k) lastrun = i;
-    }
-    if (!__syncthreads_or(anyk)) break;
-    int run = block_excl_max(lastrun, E.scan);
-    for (int i = lo; i < hi; ++i) {
-      if (i == 0 || kr_rank(E.kr[i - 1]) != kr_rank(E.kr[i])) run = i;
-      E.rs[i] = (uint16_t)run;
+  // engine batches over the unresolved fragments
+  for (int ub = 0; ub < nu;) {
+    if (tid == 0) {  // largest ue with ueoff[ue] - ueoff[ub] <= B_CAP
+      int a = ub + 1, b = nu;
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (E.ueoff[mid] - E.ueoff[ub] <= B_CAP) a = mid; else b = mid - 1;
+      }
+      E.batch_end = a;
     }
     __syncthreads();
-    // B: safe pairs
-    if (V.monotone) {
-      for (int i = lo; i < hi; ++i) {
-        const uint32_t k = kr_rank(E.kr[i]);
-        E.fl[i] = (mergeable(k) && pair_safe(V, E.sym, E.len, E.kr, E.rs, m, i, k)) ? 1 : 0;
+    const int ue = E.batch_end;
+    const int base = E.ueoff[ub];
+    const int M = E.ueoff[ue] - base;
+    for (int i = tid; i < M; i += T) {
+      int a = ub, b = ue - 1;  // fragment k with ueoff[k] <= base + i < ueoff[k+1]
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (E.ueoff[mid] <= base + i) a = mid; else b = mid - 1;
       }
-    } else {
-      unsigned long long best = ~0ull;
+      const int f = E.ulist[a];
+      const int j = base + i - E.ueoff[a];
+      const uint8_t byte = E.text[E.fstart[f] + j];
+      E.sym[i] = (uint32_t)E.byte_id[byte];
+      E.len[i] = (uint16_t)(1u | (j == 0 ? FRAG_START : 0u));
+      E.fidx[i] = (uint16_t)f;
+      E.ml[i] = E.byte_ml[byte];
+      E.mr[i] = E.byte_mr[byte];
+    }
+    __syncthreads();
+    for (int i = tid; i < M; i += T)
+      E.kr[i] = (i + 1 >= M || (E.len[i + 1] & FRAG_START)) ? KR_WALL : merge_lookup(V, E.sym[i], E.sym[i + 1]);
+    __syncthreads();
+
+    int m = M;
+    for (int sweep = 0; sweep <= M; ++sweep) {
+      const int B = (m + T - 1) / T;
+      const int lo = min(tid * B, m), hi = min(lo + B, m);
+      // A: any mergeable pair left?  any overlapping equal-rank pairs?
+      int fl2 = 0;
       for (int i = lo; i < hi; ++i) {
         const uint32_t k = kr_rank(E.kr[i]);
         if (mergeable(k)) {
-          const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
-          best = key < best ? key : best;
+          fl2 |= 1;
+          if (i > 0 && kr_rank(E.kr[i - 1]) == k) fl2 |= 2;
         }
       }
-      best = block_min_u64(best, E.scan64);
-      for (int i = lo; i < hi; ++i) E.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
-    }
-    __syncthreads();
-    // C: merge and compact, through registers
-    uint32_t nsym[ENG_EPT];
-    uint16_t nlen[ENG_EPT], nfi[ENG_EPT];
-    unsigned long long nkr[ENG_EPT];
-    uint32_t keep = 0;
-#pragma unroll
-    for (int j = 0; j < ENG_EPT; ++j) {
-      const int i = lo + j;
-      nsym[j] = 0; nlen[j] = 0; nkr[j] = 0; nfi[j] = 0;
-      if (i < hi && !(i > 0 && E.fl[i - 1])) {
-        keep |= 1u << j;
-        const bool mg = E.fl[i] != 0;
-        if (mg) {
-          nsym[j] = kr_result(E.kr[i]);
-          nlen[j] = (uint16_t)(((E.len[i] & LEN_MASK) + (E.len[i + 1] & LEN_MASK)) | (E.len[i] & FRAG_START));
-        } else {
-          nsym[j] = E.sym[i];
-          nlen[j] = E.len[i];
+      fl2 = __reduce_or_sync(0xffffffffu, fl2);
+      if (lane == 0 && fl2) atomicOr(&E.sflags, fl2);
+      __syncthreads();
+      const int flags = E.sflags;
+      if (!(flags & 1)) break;
+      if (flags & 2) {
+        int lastrun = -1;
+        for (int i = lo; i < hi; ++i)
+          if (i == 0 || kr_rank(E.kr[i - 1]) != kr_rank(E.kr[i])) lastrun = i;
+        int run = block_excl_max(lastrun, E.scan);
+        for (int i = lo; i < hi; ++i) {
+          if (i == 0 || kr_rank(E.kr[i - 1]) != kr_rank(E.kr[i])) run = i;
+          E.rs[i] = (uint16_t)run;
         }
-        nfi[j] = E.fidx[i];
-        // an unchanged pair keeps its key; pairs touching a new symbol are looked up
-        nkr[j] = (!mg && i + 1 < m && !E.fl[i + 1]) ? E.kr[i] : KR_NEED;
+        __syncthreads();
       }
-    }
-    int newm = 0;
-    const int base = block_excl_sum(__popc(keep), &newm, E.scan);
+      // B: safe pairs
+      if (V.monotone) {
+        auto mlf = [&](int x) { return (int)E.ml[x]; };
+        auto mrf = [&](int x) { return (int)E.mr[x]; };
+        for (int i = lo; i < hi; ++i) {
+          const uint32_t k = kr_rank(E.kr[i]);
+          const int u = (flags & 2) ? (int)E.rs[i] : i;
+          E.fl[i] = (mergeable(k) && pair_safe(E.len, E.kr, m, i, u, k, mlf, mrf)) ? 1 : 0;
+        }
+      } else {
+        unsigned long long best = ~0ull;
+        for (int i = lo; i < hi; ++i) {
+          const uint32_t k = kr_rank(E.kr[i]);
+          if (mergeable(k)) {
+            const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
+            best = key < best ? key : best;
+          }
+        }
+        best = block_min_u64(best, E.scan64);
+        for (int i = lo; i < hi; ++i) E.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
+      }
+      __syncthreads();
+      // C: merge, look up the new pairs, compact
+      uint32_t nsym[B_EPT];
+      uint16_t nlen[B_EPT], nfi[B_EPT], nml[B_EPT], nmr[B_EPT];
+      unsigned long long nkr[B_EPT];
+      uint32_t keep = 0;
 #pragma unroll
-    for (int j = 0; j < ENG_EPT; ++j) {
-      if ((keep >> j) & 1u) {
-        const int p = base + __popc(keep & ((1u << j) - 1u));
-        E.sym[p] = nsym[j];
-        E.len[p] = nlen[j];
-        E.kr[p] = nkr[j];
-        E.fidx[p] = nfi[j];
+      for (int j = 0; j < B_EPT; ++j) {
+        const int i = lo + j;
+        nsym[j] = 0; nlen[j] = 0; nfi[j] = 0; nml[j] = 0; nmr[j] = 0; nkr[j] = KR_WALL;
+        if (i < hi && !(i > 0 && E.fl[i - 1])) {
+          keep |= 1u << j;
+          const bool mg = E.fl[i] != 0;
+          if (mg) {
+            const uint32_t r = kr_result(E.kr[i]);
+            nsym[j] = r;
+            nlen[j] = (uint16_t)(((E.len[i] & LEN_MASK) + (E.len[i + 1] & LEN_MASK)) | (E.len[i] & FRAG_START));
+            nml[j] = __ldg(V.max_left + r);
+            nmr[j] = __ldg(V.max_right + r);
+          } else {
+            nsym[j] = E.sym[i];
+            nlen[j] = E.len[i];
+            nml[j] = E.ml[i];
+            nmr[j] = E.mr[i];
+          }
+          nfi[j] = E.fidx[i];
+          const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
+          if (jn >= m || (E.len[jn] & FRAG_START)) nkr[j] = KR_WALL;
+          else if (!mg && !E.fl[jn]) nkr[j] = E.kr[i];  // unchanged pair keeps its key
+          else nkr[j] = merge_lookup(V, nsym[j], E.fl[jn] ? kr_result(E.kr[jn]) : E.sym[jn]);
+        }
       }
+      int newm = 0;
+      const int bpos = block_excl_sum(__popc(keep), &newm, E.scan);
+#pragma unroll
+      for (int j = 0; j < B_EPT; ++j) {
+        if ((keep >> j) & 1u) {
+          const int p = bpos + __popc(keep & ((1u << j) - 1u));
+          E.sym[p] = nsym[j];
+          E.len[p] = nlen[j];
+          E.kr[p] = nkr[j];
+          E.fidx[p] = nfi[j];
+          E.ml[p] = nml[j];
+          E.mr[p] = nmr[j];
+        }
+      }
+      if (tid == 0) E.sflags = 0;
+      m = newm;
+      __syncthreads();
+      if (sweep == M && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
+    }
+    // this batch's results
+    for (int i = tid; i < m; i += T) {
+      const int f = E.fidx[i];
+      if (E.len[i] & FRAG_START) E.feng[f] = (uint16_t)i;
+      atomicAdd(&E.fcnt[f], 1);
     }
     __syncthreads();
-    // D: keys of pairs that touch a new symbol
-    const int cnt = __popc(keep);
-    for (int p = base; p < base + cnt; ++p) {
-      if (kr_rank(E.kr[p]) == RANK_NEED) {
-        if (p + 1 >= newm || (E.len[p + 1] & FRAG_START)) E.kr[p] = KR_WALL;
-        else E.kr[p] = merge_lookup(V, E.sym[p], E.sym[p + 1]);
-      }
+    for (int i = tid; i < m; i += T) {
+      const int f = E.fidx[i];
+      E.efinal[E.feoff[f] + (i - E.feng[f])] = E.sym[i];
     }
-    m = newm;
+    if (tid == 0) E.sflags = 0;
     __syncthreads();
-    if (sweep == m0 && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
+    ub = ue;
   }
-  // ids per fragment, then the fragments' first ids
-  for (int i = tid; i < m; i += T) {
-    const int f = E.fidx[i];
-    if (E.len[i] & FRAG_START) E.feng[f] = (uint16_t)i;
-    atomicAdd(&E.fcnt[f], 1);
-  }
-  __syncthreads();
+  // first id of each fragment, then the ids
   int ids = 0;
   for (int f = flo; f < fhi; ++f) ids += E.fcnt[f];
   int total = 0;
@@ -376,11 +451,14 @@ __global__ void __launch_bounds__(ENG_THREADS) k_bpe_chunk(Call c, Workspace ws,
     oo += E.fcnt[f];
   }
   __syncthreads();
-  for (int f = tid; f < nf; f += T)
-    if (E.ftok[f] >= 0) ws.tok[fs + E.fout[f]] = E.ftok[f];
-  for (int i = tid; i < m; i += T) {
-    const int f = E.fidx[i];
-    ws.tok[fs + E.fout[f] + (i - E.feng[f])] = (int32_t)E.sym[i];
+  for (int f = tid; f < nf; f += T) {
+    const int o = E.fout[f];
+    if (E.ftok[f] >= 0) {
+      ws.tok[fs + o] = E.ftok[f];
+    } else {
+      const int e0 = E.feoff[f], cnt = E.fcnt[f];
+      for (int j = 0; j < cnt; ++j) ws.tok[fs + o + j] = (int32_t)E.efinal[e0 + j];
+    }
   }
   if (tid == 0) {
     ws.cm_first[chunk] = fs;
@@ -490,7 +568,10 @@ __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws,
       if (V.monotone) {
         for (int i = lo; i < hi; ++i) {
           const uint32_t k = kr_rank(K[i]);
-          FL[i] = (mergeable(k) && pair_safe(V, S, L, K, RS, m, i, k)) ? 1 : 0;
+          FL[i] = (mergeable(k) && pair_safe(L, K, m, i, RS[i], k, [&](int x) { return (int)V.max_left[S[x]]; },
+                                             [&](int x) { return (int)V.max_right[S[x]]; }))
+                      ? 1
+                      : 0;
         }
       } else {
         unsigned long long best = ~0ull;
@@ -541,7 +622,7 @@ void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cuda
     cudaFuncSetAttribute(k_bpe_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ChunkEngine));
     attr_set[dev] = true;
   }
-  k_bpe_chunk<<<(unsigned)n_chunks(c.n), ENG_THREADS, sizeof(ChunkEngine), s>>>(c, w, v);
+  k_bpe_chunk<<<(unsigned)n_bchunks(c.n), B_THREADS, sizeof(ChunkEngine), s>>>(c, w, v);
 }
 
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {

@@ -24,9 +24,11 @@ constexpr int CHUNK = 1024;        // bytes per chunk (every per-chunk kernel)
 constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K1 / K2
 constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
-constexpr int ENG_CAP = 2048;      // symbols one K3 CTA holds: its chunk + the tail of its last fragment
-constexpr int ENG_THREADS = 256;
-constexpr int ENG_EPT = ENG_CAP / ENG_THREADS;  // symbols per thread at most
+constexpr int BCHUNK = 512;        // bytes per BPE / emit CTA (K3, K5)
+constexpr int B_RANGE = 2 * BCHUNK;// bytes a K3 CTA covers: its chunk + the tail of its last fragment
+constexpr int B_CAP = 512;         // engine symbols per batch; a longer last fragment goes to K4
+constexpr int B_THREADS = 128;
+constexpr int B_EPT = B_CAP / B_THREADS;  // engine symbols per thread at most
 constexpr int LONG_THREADS = 1024; // K4
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
@@ -45,11 +47,12 @@ struct __align__(16) MergeEntry {
 };
 
 // whole-token table entry: a token whose own bytes encode to itself, keyed by
-// a hash of those bytes; len == 0 marks an empty slot
+// a hash of those bytes; offlen = byte offset of the token << 8 | length
+// (length 2..255), offlen == 0 marks an empty slot
 struct __align__(16) WholeEntry {
   unsigned long long hash;
   uint32_t token;
-  uint32_t len;
+  uint32_t offlen;
 };
 
 struct DevVocab {
@@ -91,7 +94,7 @@ struct Workspace {
   uint32_t* pstart;         // fragment-start bitmask
   int32_t* tok;             // token ids, compacted per chunk at the chunk's first fragment start
   long long* cm_first;      // per chunk: first fragment start in it, or -1
-  int32_t* cm_count;        // per chunk: ids K3 produced
+  int32_t* cm_count;        // per chunk: ids K3 produced  (K3 / K5 chunks are BCHUNK bytes)
   long long* cm_long;       // per chunk: start of its queued long fragment, or -1
   int32_t* cm_long_count;   // per chunk: ids K4 produced for it
   Frag* longq;              // K4 queue
@@ -159,15 +162,15 @@ __device__ __forceinline__ unsigned long long merge_lookup(const DevVocab& v, ui
 // Token whose bytes equal s[0..len) and whose own bytes encode to itself,
 // or -1.  The hash only selects candidates; the bytes are compared.
 __device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s, int len) {
-  if (len < 2 || len > (int)v.max_tok_len) return -1;
+  if (len < 2 || len > 255 || len > (int)v.max_tok_len) return -1;
   const unsigned long long h = bytes_hash(s, len);
   const uint32_t mask = (1u << v.whole_bits) - 1u;
   uint32_t slot = (uint32_t)(h >> (64 - v.whole_bits));
   for (uint32_t probe = 0; probe <= mask; ++probe) {
     const uint4 e = __ldg(reinterpret_cast<const uint4*>(v.whole + slot));
     if (e.w == 0u) return -1;
-    if (e.w == (uint32_t)len && (((unsigned long long)e.y << 32) | e.x) == h) {
-      const uint8_t* t = v.vocab_bytes + __ldg(v.vocab_off + e.z);
+    if ((e.w & 255u) == (uint32_t)len && (((unsigned long long)e.y << 32) | e.x) == h) {
+      const uint8_t* t = v.vocab_bytes + (e.w >> 8);
       bool eq = true;
       for (int i = 0; i < len && eq; ++i) eq = __ldg(t + i) == s[i];
       if (eq) return (int)e.z;
@@ -218,5 +221,6 @@ void launch_emit(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);
 
 __host__ __device__ inline long long n_chunks(long long n) { return (n + CHUNK - 1) / CHUNK; }
+__host__ __device__ inline long long n_bchunks(long long n) { return (n + BCHUNK - 1) / BCHUNK; }
 
 }  // namespace tokgb

@@ -2,7 +2,7 @@
 // exact stateful tokenization for agentic LLM serving", Section 4.3 returns
 // an id array; Section 4.4: ids only, no byte offsets).
 //
-// Each CTA owns a 1 KiB chunk and emits the ids of the fragments that start
+// Each CTA owns a 512-byte chunk and emits the ids of the fragments that start
 // in it (K3 left them compacted; a long last fragment's ids come from K4).  The number of tokens before the range comes from a
 // decoupled look-back over the CTAs' published counts (Merrill and Garland,
 // "Single-pass parallel prefix scan with decoupled look-back", 2016): ranges
@@ -31,18 +31,18 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
   c.user_status[3] = 0;
 }
 
-__global__ void __launch_bounds__(CHUNK_THREADS) k_emit(Call c, Workspace ws) {
+__global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
   __shared__ uint32_t s_chunk;
   __shared__ unsigned long long s_prefix;
   __shared__ int s_item;
   const int tid = threadIdx.x;
-  const long long nch = n_chunks(c.n);
+  const long long nch = n_bchunks(c.n);
   DevStatus* st = ws.st;
   if (tid == 0) s_chunk = atomicAdd(&st->emit_ticket, 1u);
   __syncthreads();
   const long long chunk = s_chunk;
-  const long long r0 = chunk * CHUNK;
-  const long long r1 = min(r0 + CHUNK, c.n);
+  const long long r0 = chunk * BCHUNK;
+  const long long r1 = min(r0 + BCHUNK, c.n);
   const long long first = ws.cm_first[chunk];
   const int n_short = first >= 0 ? ws.cm_count[chunk] : 0;
   const long long lf = first >= 0 ? ws.cm_long[chunk] : -1;
@@ -91,8 +91,8 @@ __global__ void __launch_bounds__(CHUNK_THREADS) k_emit(Call c, Workspace ws) {
   __syncthreads();
   const unsigned long long base = s_prefix;
   // ids: the chunk's fragments, then its long fragment (always its last one)
-  for (int j = tid; j < n_short; j += CHUNK_THREADS) c.out[base + j] = ws.tok[first + j];
-  for (int j = tid; j < n_long; j += CHUNK_THREADS) c.out[base + n_short + j] = ws.tok[lf + j];
+  for (int j = tid; j < n_short; j += B_THREADS) c.out[base + j] = ws.tok[first + j];
+  for (int j = tid; j < n_long; j += B_THREADS) c.out[base + n_short + j] = ws.tok[lf + j];
   // batch: K3 stored the ids before each item start relative to its chunk
   if (c.item_off) {
     if (tid == 0) {
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(CHUNK_THREADS) k_emit(Call c, Workspace ws) {
       s_item = a;
     }
     __syncthreads();
-    for (int k = s_item + tid; k <= c.n_items; k += CHUNK_THREADS) {
+    for (int k = s_item + tid; k <= c.n_items; k += B_THREADS) {
       if (c.item[k] >= r1) break;
       c.item_off[k] += (long long)base;
     }
@@ -137,7 +137,7 @@ __global__ void k_status_only(Call c, Workspace ws) {
 }
 
 void launch_emit(const Call& c, const Workspace& w, cudaStream_t s) {
-  k_emit<<<(unsigned)n_chunks(c.n), CHUNK_THREADS, 0, s>>>(c, w);
+  k_emit<<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w);
 }
 
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s) {
