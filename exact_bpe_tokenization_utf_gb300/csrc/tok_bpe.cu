@@ -2,8 +2,9 @@
 // serving", Section 4.2): every fragment is encoded on its own by merging the
 // lowest-rank adjacent pair (leftmost on ties) until no adjacent pair is a
 // merge.  The pages tier fragments by length (one thread, one warp, one block
-// per fragment); here one CTA encodes all fragments of a 512-byte chunk at
-// once, and only fragments longer than 512 bytes get a CTA each.
+// per fragment); here a fragment is settled by one probe when it is a single
+// byte or a whole self-encoding token, otherwise batched with others into one
+// warp (<= 128 bytes) or given a CTA (longer).
 //
 // Sweep engine.  The symbols of many fragments sit in one array; the pair
 // between two fragments is a "wall" that never merges.  Let k be the rank of
@@ -138,359 +139,315 @@ __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v
 __device__ __forceinline__ bool bit_at(const uint32_t* bits, int p) { return (bits[p >> 5] >> (p & 31)) & 1u; }
 
 // ---------------------------------------------------------------------------
-// K3: the fragments that start in one 512-byte chunk
+// K3: settle the fragments that start in one 512-byte chunk
 //
 // Most fragments need no merge loop: a single byte is its byte token, and a
 // fragment whose bytes equal a token t with BPE(bytes(t)) == [t] (checked for
 // every token at load time) encodes to [t].  One thread per fragment settles
-// those with a hash probe; the rest go through the sweep engine in shared
-// memory, in batches of at most B_CAP symbols, with walls between fragments.
-// Each symbol carries its operand-length bounds, so the safety test reads
-// shared memory only; the merge lookups of a sweep are issued before its
-// compaction scan.
+// those with a hash probe; the others are queued for K3b (at most WCAP
+// bytes) or K4.
 
-struct ChunkEngine {
-  // one engine batch
-  uint32_t sym[B_CAP];
-  unsigned long long kr[B_CAP];
-  uint16_t len[B_CAP];      // byte length | FRAG_START
-  uint16_t rs[B_CAP];       // run start of equal-rank pairs
-  uint16_t fidx[B_CAP];     // fragment of each symbol
-  uint16_t ml[B_CAP];       // longest left operand of merges whose right operand is this symbol
-  uint16_t mr[B_CAP];       // longest right operand of merges whose left operand is this symbol
-  uint8_t fl[B_CAP];        // pair merges this sweep
-  // the CTA's bytes and fragment starts
-  uint8_t text[B_RANGE];
-  uint32_t bits[B_RANGE / 32];
-  // fragments that start in the chunk (at most BCHUNK)
-  uint16_t fstart[BCHUNK + 1];  // relative to `first`; then the span
-  int32_t ftok[BCHUNK];         // settled token, or -1
-  int32_t fcnt[BCHUNK];         // ids of each fragment
-  uint16_t fout[BCHUNK];        // first id of each fragment
-  uint16_t feng[BCHUNK];        // first engine symbol of a fragment in its batch
-  uint16_t feoff[BCHUNK];       // offset of an unresolved fragment among all unresolved bytes
-  uint16_t ulist[BCHUNK];       // unresolved fragments in order
-  uint16_t ueoff[BCHUNK + 1];   // their offsets, then the total
-  uint32_t efinal[B_RANGE];     // engine results at their fragment's feoff
-  int32_t byte_id[256];
-  uint16_t byte_ml[256], byte_mr[256];
-  int scan[B_THREADS / 32];
-  unsigned long long scan64[B_THREADS / 32];
-  long long first, end, longfrag, item0;
-  int nf, nu, sflags, batch_end;
-};
-
-__global__ void __launch_bounds__(B_THREADS) k_bpe_chunk(Call c, Workspace ws, DevVocab V) {
-  extern __shared__ __align__(16) uint8_t dsm[];
-  ChunkEngine& E = *reinterpret_cast<ChunkEngine*>(dsm);
-  const int tid = threadIdx.x, T = B_THREADS, lane = tid & 31;
-  const long long chunk = blockIdx.x;
-  const long long r0 = chunk * BCHUNK;
+__global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevVocab V) {
+  __shared__ __align__(16) uint8_t text[S_RANGE];
+  __shared__ uint32_t bits[S_RANGE / 32];
+  __shared__ uint16_t fstart[BCHUNK + 1];
+  __shared__ int scan[B_THREADS / 32];
+  __shared__ long long s_last_end;
+  __shared__ uint32_t s_wbase, s_lbase;
+  const int tid = threadIdx.x, T = B_THREADS;
+  const long long r0 = (long long)blockIdx.x * BCHUNK;
   const long long r1 = min(r0 + BCHUNK, c.n);
-  const long long lim = min(r0 + B_RANGE, c.n);
-  for (int b = tid; b < 256; b += T) {
-    const int32_t id = V.byte_id[b];
-    E.byte_id[b] = id;
-    E.byte_ml[b] = V.max_left[id];
-    E.byte_mr[b] = V.max_right[id];
+  const long long lim = min(r0 + S_RANGE, c.n);
+  const int nb = (int)(lim - r0);
+  if (((reinterpret_cast<uintptr_t>(c.text) & 15u) == 0) && nb == S_RANGE) {
+    for (int k = tid; k < S_RANGE / 16; k += T)
+      reinterpret_cast<uint4*>(text)[k] = reinterpret_cast<const uint4*>(c.text + r0)[k];
+  } else {
+    for (int k = tid; k < nb; k += T) text[k] = c.text[r0 + k];
   }
-  if (tid < B_RANGE / 32) {
+  if (tid < S_RANGE / 32) {
     const long long p = r0 + 32ll * tid;
     uint32_t v = 0;
     if (p < lim) {
       v = ws.pstart[(r0 >> 5) + tid];
       if (lim - p < 32) v &= (1u << (lim - p)) - 1u;
     }
-    E.bits[tid] = v;
-  }
-  if (tid == 0) E.sflags = 0;
-  __syncthreads();
-  if (tid < 32) {
-    // first and last fragment start in [r0, r1) (words 0..15), first start in [r1, lim) (16..31)
-    const uint32_t w = E.bits[lane];
-    const uint32_t nz = __ballot_sync(0xffffffffu, lane < BCHUNK / 32 && w != 0u);
-    const uint32_t nz1 = __ballot_sync(0xffffffffu, lane >= BCHUNK / 32 && w != 0u) >> (BCHUNK / 32);
-    if (lane == 0) {
-      long long first = -1, last = -1, end = -1;
-      if (nz) {
-        const int a = __ffs(nz) - 1, b = 31 - __clz(nz);
-        first = r0 + 32ll * a + (__ffs(E.bits[a]) - 1);
-        last = r0 + 32ll * b + (31 - __clz(E.bits[b]));
-      }
-      if (r1 >= c.n) end = c.n;
-      else if (nz1) {
-        const int a = __ffs(nz1) - 1;
-        end = r1 + 32ll * a + (__ffs(E.bits[BCHUNK / 32 + a]) - 1);
-      } else if (lim >= c.n) end = c.n;
-      long long lf = -1;
-      if (first >= 0 && (end < 0 || end - last > B_CAP)) {  // the last fragment is long: queue it
-        lf = last;
-        end = last;
-        const uint32_t q = atomicAdd(&ws.st->long_count, 1u);
-        ws.longq[q] = Frag{last, chunk};
-      }
-      E.first = first;
-      E.end = end;
-      E.longfrag = lf;
-    }
+    bits[tid] = v;
   }
   __syncthreads();
-  const long long fs = E.first;
-  if (fs < 0) {  // no fragment starts here (the chunk lies inside a long fragment)
-    if (tid == 0) {
-      ws.cm_first[chunk] = -1;
-      ws.cm_count[chunk] = 0;
-      ws.cm_long[chunk] = -1;
+  if (tid == 0) {  // end of the last fragment: the first start at or after r1
+    long long e = -1;
+    if (r1 >= c.n) {
+      e = c.n;
+    } else {
+      for (int w = BCHUNK / 32; w < S_RANGE / 32 && e < 0; ++w)
+        if (bits[w]) e = r0 + 32ll * w + (__ffs(bits[w]) - 1);
+      if (e < 0 && lim >= c.n) e = c.n;
     }
-    return;
+    s_last_end = e;
   }
-  const int span = (int)(E.end - fs);
-  const int rel = (int)(fs - r0);
-  for (int i = tid; i < span; i += T) E.text[i] = c.text[fs + i];
-  {  // fragment starts in [fs, min(r1, end)): thread t looks at 4 bit positions
-    const int q0 = tid * 4;
-    const uint32_t nib = (E.bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
-    uint32_t mine = 0;
+  // fragment starts in [r0, r1): thread t looks at 4 bit positions
+  const int q0 = tid * 4;
+  const uint32_t mine = (bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
+  int nf = 0;
+  int idx = block_excl_sum(__popc(mine), &nf, scan);
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (((nib >> q) & 1u) && r0 + q0 + q < E.end) mine |= 1u << q;
-    int nf = 0;
-    int idx = block_excl_sum(__popc(mine), &nf, E.scan);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if ((mine >> q) & 1u) E.fstart[idx++] = (uint16_t)(q0 + q - rel);
-    if (tid == 0) {
-      E.nf = nf;
-      E.fstart[nf] = (uint16_t)span;
-    }
-  }
+  for (int q = 0; q < 4; ++q)
+    if ((mine >> q) & 1u) fstart[idx++] = (uint16_t)(q0 + q);
   __syncthreads();
-  const int nf = E.nf;
-  // settle single bytes and whole tokens (contiguous fragments per thread)
+  // contiguous blocks of at most 4 fragments per thread (nf <= BCHUNK = 4 * T)
   const int FB = (nf + T - 1) / T;
   const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
-  int ubytes = 0, ucount = 0;
-  for (int f = flo; f < fhi; ++f) {
-    const int a = E.fstart[f], L = E.fstart[f + 1] - a;
-    const int t = L == 1 ? E.byte_id[E.text[a]] : whole_lookup(V, E.text + a, L);
-    E.ftok[f] = t;
-    E.fcnt[f] = t >= 0 ? 1 : 0;
-    if (t < 0) { ubytes += L; ++ucount; }
-  }
-  int nu = 0, ub_all = 0;
-  int ui = block_excl_sum(ucount, &nu, E.scan);
-  int uo = block_excl_sum(ubytes, &ub_all, E.scan);
-  for (int f = flo; f < fhi; ++f) {
-    if (E.ftok[f] >= 0) continue;
-    E.ulist[ui] = (uint16_t)f;
-    E.ueoff[ui] = (uint16_t)uo;
-    E.feoff[f] = (uint16_t)uo;
-    ++ui;
-    uo += E.fstart[f + 1] - E.fstart[f];
-  }
-  if (tid == 0) E.ueoff[nu] = (uint16_t)ub_all;
-  __syncthreads();
-
-  // engine batches over the unresolved fragments
-  for (int ub = 0; ub < nu;) {
-    if (tid == 0) {  // largest ue with ueoff[ue] - ueoff[ub] <= B_CAP
-      int a = ub + 1, b = nu;
-      while (a < b) {
-        const int mid = (a + b + 1) >> 1;
-        if (E.ueoff[mid] - E.ueoff[ub] <= B_CAP) a = mid; else b = mid - 1;
-      }
-      E.batch_end = a;
-    }
-    __syncthreads();
-    const int ue = E.batch_end;
-    const int base = E.ueoff[ub];
-    const int M = E.ueoff[ue] - base;
-    for (int i = tid; i < M; i += T) {
-      int a = ub, b = ue - 1;  // fragment k with ueoff[k] <= base + i < ueoff[k+1]
-      while (a < b) {
-        const int mid = (a + b + 1) >> 1;
-        if (E.ueoff[mid] <= base + i) a = mid; else b = mid - 1;
-      }
-      const int f = E.ulist[a];
-      const int j = base + i - E.ueoff[a];
-      const uint8_t byte = E.text[E.fstart[f] + j];
-      E.sym[i] = (uint32_t)E.byte_id[byte];
-      E.len[i] = (uint16_t)(1u | (j == 0 ? FRAG_START : 0u));
-      E.fidx[i] = (uint16_t)f;
-      E.ml[i] = E.byte_ml[byte];
-      E.mr[i] = E.byte_mr[byte];
-    }
-    __syncthreads();
-    for (int i = tid; i < M; i += T)
-      E.kr[i] = (i + 1 >= M || (E.len[i + 1] & FRAG_START)) ? KR_WALL : merge_lookup(V, E.sym[i], E.sym[i + 1]);
-    __syncthreads();
-
-    int m = M;
-    for (int sweep = 0; sweep <= M; ++sweep) {
-      const int B = (m + T - 1) / T;
-      const int lo = min(tid * B, m), hi = min(lo + B, m);
-      // A: any mergeable pair left?  any overlapping equal-rank pairs?
-      int fl2 = 0;
-      for (int i = lo; i < hi; ++i) {
-        const uint32_t k = kr_rank(E.kr[i]);
-        if (mergeable(k)) {
-          fl2 |= 1;
-          if (i > 0 && kr_rank(E.kr[i - 1]) == k) fl2 |= 2;
-        }
-      }
-      fl2 = __reduce_or_sync(0xffffffffu, fl2);
-      if (lane == 0 && fl2) atomicOr(&E.sflags, fl2);
-      __syncthreads();
-      const int flags = E.sflags;
-      if (!(flags & 1)) break;
-      if (flags & 2) {
-        int lastrun = -1;
-        for (int i = lo; i < hi; ++i)
-          if (i == 0 || kr_rank(E.kr[i - 1]) != kr_rank(E.kr[i])) lastrun = i;
-        int run = block_excl_max(lastrun, E.scan);
-        for (int i = lo; i < hi; ++i) {
-          if (i == 0 || kr_rank(E.kr[i - 1]) != kr_rank(E.kr[i])) run = i;
-          E.rs[i] = (uint16_t)run;
-        }
-        __syncthreads();
-      }
-      // B: safe pairs
-      if (V.monotone) {
-        auto mlf = [&](int x) { return (int)E.ml[x]; };
-        auto mrf = [&](int x) { return (int)E.mr[x]; };
-        for (int i = lo; i < hi; ++i) {
-          const uint32_t k = kr_rank(E.kr[i]);
-          const int u = (flags & 2) ? (int)E.rs[i] : i;
-          E.fl[i] = (mergeable(k) && pair_safe(E.len, E.kr, m, i, u, k, mlf, mrf)) ? 1 : 0;
-        }
-      } else {
-        unsigned long long best = ~0ull;
-        for (int i = lo; i < hi; ++i) {
-          const uint32_t k = kr_rank(E.kr[i]);
-          if (mergeable(k)) {
-            const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
-            best = key < best ? key : best;
-          }
-        }
-        best = block_min_u64(best, E.scan64);
-        for (int i = lo; i < hi; ++i) E.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
-      }
-      __syncthreads();
-      // C: merge, look up the new pairs, compact
-      uint32_t nsym[B_EPT];
-      uint16_t nlen[B_EPT], nfi[B_EPT], nml[B_EPT], nmr[B_EPT];
-      unsigned long long nkr[B_EPT];
-      uint32_t keep = 0;
+  uint32_t wmask = 0, lmask = 0;  // fragments of this thread to queue
+  long long flen[4];
 #pragma unroll
-      for (int j = 0; j < B_EPT; ++j) {
-        const int i = lo + j;
-        nsym[j] = 0; nlen[j] = 0; nfi[j] = 0; nml[j] = 0; nmr[j] = 0; nkr[j] = KR_WALL;
-        if (i < hi && !(i > 0 && E.fl[i - 1])) {
-          keep |= 1u << j;
-          const bool mg = E.fl[i] != 0;
-          if (mg) {
-            const uint32_t r = kr_result(E.kr[i]);
-            nsym[j] = r;
-            nlen[j] = (uint16_t)(((E.len[i] & LEN_MASK) + (E.len[i + 1] & LEN_MASK)) | (E.len[i] & FRAG_START));
-            nml[j] = __ldg(V.max_left + r);
-            nmr[j] = __ldg(V.max_right + r);
-          } else {
-            nsym[j] = E.sym[i];
-            nlen[j] = E.len[i];
-            nml[j] = E.ml[i];
-            nmr[j] = E.mr[i];
-          }
-          nfi[j] = E.fidx[i];
-          const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
-          if (jn >= m || (E.len[jn] & FRAG_START)) nkr[j] = KR_WALL;
-          else if (!mg && !E.fl[jn]) nkr[j] = E.kr[i];  // unchanged pair keeps its key
-          else nkr[j] = merge_lookup(V, nsym[j], E.fl[jn] ? kr_result(E.kr[jn]) : E.sym[jn]);
-        }
-      }
-      int newm = 0;
-      const int bpos = block_excl_sum(__popc(keep), &newm, E.scan);
-#pragma unroll
-      for (int j = 0; j < B_EPT; ++j) {
-        if ((keep >> j) & 1u) {
-          const int p = bpos + __popc(keep & ((1u << j) - 1u));
-          E.sym[p] = nsym[j];
-          E.len[p] = nlen[j];
-          E.kr[p] = nkr[j];
-          E.fidx[p] = nfi[j];
-          E.ml[p] = nml[j];
-          E.mr[p] = nmr[j];
-        }
-      }
-      if (tid == 0) E.sflags = 0;
-      m = newm;
-      __syncthreads();
-      if (sweep == M && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
-    }
-    // this batch's results
-    for (int i = tid; i < m; i += T) {
-      const int f = E.fidx[i];
-      if (E.len[i] & FRAG_START) E.feng[f] = (uint16_t)i;
-      atomicAdd(&E.fcnt[f], 1);
-    }
-    __syncthreads();
-    for (int i = tid; i < m; i += T) {
-      const int f = E.fidx[i];
-      E.efinal[E.feoff[f] + (i - E.feng[f])] = E.sym[i];
-    }
-    if (tid == 0) E.sflags = 0;
-    __syncthreads();
-    ub = ue;
-  }
-  // first id of each fragment, then the ids
-  int ids = 0;
-  for (int f = flo; f < fhi; ++f) ids += E.fcnt[f];
-  int total = 0;
-  int oo = block_excl_sum(ids, &total, E.scan);
-  for (int f = flo; f < fhi; ++f) {
-    E.fout[f] = (uint16_t)oo;
-    oo += E.fcnt[f];
-  }
-  __syncthreads();
-  for (int f = tid; f < nf; f += T) {
-    const int o = E.fout[f];
-    if (E.ftok[f] >= 0) {
-      ws.tok[fs + o] = E.ftok[f];
+  for (int j = 0; j < 4; ++j) {
+    const int f = flo + j;
+    flen[j] = 0;
+    if (f >= fhi) continue;
+    const int a = fstart[f];
+    const long long e = (f + 1 < nf) ? r0 + fstart[f + 1] : s_last_end;
+    const long long L = e < 0 ? -1 : e - (r0 + a);
+    flen[j] = L;
+    int t = -1;
+    if (L == 1) t = V.byte_id[text[a]];
+    else if (L > 1 && a + L <= S_RANGE) t = whole_lookup(V, text + a, (int)L);
+    if (t >= 0) {
+      ws.tok[r0 + a] = t;
+      ws.fcnt[r0 + a] = 1;
+    } else if (L > 1 && L <= WCAP) {
+      wmask |= 1u << j;
     } else {
-      const int e0 = E.feoff[f], cnt = E.fcnt[f];
-      for (int j = 0; j < cnt; ++j) ws.tok[fs + o + j] = (int32_t)E.efinal[e0 + j];
+      lmask |= 1u << j;
     }
   }
+  // one queue reservation per CTA and queue
+  int nw = 0, nl = 0;
+  int wi = block_excl_sum(__popc(wmask), &nw, scan);
+  int li = block_excl_sum(__popc(lmask), &nl, scan);
   if (tid == 0) {
-    ws.cm_first[chunk] = fs;
-    ws.cm_count[chunk] = total;
-    ws.cm_long[chunk] = E.longfrag;
+    s_wbase = nw ? atomicAdd(&ws.st->wq_count, (uint32_t)nw) : 0u;
+    s_lbase = nl ? atomicAdd(&ws.st->long_count, (uint32_t)nl) : 0u;
   }
-  // batch: ids before each item start in this chunk (K5 adds the chunk's offset)
-  if (c.item_off) {
-    if (tid == 0) {
-      int a = 0, b = c.n_items + 1;  // first item start >= r0
-      while (a < b) {
-        const int mid = (a + b) >> 1;
-        if (c.item[mid] < r0) a = mid + 1; else b = mid;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int f = flo + j;
+    if ((wmask >> j) & 1u) ws.wq[s_wbase + wi++] = Frag{r0 + fstart[f], flen[j]};
+    if ((lmask >> j) & 1u) ws.longq[s_lbase + li++] = Frag{r0 + fstart[f], flen[j]};
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K3b: queued fragments of at most WCAP bytes, several per warp, through the
+// sweep engine with warp-synchronous steps only.  Lane l owns symbols
+// [W_EPT*l, W_EPT*l + W_EPT) of the batch.
+
+struct WarpEngine {
+  uint32_t sym[WCAP];
+  unsigned long long kr[WCAP];
+  uint16_t len[WCAP];
+  uint16_t ml[WCAP];
+  uint16_t mr[WCAP];
+  uint8_t rs[WCAP];
+  uint8_t fl[WCAP];
+  uint8_t fi[WCAP];        // fragment of each symbol within the batch
+  uint8_t first[W_GRAB + 1];
+  long long fstart[W_GRAB];
+  int foff[W_GRAB + 1];    // fragment offsets in the batch, then its size
+};
+
+__device__ __forceinline__ int warp_excl_sum(int v, int* total) {
+  const int lane = threadIdx.x & 31;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  *total = __shfl_sync(0xffffffffu, inc, 31);
+  return inc - v;
+}
+
+__device__ __forceinline__ int warp_excl_max(int v) {
+  const int lane = threadIdx.x & 31;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc = max(inc, o);
+  }
+  const int ex = __shfl_up_sync(0xffffffffu, inc, 1);
+  return lane == 0 ? -1 : ex;
+}
+
+// Encode the batch described by W.fstart / W.foff (nfrag fragments, M symbols).
+__device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, const DevVocab& V, int nfrag, int M) {
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i < M; i += 32) {
+    int k = 0;
+    while (k + 1 < nfrag && W.foff[k + 1] <= i) ++k;
+    const int j = i - W.foff[k];
+    const int32_t id = __ldg(V.byte_id + c.text[W.fstart[k] + j]);
+    W.sym[i] = (uint32_t)id;
+    W.len[i] = (uint16_t)(1u | (j == 0 ? FRAG_START : 0u));
+    W.fi[i] = (uint8_t)k;
+    W.ml[i] = __ldg(V.max_left + id);
+    W.mr[i] = __ldg(V.max_right + id);
+  }
+  __syncwarp();
+  for (int i = lane; i < M; i += 32)
+    W.kr[i] = (i + 1 >= M || (W.len[i + 1] & FRAG_START)) ? KR_WALL : merge_lookup(V, W.sym[i], W.sym[i + 1]);
+  __syncwarp();
+  int m = M;
+  for (int sweep = 0; sweep <= M; ++sweep) {
+    const int lo = min(lane * W_EPT, m), hi = min(lo + W_EPT, m);
+    bool anyk = false, eq = false;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t k = kr_rank(W.kr[i]);
+      if (mergeable(k)) {
+        anyk = true;
+        if (i > 0 && kr_rank(W.kr[i - 1]) == k) eq = true;
       }
-      E.item0 = a;
     }
-    __syncthreads();
-    for (int k = (int)E.item0 + tid; k <= c.n_items; k += T) {
-      const long long x = c.item[k];
-      if (x >= r1) break;
-      int a = 0, b = nf;  // fragment starting at x (or the long fragment after the last)
-      while (a < b) {
-        const int mid = (a + b) >> 1;
-        if (fs + E.fstart[mid] < x) a = mid + 1; else b = mid;
+    if (!__any_sync(0xffffffffu, anyk)) break;
+    const bool runs = __any_sync(0xffffffffu, eq);
+    if (runs) {
+      int lastrun = -1;
+      for (int i = lo; i < hi; ++i)
+        if (i == 0 || kr_rank(W.kr[i - 1]) != kr_rank(W.kr[i])) lastrun = i;
+      int run = warp_excl_max(lastrun);
+      for (int i = lo; i < hi; ++i) {
+        if (i == 0 || kr_rank(W.kr[i - 1]) != kr_rank(W.kr[i])) run = i;
+        W.rs[i] = (uint8_t)run;
       }
-      c.item_off[k] = a < nf ? E.fout[a] : total;
+      __syncwarp();
+    }
+    if (V.monotone) {
+      auto mlf = [&](int x) { return (int)W.ml[x]; };
+      auto mrf = [&](int x) { return (int)W.mr[x]; };
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t k = kr_rank(W.kr[i]);
+        const int u = runs ? (int)W.rs[i] : i;
+        W.fl[i] = (mergeable(k) && pair_safe(W.len, W.kr, m, i, u, k, mlf, mrf)) ? 1 : 0;
+      }
+    } else {
+      unsigned long long best = ~0ull;
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t k = kr_rank(W.kr[i]);
+        if (mergeable(k)) {
+          const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
+          best = key < best ? key : best;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o < best ? o : best;
+      }
+      for (int i = lo; i < hi; ++i) W.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
+    }
+    __syncwarp();
+    // merge, look up the new pairs, compact (through registers)
+    uint32_t nsym[W_EPT];
+    uint16_t nlen[W_EPT], nml[W_EPT], nmr[W_EPT];
+    uint8_t nfi[W_EPT];
+    unsigned long long nkr[W_EPT];
+    uint32_t keep = 0;
+#pragma unroll
+    for (int j = 0; j < W_EPT; ++j) {
+      const int i = lo + j;
+      nsym[j] = 0; nlen[j] = 0; nml[j] = 0; nmr[j] = 0; nfi[j] = 0; nkr[j] = KR_WALL;
+      if (i < hi && !(i > 0 && W.fl[i - 1])) {
+        keep |= 1u << j;
+        const bool mg = W.fl[i] != 0;
+        if (mg) {
+          const uint32_t r = kr_result(W.kr[i]);
+          nsym[j] = r;
+          nlen[j] = (uint16_t)(((W.len[i] & LEN_MASK) + (W.len[i + 1] & LEN_MASK)) | (W.len[i] & FRAG_START));
+          nml[j] = __ldg(V.max_left + r);
+          nmr[j] = __ldg(V.max_right + r);
+        } else {
+          nsym[j] = W.sym[i];
+          nlen[j] = W.len[i];
+          nml[j] = W.ml[i];
+          nmr[j] = W.mr[i];
+        }
+        nfi[j] = W.fi[i];
+        const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
+        if (jn >= m || (W.len[jn] & FRAG_START)) nkr[j] = KR_WALL;
+        else if (!mg && !W.fl[jn]) nkr[j] = W.kr[i];  // an unchanged pair keeps its key
+        else nkr[j] = merge_lookup(V, nsym[j], W.fl[jn] ? kr_result(W.kr[jn]) : W.sym[jn]);
+      }
+    }
+    int newm = 0;
+    const int base = warp_excl_sum(__popc(keep), &newm);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < W_EPT; ++j) {
+      if ((keep >> j) & 1u) {
+        const int p = base + __popc(keep & ((1u << j) - 1u));
+        W.sym[p] = nsym[j];
+        W.len[p] = nlen[j];
+        W.kr[p] = nkr[j];
+        W.ml[p] = nml[j];
+        W.mr[p] = nmr[j];
+        W.fi[p] = nfi[j];
+      }
+    }
+    m = newm;
+    __syncwarp();
+    if (sweep == M && lane == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
+  }
+  // ids at each fragment's byte offset, and their number
+  for (int i = lane; i < m; i += 32)
+    if (W.len[i] & FRAG_START) W.first[W.fi[i]] = (uint8_t)i;
+  if (lane == 0) W.first[nfrag] = (uint8_t)m;
+  __syncwarp();
+  for (int i = lane; i < m; i += 32) {
+    const int k = W.fi[i];
+    ws.tok[W.fstart[k] + (i - W.first[k])] = (int32_t)W.sym[i];
+  }
+  if (lane < nfrag) ws.fcnt[W.fstart[lane]] = W.first[lane + 1] - W.first[lane];
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(W_WARPS * 32) k_bpe_warp(Call c, Workspace ws, DevVocab V) {
+  __shared__ WarpEngine engines[W_WARPS];
+  WarpEngine& W = engines[threadIdx.x >> 5];
+  const int lane = threadIdx.x & 31;
+  const uint32_t count = *(volatile uint32_t*)&ws.st->wq_count;
+  while (true) {
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&ws.st->wq_taken, (uint32_t)W_GRAB);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (base >= count) break;
+    const int ng = (int)min((uint32_t)W_GRAB, count - base);
+    Frag f{0, 0};
+    if (lane < ng) f = ws.wq[base + lane];
+    // batches of consecutive entries with at most WCAP symbols
+    for (int k0 = 0; k0 < ng;) {
+      const int l = (lane >= k0 && lane < ng) ? (int)f.len : 0;
+      int tot = 0;
+      const int ex = warp_excl_sum(l, &tot);
+      const bool fits = lane >= k0 && lane < ng && ex + l <= WCAP;
+      const uint32_t mask = __ballot_sync(0xffffffffu, fits);
+      const int k1 = k0 + __popc(mask);
+      if (fits) {
+        W.fstart[lane - k0] = f.start;
+        W.foff[lane - k0] = ex;
+      }
+      const int M = __shfl_sync(0xffffffffu, ex + l, k1 - 1);
+      if (lane == 0) W.foff[k1 - k0] = M;
+      __syncwarp();
+      warp_engine(W, c, ws, V, k1 - k0, M);
+      k0 = k1;
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// K4: fragments longer than a chunk engine holds, one CTA each, in global
+// K4: fragments longer than a warp batch holds, one CTA each, in global
 // memory at the fragment's byte offsets (double-buffered)
 
 __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws, DevVocab V) {
@@ -507,10 +464,11 @@ __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws,
     __syncthreads();
     if (idx >= count) break;
     const Frag f = ws.longq[idx];
-    // end: the next fragment start after f.start, or the text end
-    if (tid == 0) s_end = (unsigned long long)c.n;
+    // end: known from the queue entry, or the next fragment start after
+    // f.start (or the text end)
+    if (tid == 0) s_end = f.len > 0 ? (unsigned long long)(f.start + f.len) : (unsigned long long)c.n;
     __syncthreads();
-    const long long w0 = (f.start + 1) >> 5, wn = (c.n + 31) >> 5;
+    const long long w0 = (f.start + 1) >> 5, wn = f.len > 0 ? w0 : (c.n + 31) >> 5;
     for (long long base = w0; base < wn; base += T) {
       const long long wi = base + tid;
       if (wi < wn) {
@@ -609,20 +567,17 @@ __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws,
     }
     const uint32_t* S = cur ? S1 : S0;
     for (int i = tid; i < m; i += T) ws.tok[a + i] = (int32_t)S[i];
-    if (tid == 0) ws.cm_long_count[f.chunk] = m;
+    if (tid == 0) ws.fcnt[a] = m;
     __syncthreads();
   }
 }
 
-void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaFuncSetAttribute(k_bpe_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ChunkEngine));
-    attr_set[dev] = true;
-  }
-  k_bpe_chunk<<<(unsigned)n_bchunks(c.n), B_THREADS, sizeof(ChunkEngine), s>>>(c, w, v);
+void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
+  k_settle<<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
+}
+
+void launch_bpe_warp(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
+  k_bpe_warp<<<n_sms * 8, W_WARPS * 32, 0, s>>>(c, w, v);
 }
 
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {

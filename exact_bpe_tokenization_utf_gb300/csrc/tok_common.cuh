@@ -7,13 +7,16 @@
 //                    "CR/LF later in this whitespace run")
 //   K2 boundaries    UTF-8 validation + per-code-point class + run
 //                    decomposition rules -> fragment-start bitmask (Section 4.1)
-//   K3 bpe_chunk     every fragment that starts in the chunk (and fits in
-//                    ENG_CAP symbols with its neighbours) is encoded by one CTA
-//                    in shared memory, merging all certified-safe pairs per
-//                    sweep; a longer last fragment is queued (Section 4.2)
-//   K4 bpe_long      queued fragments, one CTA each, arrays in global memory
-//   K5 emit          per-chunk token counts -> offsets (decoupled look-back),
-//                    coalesced copy of the ids
+//   K3 settle        per 512-byte chunk: every fragment that is one byte, or
+//                    whose bytes are a token that encodes to itself, is settled
+//                    with one probe; the others are queued (Section 4.2)
+//   K3b bpe_warp     queued fragments of at most 128 bytes, batched per warp,
+//                    merging all certified-safe pairs per sweep
+//   K4 bpe_long      longer fragments, one CTA each, arrays in global memory
+//   K5 emit          per-fragment id counts -> offsets (decoupled look-back
+//                    across chunks), copy of the ids in text order
+// Every tier writes a fragment's ids at the fragment's byte offset in `tok`
+// and their number at the same offset in `fcnt`.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -24,11 +27,13 @@ constexpr int CHUNK = 1024;        // bytes per chunk (every per-chunk kernel)
 constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K1 / K2
 constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
-constexpr int BCHUNK = 512;        // bytes per BPE / emit CTA (K3, K5)
-constexpr int B_RANGE = 2 * BCHUNK;// bytes a K3 CTA covers: its chunk + the tail of its last fragment
-constexpr int B_CAP = 512;         // engine symbols per batch; a longer last fragment goes to K4
+constexpr int BCHUNK = 512;        // bytes per settle / emit CTA (K3, K5)
 constexpr int B_THREADS = 128;
-constexpr int B_EPT = B_CAP / B_THREADS;  // engine symbols per thread at most
+constexpr int WCAP = 128;          // symbols per warp-engine batch; longer fragments go to K4
+constexpr int W_EPT = WCAP / 32;   // symbols per lane
+constexpr int W_WARPS = 4;         // warps per K3b CTA
+constexpr int W_GRAB = 8;          // queue entries a warp takes at a time
+constexpr int S_RANGE = BCHUNK + 256;  // bytes K3 stages: its chunk + the tail of its last fragment
 constexpr int LONG_THREADS = 1024; // K4
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
@@ -71,10 +76,10 @@ struct DevVocab {
   int monotone;               // every merge that uses a token comes after every merge making it
 };
 
-// one queued long fragment: its start; the chunk whose last fragment it is
+// one queued fragment: byte offset and length (-1: end not yet known)
 struct Frag {
   long long start;
-  long long chunk;
+  long long len;
 };
 
 // device-side per-call status and work counters
@@ -84,19 +89,18 @@ struct DevStatus {
   unsigned long long err_off;   // first malformed UTF-8 byte (atomicMin), ~0 if none
   unsigned long long n_ids;
   uint32_t long_count, long_taken;
+  uint32_t wq_count, wq_taken;
   uint32_t emit_ticket, emit_done;
-  uint32_t pad[8];
+  uint32_t pad[6];
 };
 
 struct Workspace {
   uint8_t* text;            // device copy of host input (host entry points)
   uint32_t* csum;           // K1 chunk summaries
   uint32_t* pstart;         // fragment-start bitmask
-  int32_t* tok;             // token ids, compacted per chunk at the chunk's first fragment start
-  long long* cm_first;      // per chunk: first fragment start in it, or -1
-  int32_t* cm_count;        // per chunk: ids K3 produced  (K3 / K5 chunks are BCHUNK bytes)
-  long long* cm_long;       // per chunk: start of its queued long fragment, or -1
-  int32_t* cm_long_count;   // per chunk: ids K4 produced for it
+  int32_t* tok;             // a fragment's ids, at the fragment's byte offset
+  int32_t* fcnt;            // a fragment's number of ids, at its byte offset
+  Frag* wq;                 // K3b queue
   Frag* longq;              // K4 queue
   unsigned long long* lb;   // K5 look-back words
   DevStatus* st;
@@ -215,7 +219,8 @@ __device__ __forceinline__ int utf8_decode(const uint8_t* s, int avail, uint32_t
 // host-side launchers (defined in the kernel translation units)
 void launch_run_summary(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
-void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
+void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
+void launch_bpe_warp(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
 void launch_emit(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);
