@@ -249,6 +249,8 @@ struct WarpEngine {
   uint16_t len[WCAP];
   uint16_t ml[WCAP];
   uint16_t mr[WCAP];
+  uint32_t pmin[WCAP];      // lowest rank from the fragment's first pair to this one
+  uint32_t smin[WCAP];      // lowest rank from this pair to the fragment's last one
   uint8_t rs[WCAP];
   uint8_t fl[WCAP];
   uint8_t fi[WCAP];        // fragment of each symbol within the batch
@@ -284,20 +286,52 @@ __device__ __forceinline__ int warp_excl_max(int v) {
 // Encode the batch described by W.fstart / W.foff (nfrag fragments, M symbols).
 __device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, const DevVocab& V, int nfrag, int M) {
   const int lane = threadIdx.x & 31;
-  for (int i = lane; i < M; i += 32) {
-    int k = 0;
-    while (k + 1 < nfrag && W.foff[k + 1] <= i) ++k;
-    const int j = i - W.foff[k];
-    const int32_t id = __ldg(V.byte_id + c.text[W.fstart[k] + j]);
-    W.sym[i] = (uint32_t)id;
-    W.len[i] = (uint16_t)(1u | (j == 0 ? FRAG_START : 0u));
-    W.fi[i] = (uint8_t)k;
-    W.ml[i] = __ldg(V.max_left + id);
-    W.mr[i] = __ldg(V.max_right + id);
+  {
+    uint32_t id[W_EPT];
+#pragma unroll
+    for (int r = 0; r < W_EPT; ++r) {
+      const int i = lane + 32 * r;
+      id[r] = 0;
+      if (i < M) {
+        int k = 0;
+        while (k + 1 < nfrag && W.foff[k + 1] <= i) ++k;
+        const int j = i - W.foff[k];
+        id[r] = (uint32_t)__ldg(V.byte_id + c.text[W.fstart[k] + j]);
+        W.len[i] = (uint16_t)(1u | (j == 0 ? FRAG_START : 0u));
+        W.fi[i] = (uint8_t)k;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < W_EPT; ++r) {
+      const int i = lane + 32 * r;
+      if (i < M) {
+        W.sym[i] = id[r];
+        W.ml[i] = __ldg(V.max_left + id[r]);
+        W.mr[i] = __ldg(V.max_right + id[r]);
+      }
+    }
   }
   __syncwarp();
-  for (int i = lane; i < M; i += 32)
-    W.kr[i] = (i + 1 >= M || (W.len[i + 1] & FRAG_START)) ? KR_WALL : merge_lookup(V, W.sym[i], W.sym[i + 1]);
+  {
+    uint32_t a[W_EPT], b[W_EPT], valid = 0;
+    unsigned long long kr[W_EPT];
+#pragma unroll
+    for (int r = 0; r < W_EPT; ++r) {
+      const int i = lane + 32 * r;
+      a[r] = 0; b[r] = 0;
+      if (i + 1 < M && !(W.len[i + 1] & FRAG_START)) {
+        a[r] = W.sym[i];
+        b[r] = W.sym[i + 1];
+        valid |= 1u << r;
+      }
+    }
+    merge_lookup_n<W_EPT>(V, a, b, valid, kr);
+#pragma unroll
+    for (int r = 0; r < W_EPT; ++r) {
+      const int i = lane + 32 * r;
+      if (i < M) W.kr[i] = ((valid >> r) & 1u) ? kr[r] : KR_WALL;
+    }
+  }
   __syncwarp();
   int m = M;
   for (int sweep = 0; sweep <= M; ++sweep) {
@@ -324,12 +358,111 @@ __device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, c
       __syncwarp();
     }
     if (V.monotone) {
+      // lowest rank over the pairs of the same fragment to the left (pmin)
+      // and to the right (smin) of each pair; a wall pair is a segment of its
+      // own with no rank
+      uint32_t pm[W_EPT], sm[W_EPT];
+      uint32_t lp = NO_RANK, lflag = 0;  // lane's suffix of prefix-min; segment restarted in lane
+#pragma unroll
+      for (int j = 0; j < W_EPT; ++j) {
+        const int i = lo + j;
+        pm[j] = NO_RANK;
+        if (i < hi) {
+          const uint32_t k = kr_rank(W.kr[i]);
+          const bool wall = k == RANK_WALL;
+          const bool start = i == 0 || wall || kr_rank(W.kr[i - 1]) == RANK_WALL;
+          const uint32_t v = wall ? NO_RANK : k;
+          lp = start ? v : min(lp, v);
+          lflag |= start;
+          pm[j] = lp;
+        }
+      }
+      // carry from lower lanes: the prefix-min of the segment open at the lane's start
+      uint32_t carry = lp, cflag = lflag;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t oc = __shfl_up_sync(0xffffffffu, carry, off);
+        const uint32_t of = __shfl_up_sync(0xffffffffu, cflag, off);
+        if (lane >= off) {
+          if (!cflag) carry = min(carry, oc);
+          cflag |= of;
+        }
+      }
+      uint32_t in = __shfl_up_sync(0xffffffffu, carry, 1);
+      if (lane == 0) in = NO_RANK;
+      bool open = true;  // before the first segment start in this lane
+#pragma unroll
+      for (int j = 0; j < W_EPT; ++j) {
+        const int i = lo + j;
+        if (i < hi) {
+          const uint32_t k = kr_rank(W.kr[i]);
+          const bool start = i == 0 || k == RANK_WALL || kr_rank(W.kr[i - 1]) == RANK_WALL;
+          if (start) open = false;
+          if (open) pm[j] = min(pm[j], in);
+        }
+      }
+      uint32_t ls = NO_RANK, rflag = 0;  // suffix-min, scanning right to left
+#pragma unroll
+      for (int j = W_EPT - 1; j >= 0; --j) {
+        const int i = lo + j;
+        sm[j] = NO_RANK;
+        if (i < hi) {
+          const uint32_t k = kr_rank(W.kr[i]);
+          const bool wall = k == RANK_WALL;
+          const bool end = i + 1 >= m || wall || kr_rank(W.kr[i + 1]) == RANK_WALL;
+          const uint32_t v = wall ? NO_RANK : k;
+          ls = end ? v : min(ls, v);
+          rflag |= end;
+          sm[j] = ls;
+        }
+      }
+      uint32_t carry2 = ls, cflag2 = rflag;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t oc = __shfl_down_sync(0xffffffffu, carry2, off);
+        const uint32_t of = __shfl_down_sync(0xffffffffu, cflag2, off);
+        if (lane + off < 32) {
+          if (!cflag2) carry2 = min(carry2, oc);
+          cflag2 |= of;
+        }
+      }
+      uint32_t in2 = __shfl_down_sync(0xffffffffu, carry2, 1);
+      if (lane == 31) in2 = NO_RANK;
+      bool open2 = true;
+#pragma unroll
+      for (int j = W_EPT - 1; j >= 0; --j) {
+        const int i = lo + j;
+        if (i < hi) {
+          const uint32_t k = kr_rank(W.kr[i]);
+          const bool end = i + 1 >= m || k == RANK_WALL || kr_rank(W.kr[i + 1]) == RANK_WALL;
+          if (end) open2 = false;
+          if (open2) sm[j] = min(sm[j], in2);
+        }
+      }
+      // pm / sm of a pair held by another lane come through shared memory
+#pragma unroll
+      for (int j = 0; j < W_EPT; ++j) {
+        const int i = lo + j;
+        if (i < hi) { W.pmin[i] = pm[j]; W.smin[i] = sm[j]; }
+      }
+      __syncwarp();
       auto mlf = [&](int x) { return (int)W.ml[x]; };
       auto mrf = [&](int x) { return (int)W.mr[x]; };
       for (int i = lo; i < hi; ++i) {
         const uint32_t k = kr_rank(W.kr[i]);
-        const int u = runs ? (int)W.rs[i] : i;
-        W.fl[i] = (mergeable(k) && pair_safe(W.len, W.kr, m, i, u, k, mlf, mrf)) ? 1 : 0;
+        bool safe = false;
+        if (mergeable(k)) {
+          const int u = runs ? (int)W.rs[i] : i;
+          // no lower rank anywhere in the fragment beyond the direct neighbours:
+          // safe without walking the length-bounded windows
+          const bool left_clear = u < 2 || W.pmin[u - 2] >= k;
+          const bool right_clear = i + 2 >= m || W.smin[i + 2] >= k;
+          const bool nbr_ok = ((i - u) & 1) == 0 && (u == 0 || kr_rank(W.kr[u - 1]) >= k) &&
+                              (i + 1 >= m || kr_rank(W.kr[i + 1]) >= k);
+          if (left_clear && right_clear) safe = nbr_ok;
+          else safe = pair_safe(W.len, W.kr, m, i, u, k, mlf, mrf);
+        }
+        W.fl[i] = safe ? 1 : 0;
       }
     } else {
       unsigned long long best = ~0ull;
@@ -354,19 +487,18 @@ __device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, c
     uint8_t nfi[W_EPT];
     unsigned long long nkr[W_EPT];
     uint32_t keep = 0;
+    uint32_t la[W_EPT], lb[W_EPT], need = 0, merged = 0;
 #pragma unroll
     for (int j = 0; j < W_EPT; ++j) {
       const int i = lo + j;
-      nsym[j] = 0; nlen[j] = 0; nml[j] = 0; nmr[j] = 0; nfi[j] = 0; nkr[j] = KR_WALL;
+      nsym[j] = 0; nlen[j] = 0; nml[j] = 0; nmr[j] = 0; nfi[j] = 0; nkr[j] = KR_WALL; la[j] = 0; lb[j] = 0;
       if (i < hi && !(i > 0 && W.fl[i - 1])) {
         keep |= 1u << j;
         const bool mg = W.fl[i] != 0;
         if (mg) {
-          const uint32_t r = kr_result(W.kr[i]);
-          nsym[j] = r;
+          merged |= 1u << j;
+          nsym[j] = kr_result(W.kr[i]);
           nlen[j] = (uint16_t)(((W.len[i] & LEN_MASK) + (W.len[i + 1] & LEN_MASK)) | (W.len[i] & FRAG_START));
-          nml[j] = __ldg(V.max_left + r);
-          nmr[j] = __ldg(V.max_right + r);
         } else {
           nsym[j] = W.sym[i];
           nlen[j] = W.len[i];
@@ -375,10 +507,27 @@ __device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, c
         }
         nfi[j] = W.fi[i];
         const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
-        if (jn >= m || (W.len[jn] & FRAG_START)) nkr[j] = KR_WALL;
-        else if (!mg && !W.fl[jn]) nkr[j] = W.kr[i];  // an unchanged pair keeps its key
-        else nkr[j] = merge_lookup(V, nsym[j], W.fl[jn] ? kr_result(W.kr[jn]) : W.sym[jn]);
+        if (jn >= m || (W.len[jn] & FRAG_START)) {
+          nkr[j] = KR_WALL;
+        } else if (!mg && !W.fl[jn]) {
+          nkr[j] = W.kr[i];  // an unchanged pair keeps its key
+        } else {
+          la[j] = nsym[j];
+          lb[j] = W.fl[jn] ? kr_result(W.kr[jn]) : W.sym[jn];
+          need |= 1u << j;
+        }
       }
+    }
+    // operand bounds of new symbols and keys of new pairs, loads overlapped
+#pragma unroll
+    for (int j = 0; j < W_EPT; ++j)
+      if ((merged >> j) & 1u) { nml[j] = __ldg(V.max_left + nsym[j]); nmr[j] = __ldg(V.max_right + nsym[j]); }
+    {
+      unsigned long long got[W_EPT];
+      merge_lookup_n<W_EPT>(V, la, lb, need, got);
+#pragma unroll
+      for (int j = 0; j < W_EPT; ++j)
+        if ((need >> j) & 1u) nkr[j] = got[j];
     }
     int newm = 0;
     const int base = warp_excl_sum(__popc(keep), &newm);
@@ -412,7 +561,7 @@ __device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, c
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(W_WARPS * 32) k_bpe_warp(Call c, Workspace ws, DevVocab V) {
+__global__ void __launch_bounds__(W_WARPS * 32, 6) k_bpe_warp(Call c, Workspace ws, DevVocab V) {
   __shared__ WarpEngine engines[W_WARPS];
   WarpEngine& W = engines[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
@@ -577,7 +726,7 @@ void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStr
 }
 
 void launch_bpe_warp(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
-  k_bpe_warp<<<n_sms * 8, W_WARPS * 32, 0, s>>>(c, w, v);
+  k_bpe_warp<<<n_sms * 6, W_WARPS * 32, 0, s>>>(c, w, v);
 }
 
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {

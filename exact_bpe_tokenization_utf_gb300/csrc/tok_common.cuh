@@ -184,6 +184,45 @@ __device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s,
   return -1;
 }
 
+// Probe the merge table from slot s on (after a first probe missed).
+static __device__ __noinline__ unsigned long long merge_lookup_from(const DevVocab& v, unsigned long long key, uint32_t s) {
+  const uint32_t mask = (1u << v.bits) - 1u;
+  for (uint32_t probe = 0; probe <= mask; ++probe) {
+    s &= mask;
+    const uint4 e = __ldg(reinterpret_cast<const uint4*>(v.table + s));
+    const unsigned long long k = ((unsigned long long)e.y << 32) | e.x;
+    if (k == key) return ((unsigned long long)e.z << 32) | e.w;
+    if (k == EMPTY_KEY) break;
+    ++s;
+  }
+  return ~0ull;
+}
+
+// N lookups at once: the first probes are all issued before any is used, so
+// their latencies overlap; further probes (rare at load factor <= 1/2) follow.
+template <int N>
+__device__ __forceinline__ void merge_lookup_n(const DevVocab& v, const uint32_t (&a)[N], const uint32_t (&b)[N],
+                                               uint32_t valid, unsigned long long (&out)[N]) {
+  uint4 e[N];
+  unsigned long long key[N];
+  uint32_t slot[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    key[j] = ((unsigned long long)a[j] << 32) | b[j];
+    slot[j] = merge_slot(key[j], v.bits);
+    if ((valid >> j) & 1u) e[j] = __ldg(reinterpret_cast<const uint4*>(v.table + slot[j]));
+  }
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    out[j] = ~0ull;
+    if ((valid >> j) & 1u) {
+      const unsigned long long k = ((unsigned long long)e[j].y << 32) | e[j].x;
+      if (k == key[j]) out[j] = ((unsigned long long)e[j].z << 32) | e[j].w;
+      else if (k != EMPTY_KEY) out[j] = merge_lookup_from(v, key[j], slot[j] + 1);
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t kr_rank(unsigned long long kr) { return (uint32_t)(kr >> 32); }
 __device__ __forceinline__ uint32_t kr_result(unsigned long long kr) { return (uint32_t)kr; }
 
