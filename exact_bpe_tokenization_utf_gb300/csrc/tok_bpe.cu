@@ -144,8 +144,8 @@ __device__ __forceinline__ bool bit_at(const uint32_t* bits, int p) { return (bi
 // Most fragments need no merge loop: a single byte is its byte token, and a
 // fragment whose bytes equal a token t with BPE(bytes(t)) == [t] (checked for
 // every token at load time) encodes to [t].  One thread per fragment settles
-// those with a hash probe; the others are queued for K3b (at most WCAP
-// bytes) or K4.
+// those with a hash probe; the others are queued for K3b (thread tier up to
+// TCAP bytes, warp tier up to WCAP bytes) or K4.
 
 __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevVocab V) {
   __shared__ __align__(16) uint8_t text[S_RANGE];
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
   __shared__ uint16_t fstart[BCHUNK + 1];
   __shared__ int scan[B_THREADS / 32];
   __shared__ long long s_last_end;
-  __shared__ uint32_t s_wbase, s_lbase;
+  __shared__ uint32_t s_tbase, s_wbase, s_lbase;
   const int tid = threadIdx.x, T = B_THREADS;
   const long long r0 = (long long)blockIdx.x * BCHUNK;
   const long long r1 = min(r0 + BCHUNK, c.n);
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
   // contiguous blocks of at most 4 fragments per thread (nf <= BCHUNK = 4 * T)
   const int FB = (nf + T - 1) / T;
   const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
-  uint32_t wmask = 0, lmask = 0;  // fragments of this thread to queue
+  uint32_t tmask = 0, wmask = 0, lmask = 0;  // fragments of this thread to queue
   long long flen[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -215,6 +215,8 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
     if (t >= 0) {
       ws.tok[r0 + a] = t;
       ws.fcnt[r0 + a] = 1;
+    } else if (L > 1 && L <= TCAP) {
+      tmask |= 1u << j;
     } else if (L > 1 && L <= WCAP) {
       wmask |= 1u << j;
     } else {
@@ -222,10 +224,12 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
     }
   }
   // one queue reservation per CTA and queue
-  int nw = 0, nl = 0;
+  int nt = 0, nw = 0, nl = 0;
+  int ti = block_excl_sum(__popc(tmask), &nt, scan);
   int wi = block_excl_sum(__popc(wmask), &nw, scan);
   int li = block_excl_sum(__popc(lmask), &nl, scan);
   if (tid == 0) {
+    s_tbase = nt ? atomicAdd(&ws.st->tq_count, (uint32_t)nt) : 0u;
     s_wbase = nw ? atomicAdd(&ws.st->wq_count, (uint32_t)nw) : 0u;
     s_lbase = nl ? atomicAdd(&ws.st->long_count, (uint32_t)nl) : 0u;
   }
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int f = flo + j;
+    if ((tmask >> j) & 1u) ws.tq[s_tbase + ti++] = Frag{r0 + fstart[f], flen[j]};
     if ((wmask >> j) & 1u) ws.wq[s_wbase + wi++] = Frag{r0 + fstart[f], flen[j]};
     if ((lmask >> j) & 1u) ws.longq[s_lbase + li++] = Frag{r0 + fstart[f], flen[j]};
   }
@@ -561,11 +566,70 @@ __device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, c
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(W_WARPS * 32, 6) k_bpe_warp(Call c, Workspace ws, DevVocab V) {
-  __shared__ WarpEngine engines[W_WARPS];
-  WarpEngine& W = engines[threadIdx.x >> 5];
+// Thread tier: the rule itself (lowest rank first, leftmost on ties), one
+// thread per fragment of at most TCAP bytes, arrays in the warp's shared
+// memory in per-lane columns.  Both lookups a merge needs are issued together.
+struct ThreadArrays {
+  uint32_t sym[TCAP][32];
+  uint32_t rk[TCAP][32];
+  uint32_t res[TCAP][32];
+};
+
+__device__ void bpe_thread(ThreadArrays& A, const Call& c, const Workspace& ws, const DevVocab& V, long long a,
+                           int len) {
+  const int lane = threadIdx.x & 31;
+  for (int k = 0; k < len; ++k) A.sym[k][lane] = (uint32_t)__ldg(V.byte_id + c.text[a + k]);
+  for (int k0 = 0; k0 + 1 < len; k0 += 4) {  // initial pair keys, four probes at a time
+    uint32_t x[4], y[4], valid = 0;
+    unsigned long long got[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = k0 + q;
+      x[q] = 0; y[q] = 0;
+      if (k + 1 < len) { x[q] = A.sym[k][lane]; y[q] = A.sym[k + 1][lane]; valid |= 1u << q; }
+    }
+    merge_lookup_n<4>(V, x, y, valid, got);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if ((valid >> q) & 1u) { A.rk[k0 + q][lane] = kr_rank(got[q]); A.res[k0 + q][lane] = kr_result(got[q]); }
+  }
+  int m = len;
+  while (m > 1) {
+    uint32_t best = NO_RANK;
+    int j = 0;
+    for (int k = 0; k + 1 < m; ++k) {
+      const uint32_t r = A.rk[k][lane];
+      if (r < best) { best = r; j = k; }
+    }
+    if (best == NO_RANK) break;
+    const uint32_t merged = A.res[j][lane];
+    A.sym[j][lane] = merged;
+    for (int k = j + 1; k + 1 < m; ++k) A.sym[k][lane] = A.sym[k + 1][lane];
+    for (int k = j + 1; k + 2 < m; ++k) { A.rk[k][lane] = A.rk[k + 1][lane]; A.res[k][lane] = A.res[k + 1][lane]; }
+    --m;
+    uint32_t x[2] = {j > 0 ? A.sym[j - 1][lane] : 0u, merged};
+    uint32_t y[2] = {merged, j + 1 < m ? A.sym[j + 1][lane] : 0u};
+    const uint32_t valid = (j > 0 ? 1u : 0u) | (j + 1 < m ? 2u : 0u);
+    unsigned long long got[2];
+    merge_lookup_n<2>(V, x, y, valid, got);
+    if (j > 0) { A.rk[j - 1][lane] = kr_rank(got[0]); A.res[j - 1][lane] = kr_result(got[0]); }
+    if (j + 1 < m) { A.rk[j][lane] = kr_rank(got[1]); A.res[j][lane] = kr_result(got[1]); }
+  }
+  for (int k = 0; k < m; ++k) ws.tok[a + k] = (int32_t)A.sym[k][lane];
+  ws.fcnt[a] = m;
+}
+
+union PerWarp {
+  WarpEngine w;
+  ThreadArrays t;
+};
+
+__global__ void __launch_bounds__(W_WARPS * 32, 4) k_bpe_warp(Call c, Workspace ws, DevVocab V) {
+  __shared__ PerWarp per_warp[W_WARPS];
+  WarpEngine& W = per_warp[threadIdx.x >> 5].w;
   const int lane = threadIdx.x & 31;
   const uint32_t count = *(volatile uint32_t*)&ws.st->wq_count;
+  // warp tier first: its batches take longest
   while (true) {
     uint32_t base = 0;
     if (lane == 0) base = atomicAdd(&ws.st->wq_taken, (uint32_t)W_GRAB);
@@ -592,6 +656,21 @@ __global__ void __launch_bounds__(W_WARPS * 32, 6) k_bpe_warp(Call c, Workspace 
       warp_engine(W, c, ws, V, k1 - k0, M);
       k0 = k1;
     }
+  }
+  // then the thread tier, 32 fragments per warp at a time
+  ThreadArrays& A = per_warp[threadIdx.x >> 5].t;
+  const uint32_t tcount = *(volatile uint32_t*)&ws.st->tq_count;
+  __syncwarp();
+  while (true) {
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&ws.st->tq_taken, 32u);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (base >= tcount) break;
+    if (base + lane < tcount) {
+      const Frag f = ws.tq[base + lane];
+      bpe_thread(A, c, ws, V, f.start, (int)f.len);
+    }
+    __syncwarp();
   }
 }
 
@@ -726,7 +805,7 @@ void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStr
 }
 
 void launch_bpe_warp(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
-  k_bpe_warp<<<n_sms * 6, W_WARPS * 32, 0, s>>>(c, w, v);
+  k_bpe_warp<<<n_sms * 4, W_WARPS * 32, 0, s>>>(c, w, v);
 }
 
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {

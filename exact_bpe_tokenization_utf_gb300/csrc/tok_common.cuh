@@ -10,8 +10,9 @@
 //   K3 settle        per 512-byte chunk: every fragment that is one byte, or
 //                    whose bytes are a token that encodes to itself, is settled
 //                    with one probe; the others are queued (Section 4.2)
-//   K3b bpe_warp     queued fragments of at most 128 bytes, batched per warp,
-//                    merging all certified-safe pairs per sweep
+//   K3b bpe_warp     queued fragments: at most 32 bytes one thread each (the
+//                    textbook loop), 33..128 bytes batched per warp through the
+//                    sweep engine (all certified-safe pairs merge per sweep)
 //   K4 bpe_long      longer fragments, one CTA each, arrays in global memory
 //   K5 emit          per-fragment id counts -> offsets (decoupled look-back
 //                    across chunks), copy of the ids in text order
@@ -29,6 +30,7 @@ constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
 constexpr int BCHUNK = 512;        // bytes per settle / emit CTA (K3, K5)
 constexpr int B_THREADS = 128;
+constexpr int TCAP = 32;           // longest fragment of the thread tier
 constexpr int WCAP = 128;          // symbols per warp-engine batch; longer fragments go to K4
 constexpr int W_EPT = WCAP / 32;   // symbols per lane
 constexpr int W_WARPS = 4;         // warps per K3b CTA
@@ -90,8 +92,9 @@ struct DevStatus {
   unsigned long long n_ids;
   uint32_t long_count, long_taken;
   uint32_t wq_count, wq_taken;
+  uint32_t tq_count, tq_taken;
   uint32_t emit_ticket, emit_done;
-  uint32_t pad[6];
+  uint32_t pad[4];
 };
 
 struct Workspace {
@@ -100,7 +103,8 @@ struct Workspace {
   uint32_t* pstart;         // fragment-start bitmask
   int32_t* tok;             // a fragment's ids, at the fragment's byte offset
   int32_t* fcnt;            // a fragment's number of ids, at its byte offset
-  Frag* wq;                 // K3b queue
+  Frag* wq;                 // K3b queue, warp tier
+  Frag* tq;                 // K3b queue, thread tier
   Frag* longq;              // K4 queue
   unsigned long long* lb;   // K5 look-back words
   DevStatus* st;
