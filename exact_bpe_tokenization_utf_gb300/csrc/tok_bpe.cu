@@ -567,66 +567,97 @@ __device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, c
 }
 
 // Thread tier: the rule itself (lowest rank first, leftmost on ties), one
-// thread per fragment of at most TCAP bytes, arrays in the warp's shared
-// memory in per-lane columns.  Both lookups a merge needs are issued together.
-struct ThreadArrays {
-  uint32_t sym[TCAP][32];
-  uint32_t rk[TCAP][32];
-  uint32_t res[TCAP][32];
-};
-
-__device__ void bpe_thread(ThreadArrays& A, const Call& c, const Workspace& ws, const DevVocab& V, long long a,
-                           int len) {
-  const int lane = threadIdx.x & 31;
-  for (int k = 0; k < len; ++k) A.sym[k][lane] = (uint32_t)__ldg(V.byte_id + c.text[a + k]);
-  for (int k0 = 0; k0 + 1 < len; k0 += 4) {  // initial pair keys, four probes at a time
-    uint32_t x[4], y[4], valid = 0;
+// thread per fragment of at most TCAP bytes.  Symbols, pair ranks and pair
+// results stay in registers: the merge position is a one-hot bit mask and
+// every element is updated with masks, so no array is ever indexed by a
+// run-time value (which would move the arrays to local memory).  A merge's
+// two new lookups are issued together.
+__device__ void bpe_thread(const Call& c, const Workspace& ws, const DevVocab& V, long long a, int len) {
+  constexpr int N = TCAP;
+  uint32_t s[N], r[N], x[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) s[k] = k < len ? (uint32_t)__ldg(V.byte_id + c.text[a + k]) : 0u;
+#pragma unroll
+  for (int k0 = 0; k0 < N; k0 += 4) {
+    uint32_t p[4], q[4], valid = 0;
     unsigned long long got[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int k = k0 + q;
-      x[q] = 0; y[q] = 0;
-      if (k + 1 < len) { x[q] = A.sym[k][lane]; y[q] = A.sym[k + 1][lane]; valid |= 1u << q; }
+    for (int t = 0; t < 4; ++t) {
+      const int k = k0 + t;
+      p[t] = k < N ? s[k] : 0u;
+      q[t] = k + 1 < N ? s[k + 1] : 0u;
+      if (k + 1 < len) valid |= 1u << t;
     }
-    merge_lookup_n<4>(V, x, y, valid, got);
+    merge_lookup_n<4>(V, p, q, valid, got);
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if ((valid >> q) & 1u) { A.rk[k0 + q][lane] = kr_rank(got[q]); A.res[k0 + q][lane] = kr_result(got[q]); }
+    for (int t = 0; t < 4; ++t) {
+      const int k = k0 + t;
+      if (k < N) {
+        r[k] = ((valid >> t) & 1u) ? kr_rank(got[t]) : NO_RANK;
+        x[k] = ((valid >> t) & 1u) ? kr_result(got[t]) : 0u;
+      }
+    }
   }
   int m = len;
-  while (m > 1) {
-    uint32_t best = NO_RANK;
-    int j = 0;
-    for (int k = 0; k + 1 < m; ++k) {
-      const uint32_t r = A.rk[k][lane];
-      if (r < best) { best = r; j = k; }
-    }
+  for (int it = 0; it < N; ++it) {
+    // leftmost minimum, as a one-hot mask
+    uint32_t best = r[0];
+#pragma unroll
+    for (int k = 1; k < N - 1; ++k) best = min(best, r[k]);
     if (best == NO_RANK) break;
-    const uint32_t merged = A.res[j][lane];
-    A.sym[j][lane] = merged;
-    for (int k = j + 1; k + 1 < m; ++k) A.sym[k][lane] = A.sym[k + 1][lane];
-    for (int k = j + 1; k + 2 < m; ++k) { A.rk[k][lane] = A.rk[k + 1][lane]; A.res[k][lane] = A.res[k + 1][lane]; }
+    uint32_t hot = 0;
+#pragma unroll
+    for (int k = N - 2; k >= 0; --k) hot = (r[k] == best) ? (1u << k) : hot;
+    // hot has one bit: the leftmost k with r[k] == best
+    uint32_t xj = 0, left = 0, right = 0;
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const uint32_t mj = 0u - ((hot >> k) & 1u);
+      const uint32_t ml = k + 1 < N ? 0u - ((hot >> (k + 1)) & 1u) : 0u;
+      const uint32_t mr = k >= 2 ? 0u - ((hot >> (k - 2)) & 1u) : 0u;
+      xj |= x[k] & mj;
+      left |= s[k] & ml;
+      right |= s[k] & mr;
+    }
+    const uint32_t below = hot - 1u;       // k < j
+    const uint32_t above = ~(below | hot); // k > j
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const uint32_t ms = 0u - ((hot >> k) & 1u);
+      const uint32_t ma = 0u - ((above >> k) & 1u);
+      const uint32_t ns = k + 1 < N ? s[k + 1] : 0u;
+      const uint32_t nr = k + 1 < N ? r[k + 1] : NO_RANK;
+      const uint32_t nx = k + 1 < N ? x[k + 1] : 0u;
+      s[k] = (s[k] & ~(ms | ma)) | (xj & ms) | (ns & ma);
+      r[k] = (r[k] & ~ma) | (nr & ma);
+      x[k] = (x[k] & ~ma) | (nx & ma);
+    }
     --m;
-    uint32_t x[2] = {j > 0 ? A.sym[j - 1][lane] : 0u, merged};
-    uint32_t y[2] = {merged, j + 1 < m ? A.sym[j + 1][lane] : 0u};
-    const uint32_t valid = (j > 0 ? 1u : 0u) | (j + 1 < m ? 2u : 0u);
+    const bool has_left = hot > 1u;
+    const bool has_right = (above & ((1u << m) - 1u)) != 0u;  // a symbol follows the new one
+    uint32_t p2[2] = {left, xj}, q2[2] = {xj, right};
+    const uint32_t valid = (has_left ? 1u : 0u) | (has_right ? 2u : 0u);
     unsigned long long got[2];
-    merge_lookup_n<2>(V, x, y, valid, got);
-    if (j > 0) { A.rk[j - 1][lane] = kr_rank(got[0]); A.res[j - 1][lane] = kr_result(got[0]); }
-    if (j + 1 < m) { A.rk[j][lane] = kr_rank(got[1]); A.res[j][lane] = kr_result(got[1]); }
+    merge_lookup_n<2>(V, p2, q2, valid, got);
+    const uint32_t rl = kr_rank(got[0]), xl = kr_result(got[0]);
+    const uint32_t rr = has_right ? kr_rank(got[1]) : NO_RANK, xr = has_right ? kr_result(got[1]) : 0u;
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const uint32_t ml = k + 1 < N ? 0u - ((hot >> (k + 1)) & 1u) : 0u;  // k == j - 1
+      const uint32_t mj = 0u - ((hot >> k) & 1u);
+      r[k] = (r[k] & ~(ml | mj)) | (rl & ml) | (rr & mj);
+      x[k] = (x[k] & ~(ml | mj)) | (xl & ml) | (xr & mj);
+    }
   }
-  for (int k = 0; k < m; ++k) ws.tok[a + k] = (int32_t)A.sym[k][lane];
+#pragma unroll
+  for (int k = 0; k < N; ++k)
+    if (k < m) ws.tok[a + k] = (int32_t)s[k];
   ws.fcnt[a] = m;
 }
 
-union PerWarp {
-  WarpEngine w;
-  ThreadArrays t;
-};
-
 __global__ void __launch_bounds__(W_WARPS * 32, 4) k_bpe_warp(Call c, Workspace ws, DevVocab V) {
-  __shared__ PerWarp per_warp[W_WARPS];
-  WarpEngine& W = per_warp[threadIdx.x >> 5].w;
+  __shared__ WarpEngine engines[W_WARPS];
+  WarpEngine& W = engines[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
   const uint32_t count = *(volatile uint32_t*)&ws.st->wq_count;
   // warp tier first: its batches take longest
@@ -658,7 +689,6 @@ __global__ void __launch_bounds__(W_WARPS * 32, 4) k_bpe_warp(Call c, Workspace 
     }
   }
   // then the thread tier, 32 fragments per warp at a time
-  ThreadArrays& A = per_warp[threadIdx.x >> 5].t;
   const uint32_t tcount = *(volatile uint32_t*)&ws.st->tq_count;
   __syncwarp();
   while (true) {
@@ -668,7 +698,7 @@ __global__ void __launch_bounds__(W_WARPS * 32, 4) k_bpe_warp(Call c, Workspace 
     if (base >= tcount) break;
     if (base + lane < tcount) {
       const Frag f = ws.tq[base + lane];
-      bpe_thread(A, c, ws, V, f.start, (int)f.len);
+      bpe_thread(c, ws, V, f.start, (int)f.len);
     }
     __syncwarp();
   }

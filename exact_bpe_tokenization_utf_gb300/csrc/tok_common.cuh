@@ -10,8 +10,8 @@
 //   K3 settle        per 512-byte chunk: every fragment that is one byte, or
 //                    whose bytes are a token that encodes to itself, is settled
 //                    with one probe; the others are queued (Section 4.2)
-//   K3b bpe_warp     queued fragments: at most 32 bytes one thread each (the
-//                    textbook loop), 33..128 bytes batched per warp through the
+//   K3b bpe_warp     queued fragments: at most 16 bytes one thread each (the
+//                    textbook loop in registers), 17..128 bytes batched per warp through the
 //                    sweep engine (all certified-safe pairs merge per sweep)
 //   K4 bpe_long      longer fragments, one CTA each, arrays in global memory
 //   K5 emit          per-fragment id counts -> offsets (decoupled look-back
@@ -30,7 +30,7 @@ constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
 constexpr int BCHUNK = 512;        // bytes per settle / emit CTA (K3, K5)
 constexpr int B_THREADS = 128;
-constexpr int TCAP = 32;           // longest fragment of the thread tier
+constexpr int TCAP = 16;           // longest fragment of the thread tier (symbols in registers)
 constexpr int WCAP = 128;          // symbols per warp-engine batch; longer fragments go to K4
 constexpr int W_EPT = WCAP / 32;   // symbols per lane
 constexpr int W_WARPS = 4;         // warps per K3b CTA
@@ -189,7 +189,7 @@ __device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s,
 }
 
 // Probe the merge table from slot s on (after a first probe missed).
-static __device__ __noinline__ unsigned long long merge_lookup_from(const DevVocab& v, unsigned long long key, uint32_t s) {
+static __device__ __forceinline__ unsigned long long merge_lookup_from(const DevVocab& v, unsigned long long key, uint32_t s) {
   const uint32_t mask = (1u << v.bits) - 1u;
   for (uint32_t probe = 0; probe <= mask; ++probe) {
     s &= mask;
