@@ -108,7 +108,7 @@ cudaError_t dalloc(T** p, size_t count) {
 
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
-  void* ptrs[] = {w.text,     w.csum,     w.pstart,   w.tok,      w.fcnt,     w.wq,   w.tq,   w.longq,
+  void* ptrs[] = {w.text,     w.csum,     w.pstart,   w.tok,      w.fcnt,     w.q[0], w.q[1], w.q[2], w.q[3], w.q[4],
                   w.lb,       w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1], w.e_kr[0],
                   w.e_kr[1],  w.e_fl,     w.e_rs,     h->d_out};
   for (void* p : ptrs)
@@ -134,9 +134,11 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.pstart, cap / 32 + pad));
   chk(dalloc(&w.tok, cap + pad));
   chk(dalloc(&w.fcnt, cap + pad));
-  chk(dalloc(&w.wq, cap / (TCAP + 1) + pad));
-  chk(dalloc(&w.tq, cap / 2 + pad));
-  chk(dalloc(&w.longq, cap / (WCAP + 1) + nbch + pad));
+  chk(dalloc(&w.q[0], cap / 2 + pad));
+  chk(dalloc(&w.q[1], cap / 9 + pad));
+  chk(dalloc(&w.q[2], cap / 17 + pad));
+  chk(dalloc(&w.q[3], cap / 33 + pad));
+  chk(dalloc(&w.q[Q_LONG], cap / (WCAP + 1) + nbch + pad));
   chk(dalloc(&w.lb, nbch + 2));
   chk(dalloc(&w.st, 1));
   for (int b = 0; b < 2; ++b) {

@@ -3,8 +3,9 @@
 // lowest-rank adjacent pair (leftmost on ties) until no adjacent pair is a
 // merge.  The pages tier fragments by length (one thread, one warp, one block
 // per fragment); here a fragment is settled by one probe when it is a single
-// byte or a whole self-encoding token, otherwise batched with others into one
-// warp (<= 128 bytes) or given a CTA (longer).
+// byte or a whole self-encoding token; otherwise it gets one lane per symbol
+// in a segment of 8, 16 or 32 lanes (<= 32 bytes), a share of a warp batch
+// (<= 128 bytes), or a CTA (longer).
 //
 // Sweep engine.  The symbols of many fragments sit in one array; the pair
 // between two fragments is a "wall" that never merges.  Let k be the rank of
@@ -121,6 +122,28 @@ __device__ __forceinline__ int block_excl_max(int v, int* sh) {
   return lane == 0 ? pre : max(pre, ex);
 }
 
+__device__ __forceinline__ unsigned long long block_excl_sum64(unsigned long long v, unsigned long long* total,
+                                                               unsigned long long* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned long long inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  unsigned long long pre = 0, tot = 0;
+  for (int k = 0; k < nw; ++k) {
+    const unsigned long long x = sh[k];
+    pre += k < warp ? x : 0ull;
+    tot += x;
+  }
+  *total = tot;
+  __syncthreads();
+  return pre + inc - v;
+}
+
 __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v, unsigned long long* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
@@ -144,8 +167,8 @@ __device__ __forceinline__ bool bit_at(const uint32_t* bits, int p) { return (bi
 // Most fragments need no merge loop: a single byte is its byte token, and a
 // fragment whose bytes equal a token t with BPE(bytes(t)) == [t] (checked for
 // every token at load time) encodes to [t].  One thread per fragment settles
-// those with a hash probe; the others are queued for K3b (thread tier up to
-// TCAP bytes, warp tier up to WCAP bytes) or K4.
+// those with a hash probe; the others are queued by length for K3b (segment
+// engine up to 32 bytes, warp engine up to WCAP bytes) or K4.
 
 __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevVocab V) {
   __shared__ __align__(16) uint8_t text[S_RANGE];
@@ -153,7 +176,8 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
   __shared__ uint16_t fstart[BCHUNK + 1];
   __shared__ int scan[B_THREADS / 32];
   __shared__ long long s_last_end;
-  __shared__ uint32_t s_tbase, s_wbase, s_lbase;
+  __shared__ uint32_t s_qbase[5];
+  __shared__ unsigned long long scan64[B_THREADS / 32];
   const int tid = threadIdx.x, T = B_THREADS;
   const long long r0 = (long long)blockIdx.x * BCHUNK;
   const long long r1 = min(r0 + BCHUNK, c.n);
@@ -198,12 +222,13 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
   // contiguous blocks of at most 4 fragments per thread (nf <= BCHUNK = 4 * T)
   const int FB = (nf + T - 1) / T;
   const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
-  uint32_t tmask = 0, wmask = 0, lmask = 0;  // fragments of this thread to queue
+  int qcls[4];                                // queue of each of this thread's fragments, or -1
   long long flen[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int f = flo + j;
     flen[j] = 0;
+    qcls[j] = -1;
     if (f >= fhi) continue;
     const int a = fstart[f];
     const long long e = (f + 1 < nf) ? r0 + fstart[f + 1] : s_last_end;
@@ -215,31 +240,31 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
     if (t >= 0) {
       ws.tok[r0 + a] = t;
       ws.fcnt[r0 + a] = 1;
-    } else if (L > 1 && L <= TCAP) {
-      tmask |= 1u << j;
-    } else if (L > 1 && L <= WCAP) {
-      wmask |= 1u << j;
     } else {
-      lmask |= 1u << j;
+      qcls[j] = (L > 1 && L <= 8) ? 0 : (L > 1 && L <= 16) ? 1 : (L > 1 && L <= 32) ? 2
+              : (L > 1 && L <= WCAP) ? 3 : Q_LONG;
     }
   }
-  // one queue reservation per CTA and queue
-  int nt = 0, nw = 0, nl = 0;
-  int ti = block_excl_sum(__popc(tmask), &nt, scan);
-  int wi = block_excl_sum(__popc(wmask), &nw, scan);
-  int li = block_excl_sum(__popc(lmask), &nl, scan);
-  if (tid == 0) {
-    s_tbase = nt ? atomicAdd(&ws.st->tq_count, (uint32_t)nt) : 0u;
-    s_wbase = nw ? atomicAdd(&ws.st->wq_count, (uint32_t)nw) : 0u;
-    s_lbase = nl ? atomicAdd(&ws.st->long_count, (uint32_t)nl) : 0u;
+  // one queue reservation per CTA and queue: five 10-bit counts in one scan
+  unsigned long long mine_q = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (qcls[j] >= 0) mine_q += 1ull << (10 * qcls[j]);
+  unsigned long long tot_q = 0;
+  unsigned long long pos_q = block_excl_sum64(mine_q, &tot_q, scan64);
+  if (tid < 5) {
+    const uint32_t cnt = (uint32_t)(tot_q >> (10 * tid)) & 1023u;
+    s_qbase[tid] = cnt ? atomicAdd(&ws.st->qcount[tid], cnt) : 0u;
   }
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const int f = flo + j;
-    if ((tmask >> j) & 1u) ws.tq[s_tbase + ti++] = Frag{r0 + fstart[f], flen[j]};
-    if ((wmask >> j) & 1u) ws.wq[s_wbase + wi++] = Frag{r0 + fstart[f], flen[j]};
-    if ((lmask >> j) & 1u) ws.longq[s_lbase + li++] = Frag{r0 + fstart[f], flen[j]};
+    const int qc = qcls[j];
+    if (qc >= 0) {
+      const uint32_t slot = s_qbase[qc] + ((uint32_t)(pos_q >> (10 * qc)) & 1023u);
+      pos_q += 1ull << (10 * qc);
+      ws.q[qc][slot] = Frag{r0 + fstart[flo + j], flen[j]};
+    }
   }
 }
 
@@ -566,109 +591,196 @@ __device__ void warp_engine(WarpEngine& W, const Call& c, const Workspace& ws, c
   __syncwarp();
 }
 
-// Thread tier: the rule itself (lowest rank first, leftmost on ties), one
-// thread per fragment of at most TCAP bytes.  Symbols, pair ranks and pair
-// results stay in registers: the merge position is a one-hot bit mask and
-// every element is updated with masks, so no array is ever indexed by a
-// run-time value (which would move the arrays to local memory).  A merge's
-// two new lookups are issued together.
-__device__ void bpe_thread(const Call& c, const Workspace& ws, const DevVocab& V, long long a, int len) {
-  constexpr int N = TCAP;
-  uint32_t s[N], r[N], x[N];
+// Segment engine: fragments of at most W bytes (W in {8, 16, 32}), one symbol
+// per lane, 32 / W fragments per warp, each in its own W-lane segment.  The
+// same sweep as the warp engine (every certified-safe pair merges), with all
+// neighbour access through segment-local shuffles.
+template <int W>
+__device__ void segment_engine(const Call& c, const Workspace& ws, const DevVocab& V, long long a, int len) {
+  const int lane = threadIdx.x & 31;
+  const int i = lane & (W - 1);              // position in the segment
+  const int seg0 = lane & ~(W - 1);          // first lane of the segment
+  const uint32_t segbits = (W == 32 ? 0xffffffffu : ((1u << W) - 1u)) << seg0;
+  int m = len;                               // symbols in this segment (0: no fragment)
+  uint32_t sym = 0, mlv = 0, mrv = 0, lenb = 0;
+  if (i < m) {
+    const int32_t id = __ldg(V.byte_id + c.text[a + i]);
+    sym = (uint32_t)id;
+    mlv = __ldg(V.max_left + id);
+    mrv = __ldg(V.max_right + id);
+    lenb = 1;
+  }
+  unsigned long long kr = KR_WALL;
+  {
+    const uint32_t nxt = __shfl_down_sync(0xffffffffu, sym, 1, W);
+    uint32_t p[1] = {sym}, q[1] = {nxt};
+    unsigned long long got[1];
+    merge_lookup_n<1>(V, p, q, (i + 1 < m) ? 1u : 0u, got);
+    if (i + 1 < m) kr = got[0];
+  }
+  for (int sweep = 0; sweep <= W; ++sweep) {
+    const uint32_t k = kr_rank(kr);
+    const bool mrg = i + 1 < m && mergeable(k);
+    if (!__any_sync(0xffffffffu, mrg)) break;
+    // ranks of the neighbouring pairs
+    const uint32_t kl = __shfl_up_sync(0xffffffffu, k, 1, W);
+    const uint32_t kn = __shfl_down_sync(0xffffffffu, k, 1, W);
+    // run start of equal-rank pairs (runs of one symbol x with merge (x,x))
+    int u = i;
+    const bool eq = mrg && i > 0 && kl == k;
+    if (__any_sync(0xffffffffu, eq)) {
+      int st = (i + 1 < m && !(i > 0 && kl == k)) ? i : -1;
 #pragma unroll
-  for (int k = 0; k < N; ++k) s[k] = k < len ? (uint32_t)__ldg(V.byte_id + c.text[a + k]) : 0u;
-#pragma unroll
-  for (int k0 = 0; k0 < N; k0 += 4) {
-    uint32_t p[4], q[4], valid = 0;
-    unsigned long long got[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int k = k0 + t;
-      p[t] = k < N ? s[k] : 0u;
-      q[t] = k + 1 < N ? s[k + 1] : 0u;
-      if (k + 1 < len) valid |= 1u << t;
-    }
-    merge_lookup_n<4>(V, p, q, valid, got);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int k = k0 + t;
-      if (k < N) {
-        r[k] = ((valid >> t) & 1u) ? kr_rank(got[t]) : NO_RANK;
-        x[k] = ((valid >> t) & 1u) ? kr_result(got[t]) : 0u;
+      for (int off = 1; off < W; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, st, off, W);
+        if (i >= off) st = max(st, o);
       }
+      u = st < 0 ? i : st;
     }
+    // lowest rank over pairs [0, x] (pm) and [x, m-2] (sm) of the fragment
+    const uint32_t kv = (i + 1 < m) ? k : NO_RANK;
+    uint32_t pm = kv, sm = kv;
+#pragma unroll
+    for (int off = 1; off < W; off <<= 1) {
+      const uint32_t o1 = __shfl_up_sync(0xffffffffu, pm, off, W);
+      const uint32_t o2 = __shfl_down_sync(0xffffffffu, sm, off, W);
+      if (i >= off) pm = min(pm, o1);
+      if (i + off < W) sm = min(sm, o2);
+    }
+    const uint32_t pm_u2 = __shfl_sync(0xffffffffu, pm, seg0 + max(u - 2, 0));
+    const uint32_t kl_u = __shfl_sync(0xffffffffu, k, seg0 + max(u - 1, 0));
+    const uint32_t sm_i2 = __shfl_down_sync(0xffffffffu, sm, 2, W);
+    const uint32_t ml_u = __shfl_sync(0xffffffffu, mlv, seg0 + u);
+    const uint32_t mr_i1 = __shfl_down_sync(0xffffffffu, mrv, 1, W);
+    bool safe = false;
+    bool need_scan = false;
+    if (mrg) {
+      const bool nbr_ok = ((i - u) & 1) == 0 && (u == 0 || kl_u >= k) && (i + 2 >= m || kn >= k);
+      const bool left_clear = u < 2 || pm_u2 >= k;
+      const bool right_clear = i + 3 >= m || sm_i2 >= k;
+      safe = nbr_ok && left_clear && right_clear;
+      need_scan = nbr_ok && !(left_clear && right_clear);
+    }
+    // exact length-bounded windows where a lower rank exists further away
+    if (__any_sync(0xffffffffu, need_scan)) {
+      bool ok = need_scan;
+      // left: initiator pair q <= u-2 grows a token ending at u-1
+      int cum = __shfl_sync(0xffffffffu, (int)lenb, seg0 + max(u - 1, 0));
+      bool done = !(need_scan && u >= 2);
+      for (int step = 2; step < W; ++step) {
+        const int q = u - step;
+        const int qq = max(q, 0);
+        const uint32_t kq = __shfl_sync(0xffffffffu, k, seg0 + qq);
+        const int lq = __shfl_sync(0xffffffffu, (int)lenb, seg0 + qq);
+        if (!done) {
+          if (q < 0) done = true;
+          else {
+            cum += lq;
+            if (cum > (int)ml_u) done = true;
+            else if (kq < k) { ok = false; done = true; }
+          }
+        }
+        if (!__any_sync(0xffffffffu, !done)) break;
+      }
+      // right: initiator pair q >= i+2 grows a token starting at i+2
+      cum = __shfl_sync(0xffffffffu, (int)lenb, seg0 + min(i + 2, W - 1));
+      done = !(need_scan && ok && i + 3 < m);
+      for (int step = 2; step < W; ++step) {
+        const int q = i + step;
+        const int qq = min(q, W - 1);
+        const uint32_t kq = __shfl_sync(0xffffffffu, k, seg0 + qq);
+        const int lq = __shfl_sync(0xffffffffu, (int)lenb, seg0 + min(q + 1, W - 1));
+        if (!done) {
+          if (q >= m - 1) done = true;
+          else {
+            cum += lq;
+            if (cum > (int)mr_i1) done = true;
+            else if (kq < k) { ok = false; done = true; }
+          }
+        }
+        if (!__any_sync(0xffffffffu, !done)) break;
+      }
+      if (need_scan) safe = ok;
+    }
+    if (!V.monotone) {
+      // the rule itself: only the leftmost minimum pair of each fragment
+      uint32_t best = mrg ? k : NO_RANK;
+      int bi = i;
+#pragma unroll
+      for (int off = W / 2; off > 0; off >>= 1) {
+        const uint32_t ob = __shfl_xor_sync(0xffffffffu, best, off, W);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off, W);
+        if (ob < best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+      }
+      safe = mrg && bi == i;
+    }
+    // merge: a safe pair's left symbol takes the result, its right one goes
+    const bool dead = __shfl_up_sync(0xffffffffu, safe ? 1 : 0, 1, W) != 0 && i > 0;
+    const uint32_t nlen = lenb + (safe ? (uint32_t)__shfl_down_sync(0xffffffffu, (int)lenb, 1, W) : 0u);
+    uint32_t nsym = safe ? kr_result(kr) : sym;
+    const bool keep = i < m && !dead;
+    const uint32_t km = (__ballot_sync(0xffffffffu, keep) & segbits) >> seg0;
+    const bool chg = safe;
+    const int newm = __popc(km);
+    // compaction: new position p takes the (p+1)-th survivor
+    const int src = i < newm ? (int)__fns(km, 0, i + 1) : i;
+    nsym = __shfl_sync(0xffffffffu, nsym, seg0 + src);
+    const uint32_t nl2 = __shfl_sync(0xffffffffu, nlen, seg0 + src);
+    const bool c2 = __shfl_sync(0xffffffffu, chg ? 1 : 0, seg0 + src) != 0;
+    const unsigned long long okr = __shfl_sync(0xffffffffu, kr, seg0 + src);
+    uint32_t nml = __shfl_sync(0xffffffffu, mlv, seg0 + src);
+    uint32_t nmr = __shfl_sync(0xffffffffu, mrv, seg0 + src);
+    m = newm;
+    sym = i < m ? nsym : 0u;
+    lenb = i < m ? nl2 : 0u;
+    if (i < m && c2) { nml = __ldg(V.max_left + sym); nmr = __ldg(V.max_right + sym); }
+    mlv = nml;
+    mrv = nmr;
+    // keys: unchanged pairs keep theirs, pairs touching a new symbol are looked up
+    const bool c_next = __shfl_down_sync(0xffffffffu, c2 ? 1 : 0, 1, W) != 0;
+    const uint32_t nxt = __shfl_down_sync(0xffffffffu, sym, 1, W);
+    const bool look = i + 1 < m && (c2 || c_next);
+    uint32_t p[1] = {sym}, q[1] = {nxt};
+    unsigned long long got[1];
+    merge_lookup_n<1>(V, p, q, look ? 1u : 0u, got);
+    kr = (i + 1 < m) ? (look ? got[0] : okr) : KR_WALL;
+    if (sweep == W && i == 0 && m > 1) atomicExch(&ws.st->code, ST_EINTERNAL);
   }
-  int m = len;
-  for (int it = 0; it < N; ++it) {
-    // leftmost minimum, as a one-hot mask
-    uint32_t best = r[0];
-#pragma unroll
-    for (int k = 1; k < N - 1; ++k) best = min(best, r[k]);
-    if (best == NO_RANK) break;
-    uint32_t hot = 0;
-#pragma unroll
-    for (int k = N - 2; k >= 0; --k) hot = (r[k] == best) ? (1u << k) : hot;
-    // hot has one bit: the leftmost k with r[k] == best
-    uint32_t xj = 0, left = 0, right = 0;
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-      const uint32_t mj = 0u - ((hot >> k) & 1u);
-      const uint32_t ml = k + 1 < N ? 0u - ((hot >> (k + 1)) & 1u) : 0u;
-      const uint32_t mr = k >= 2 ? 0u - ((hot >> (k - 2)) & 1u) : 0u;
-      xj |= x[k] & mj;
-      left |= s[k] & ml;
-      right |= s[k] & mr;
-    }
-    const uint32_t below = hot - 1u;       // k < j
-    const uint32_t above = ~(below | hot); // k > j
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-      const uint32_t ms = 0u - ((hot >> k) & 1u);
-      const uint32_t ma = 0u - ((above >> k) & 1u);
-      const uint32_t ns = k + 1 < N ? s[k + 1] : 0u;
-      const uint32_t nr = k + 1 < N ? r[k + 1] : NO_RANK;
-      const uint32_t nx = k + 1 < N ? x[k + 1] : 0u;
-      s[k] = (s[k] & ~(ms | ma)) | (xj & ms) | (ns & ma);
-      r[k] = (r[k] & ~ma) | (nr & ma);
-      x[k] = (x[k] & ~ma) | (nx & ma);
-    }
-    --m;
-    const bool has_left = hot > 1u;
-    const bool has_right = (above & ((1u << m) - 1u)) != 0u;  // a symbol follows the new one
-    uint32_t p2[2] = {left, xj}, q2[2] = {xj, right};
-    const uint32_t valid = (has_left ? 1u : 0u) | (has_right ? 2u : 0u);
-    unsigned long long got[2];
-    merge_lookup_n<2>(V, p2, q2, valid, got);
-    const uint32_t rl = kr_rank(got[0]), xl = kr_result(got[0]);
-    const uint32_t rr = has_right ? kr_rank(got[1]) : NO_RANK, xr = has_right ? kr_result(got[1]) : 0u;
-#pragma unroll
-    for (int k = 0; k < N; ++k) {
-      const uint32_t ml = k + 1 < N ? 0u - ((hot >> (k + 1)) & 1u) : 0u;  // k == j - 1
-      const uint32_t mj = 0u - ((hot >> k) & 1u);
-      r[k] = (r[k] & ~(ml | mj)) | (rl & ml) | (rr & mj);
-      x[k] = (x[k] & ~(ml | mj)) | (xl & ml) | (xr & mj);
-    }
+  if (i < m) ws.tok[a + i] = (int32_t)sym;
+  if (i == 0 && len > 0) ws.fcnt[a] = m;
+}
+
+template <int W>
+__device__ void drain_segment_queue(const Call& c, const Workspace& ws, const DevVocab& V, int qi) {
+  constexpr int PER = 32 / W;  // fragments per warp
+  const int lane = threadIdx.x & 31;
+  const uint32_t count = *(volatile uint32_t*)&ws.st->qcount[qi];
+  while (true) {
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&ws.st->qtaken[qi], (uint32_t)PER);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (base >= count) break;
+    const uint32_t k = base + (uint32_t)(lane / W);
+    Frag f{0, 0};
+    if (k < count) f = ws.q[qi][k];
+    segment_engine<W>(c, ws, V, f.start, (int)f.len);
   }
-#pragma unroll
-  for (int k = 0; k < N; ++k)
-    if (k < m) ws.tok[a + k] = (int32_t)s[k];
-  ws.fcnt[a] = m;
 }
 
 __global__ void __launch_bounds__(W_WARPS * 32, 4) k_bpe_warp(Call c, Workspace ws, DevVocab V) {
   __shared__ WarpEngine engines[W_WARPS];
   WarpEngine& W = engines[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
-  const uint32_t count = *(volatile uint32_t*)&ws.st->wq_count;
-  // warp tier first: its batches take longest
+  const uint32_t count = *(volatile uint32_t*)&ws.st->qcount[3];
+  // longest fragments first: warp engine (33..128 bytes), then segments of 32, 16, 8
   while (true) {
     uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&ws.st->wq_taken, (uint32_t)W_GRAB);
+    if (lane == 0) base = atomicAdd(&ws.st->qtaken[3], (uint32_t)W_GRAB);
     base = __shfl_sync(0xffffffffu, base, 0);
     if (base >= count) break;
     const int ng = (int)min((uint32_t)W_GRAB, count - base);
     Frag f{0, 0};
-    if (lane < ng) f = ws.wq[base + lane];
+    if (lane < ng) f = ws.q[3][base + lane];
     // batches of consecutive entries with at most WCAP symbols
     for (int k0 = 0; k0 < ng;) {
       const int l = (lane >= k0 && lane < ng) ? (int)f.len : 0;
@@ -688,20 +800,9 @@ __global__ void __launch_bounds__(W_WARPS * 32, 4) k_bpe_warp(Call c, Workspace 
       k0 = k1;
     }
   }
-  // then the thread tier, 32 fragments per warp at a time
-  const uint32_t tcount = *(volatile uint32_t*)&ws.st->tq_count;
-  __syncwarp();
-  while (true) {
-    uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&ws.st->tq_taken, 32u);
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (base >= tcount) break;
-    if (base + lane < tcount) {
-      const Frag f = ws.tq[base + lane];
-      bpe_thread(c, ws, V, f.start, (int)f.len);
-    }
-    __syncwarp();
-  }
+  drain_segment_queue<32>(c, ws, V, 2);
+  drain_segment_queue<16>(c, ws, V, 1);
+  drain_segment_queue<8>(c, ws, V, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -714,14 +815,14 @@ __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws,
   __shared__ uint32_t s_idx;
   __shared__ unsigned long long s_end;
   const int tid = threadIdx.x, T = blockDim.x;
-  const uint32_t count = *(volatile uint32_t*)&ws.st->long_count;
+  const uint32_t count = *(volatile uint32_t*)&ws.st->qcount[Q_LONG];
   while (true) {
-    if (tid == 0) s_idx = atomicAdd(&ws.st->long_taken, 1u);
+    if (tid == 0) s_idx = atomicAdd(&ws.st->qtaken[Q_LONG], 1u);
     __syncthreads();
     const uint32_t idx = s_idx;
     __syncthreads();
     if (idx >= count) break;
-    const Frag f = ws.longq[idx];
+    const Frag f = ws.q[Q_LONG][idx];
     // end: known from the queue entry, or the next fragment start after
     // f.start (or the text end)
     if (tid == 0) s_end = f.len > 0 ? (unsigned long long)(f.start + f.len) : (unsigned long long)c.n;

@@ -10,9 +10,10 @@
 //   K3 settle        per 512-byte chunk: every fragment that is one byte, or
 //                    whose bytes are a token that encodes to itself, is settled
 //                    with one probe; the others are queued (Section 4.2)
-//   K3b bpe_warp     queued fragments: at most 16 bytes one thread each (the
-//                    textbook loop in registers), 17..128 bytes batched per warp through the
-//                    sweep engine (all certified-safe pairs merge per sweep)
+//   K3b bpe_warp     queued fragments through the sweep engine (all certified-
+//                    safe pairs merge per sweep): at most 32 bytes one symbol
+//                    per lane in 8/16/32-lane segments, 33..128 bytes batched
+//                    per warp in shared memory
 //   K4 bpe_long      longer fragments, one CTA each, arrays in global memory
 //   K5 emit          per-fragment id counts -> offsets (decoupled look-back
 //                    across chunks), copy of the ids in text order
@@ -30,8 +31,8 @@ constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
 constexpr int BCHUNK = 512;        // bytes per settle / emit CTA (K3, K5)
 constexpr int B_THREADS = 128;
-constexpr int TCAP = 16;           // longest fragment of the thread tier (symbols in registers)
 constexpr int WCAP = 128;          // symbols per warp-engine batch; longer fragments go to K4
+constexpr int Q_LONG = 4;          // queue index of fragments longer than WCAP
 constexpr int W_EPT = WCAP / 32;   // symbols per lane
 constexpr int W_WARPS = 4;         // warps per K3b CTA
 constexpr int W_GRAB = 8;          // queue entries a warp takes at a time
@@ -90,9 +91,7 @@ struct DevStatus {
   uint32_t epoch;
   unsigned long long err_off;   // first malformed UTF-8 byte (atomicMin), ~0 if none
   unsigned long long n_ids;
-  uint32_t long_count, long_taken;
-  uint32_t wq_count, wq_taken;
-  uint32_t tq_count, tq_taken;
+  uint32_t qcount[5], qtaken[5];  // queues: fragments of <= 8, <= 16, <= 32, <= 128 bytes, longer
   uint32_t emit_ticket, emit_done;
   uint32_t pad[4];
 };
@@ -103,9 +102,8 @@ struct Workspace {
   uint32_t* pstart;         // fragment-start bitmask
   int32_t* tok;             // a fragment's ids, at the fragment's byte offset
   int32_t* fcnt;            // a fragment's number of ids, at its byte offset
-  Frag* wq;                 // K3b queue, warp tier
-  Frag* tq;                 // K3b queue, thread tier
-  Frag* longq;              // K4 queue
+  Frag* q[5];               // fragments to encode: <= 8, <= 16, <= 32 bytes (segment engine),
+                            // <= 128 bytes (warp engine), longer (K4)
   unsigned long long* lb;   // K5 look-back words
   DevStatus* st;
   // K4 engine storage, indexed by byte position of the fragment
