@@ -263,7 +263,10 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
     if (qc >= 0) {
       const uint32_t slot = s_qbase[qc] + ((uint32_t)(pos_q >> (10 * qc)) & 1023u);
       pos_q += 1ull << (10 * qc);
-      ws.q[qc][slot] = Frag{r0 + fstart[flo + j], flen[j]};
+      // select the queue with constant indices: a run-time index into the
+      // kernel-parameter struct would take a generic address of parameter space
+      Frag* qp = qc == 0 ? ws.q[0] : qc == 1 ? ws.q[1] : qc == 2 ? ws.q[2] : qc == 3 ? ws.q[3] : ws.q[Q_LONG];
+      qp[slot] = Frag{r0 + fstart[flo + j], flen[j]};
     }
   }
 }
@@ -751,18 +754,19 @@ __device__ void segment_engine(const Call& c, const Workspace& ws, const DevVoca
 }
 
 template <int W>
-__device__ void drain_segment_queue(const Call& c, const Workspace& ws, const DevVocab& V, int qi) {
+__device__ void drain_segment_queue(const Call& c, const Workspace& ws, const DevVocab& V, const Frag* queue,
+                                    const uint32_t* qcount, uint32_t* qtaken) {
   constexpr int PER = 32 / W;  // fragments per warp
   const int lane = threadIdx.x & 31;
-  const uint32_t count = *(volatile uint32_t*)&ws.st->qcount[qi];
+  const uint32_t count = *(volatile const uint32_t*)qcount;
   while (true) {
     uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&ws.st->qtaken[qi], (uint32_t)PER);
+    if (lane == 0) base = atomicAdd(qtaken, (uint32_t)PER);
     base = __shfl_sync(0xffffffffu, base, 0);
     if (base >= count) break;
     const uint32_t k = base + (uint32_t)(lane / W);
     Frag f{0, 0};
-    if (k < count) f = ws.q[qi][k];
+    if (k < count) f = queue[k];
     segment_engine<W>(c, ws, V, f.start, (int)f.len);
   }
 }
@@ -800,9 +804,9 @@ __global__ void __launch_bounds__(W_WARPS * 32, 4) k_bpe_warp(Call c, Workspace 
       k0 = k1;
     }
   }
-  drain_segment_queue<32>(c, ws, V, 2);
-  drain_segment_queue<16>(c, ws, V, 1);
-  drain_segment_queue<8>(c, ws, V, 0);
+  drain_segment_queue<32>(c, ws, V, ws.q[2], &ws.st->qcount[2], &ws.st->qtaken[2]);
+  drain_segment_queue<16>(c, ws, V, ws.q[1], &ws.st->qcount[1], &ws.st->qtaken[1]);
+  drain_segment_queue<8>(c, ws, V, ws.q[0], &ws.st->qcount[0], &ws.st->qtaken[0]);
 }
 
 // ---------------------------------------------------------------------------
