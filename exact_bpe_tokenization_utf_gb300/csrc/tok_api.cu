@@ -21,9 +21,8 @@ using namespace tokgb;
 
 namespace {
 
-constexpr int N_STAGES = 6;
-const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_settle",
-                                     "k_bpe_warp",    "k_bpe_long",   "k_emit"};
+constexpr int N_STAGES = 5;
+const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_bpe_chunk", "k_bpe_long", "k_emit"};
 
 thread_local std::string g_load_error;
 
@@ -108,9 +107,9 @@ cudaError_t dalloc(T** p, size_t count) {
 
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
-  void* ptrs[] = {w.text,     w.csum,     w.pstart,   w.tok,      w.fcnt,     w.q[0], w.q[1], w.q[2], w.q[3], w.q[4],
-                  w.lb,       w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1], w.e_kr[0],
-                  w.e_kr[1],  w.e_fl,     w.e_rs,     h->d_out};
+  void* ptrs[] = {w.text, w.csum, w.pstart, w.tok, w.cm_first, w.cm_count, w.cm_long, w.cm_long_count,
+                  w.longq, w.lb, w.st, w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1], w.e_kr[0], w.e_kr[1],
+                  w.e_fl, w.e_rs, h->d_out};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   w = Workspace{};
@@ -133,12 +132,11 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.csum, nch + 2));
   chk(dalloc(&w.pstart, cap / 32 + pad));
   chk(dalloc(&w.tok, cap + pad));
-  chk(dalloc(&w.fcnt, cap + pad));
-  chk(dalloc(&w.q[0], cap / 2 + pad));
-  chk(dalloc(&w.q[1], cap / 9 + pad));
-  chk(dalloc(&w.q[2], cap / 17 + pad));
-  chk(dalloc(&w.q[3], cap / 33 + pad));
-  chk(dalloc(&w.q[Q_LONG], cap / (WCAP + 1) + nbch + pad));
+  chk(dalloc(&w.cm_first, nbch + 2));
+  chk(dalloc(&w.cm_count, nbch + 2));
+  chk(dalloc(&w.cm_long, nbch + 2));
+  chk(dalloc(&w.cm_long_count, nbch + 2));
+  chk(dalloc(&w.longq, nbch + 2));
   chk(dalloc(&w.lb, nbch + 2));
   chk(dalloc(&w.st, 1));
   for (int b = 0; b < 2; ++b) {
@@ -196,14 +194,12 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
     if (tm) cudaEventRecord(h->ev[1], s);
     launch_boundaries(c, h->ws, s);
     if (tm) cudaEventRecord(h->ev[2], s);
-    launch_settle(c, h->ws, h->v, s);
+    launch_bpe_chunk(c, h->ws, h->v, s);
     if (tm) cudaEventRecord(h->ev[3], s);
-    launch_bpe_warp(c, h->ws, h->v, h->n_sms, s);
-    if (tm) cudaEventRecord(h->ev[4], s);
     launch_bpe_long(c, h->ws, h->v, h->n_sms, s);
-    if (tm) cudaEventRecord(h->ev[5], s);
+    if (tm) cudaEventRecord(h->ev[4], s);
     launch_emit(c, h->ws, s);
-    if (tm) cudaEventRecord(h->ev[6], s);
+    if (tm) cudaEventRecord(h->ev[5], s);
     h->launches += N_STAGES;
     h->have_times = tm;
   }

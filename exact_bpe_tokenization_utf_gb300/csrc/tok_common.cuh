@@ -7,18 +7,13 @@
 //                    "CR/LF later in this whitespace run")
 //   K2 boundaries    UTF-8 validation + per-code-point class + run
 //                    decomposition rules -> fragment-start bitmask (Section 4.1)
-//   K3 settle        per 512-byte chunk: every fragment that is one byte, or
-//                    whose bytes are a token that encodes to itself, is settled
-//                    with one probe; the others are queued (Section 4.2)
-//   K3b bpe_warp     queued fragments through the sweep engine (all certified-
-//                    safe pairs merge per sweep): at most 32 bytes one symbol
-//                    per lane in 8/16/32-lane segments, 33..128 bytes batched
-//                    per warp in shared memory
-//   K4 bpe_long      longer fragments, one CTA each, arrays in global memory
-//   K5 emit          per-fragment id counts -> offsets (decoupled look-back
-//                    across chunks), copy of the ids in text order
-// Every tier writes a fragment's ids at the fragment's byte offset in `tok`
-// and their number at the same offset in `fcnt`.
+//   K3 bpe_chunk     every fragment that starts in the chunk (and fits in
+//                    ENG_CAP symbols with its neighbours) is encoded by one CTA
+//                    in shared memory, merging all certified-safe pairs per
+//                    sweep; a longer last fragment is queued (Section 4.2)
+//   K4 bpe_long      queued fragments, one CTA each, arrays in global memory
+//   K5 emit          per-chunk token counts -> offsets (decoupled look-back),
+//                    coalesced copy of the ids
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -29,14 +24,11 @@ constexpr int CHUNK = 1024;        // bytes per chunk (every per-chunk kernel)
 constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K1 / K2
 constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
-constexpr int BCHUNK = 512;        // bytes per settle / emit CTA (K3, K5)
+constexpr int BCHUNK = 512;        // bytes per BPE / emit CTA (K3, K5)
+constexpr int B_RANGE = 2 * BCHUNK;// bytes a K3 CTA covers: its chunk + the tail of its last fragment
+constexpr int B_CAP = 512;         // engine symbols per batch; a longer last fragment goes to K4
 constexpr int B_THREADS = 128;
-constexpr int WCAP = 128;          // symbols per warp-engine batch; longer fragments go to K4
-constexpr int Q_LONG = 4;          // queue index of fragments longer than WCAP
-constexpr int W_EPT = WCAP / 32;   // symbols per lane
-constexpr int W_WARPS = 4;         // warps per K3b CTA
-constexpr int W_GRAB = 8;          // queue entries a warp takes at a time
-constexpr int S_RANGE = BCHUNK + 256;  // bytes K3 stages: its chunk + the tail of its last fragment
+constexpr int B_EPT = B_CAP / B_THREADS;  // engine symbols per thread at most
 constexpr int LONG_THREADS = 1024; // K4
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
@@ -79,10 +71,10 @@ struct DevVocab {
   int monotone;               // every merge that uses a token comes after every merge making it
 };
 
-// one queued fragment: byte offset and length (-1: end not yet known)
+// one queued long fragment: its start; the chunk whose last fragment it is
 struct Frag {
   long long start;
-  long long len;
+  long long chunk;
 };
 
 // device-side per-call status and work counters
@@ -91,19 +83,21 @@ struct DevStatus {
   uint32_t epoch;
   unsigned long long err_off;   // first malformed UTF-8 byte (atomicMin), ~0 if none
   unsigned long long n_ids;
-  uint32_t qcount[5], qtaken[5];  // queues: fragments of <= 8, <= 16, <= 32, <= 128 bytes, longer
+  uint32_t long_count, long_taken;
   uint32_t emit_ticket, emit_done;
-  uint32_t pad[4];
+  uint32_t pad[8];
 };
 
 struct Workspace {
   uint8_t* text;            // device copy of host input (host entry points)
   uint32_t* csum;           // K1 chunk summaries
   uint32_t* pstart;         // fragment-start bitmask
-  int32_t* tok;             // a fragment's ids, at the fragment's byte offset
-  int32_t* fcnt;            // a fragment's number of ids, at its byte offset
-  Frag* q[5];               // fragments to encode: <= 8, <= 16, <= 32 bytes (segment engine),
-                            // <= 128 bytes (warp engine), longer (K4)
+  int32_t* tok;             // token ids, compacted per chunk at the chunk's first fragment start
+  long long* cm_first;      // per chunk: first fragment start in it, or -1
+  int32_t* cm_count;        // per chunk: ids K3 produced  (K3 / K5 chunks are BCHUNK bytes)
+  long long* cm_long;       // per chunk: start of its queued long fragment, or -1
+  int32_t* cm_long_count;   // per chunk: ids K4 produced for it
+  Frag* longq;              // K4 queue
   unsigned long long* lb;   // K5 look-back words
   DevStatus* st;
   // K4 engine storage, indexed by byte position of the fragment
@@ -186,45 +180,6 @@ __device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s,
   return -1;
 }
 
-// Probe the merge table from slot s on (after a first probe missed).
-static __device__ __forceinline__ unsigned long long merge_lookup_from(const DevVocab& v, unsigned long long key, uint32_t s) {
-  const uint32_t mask = (1u << v.bits) - 1u;
-  for (uint32_t probe = 0; probe <= mask; ++probe) {
-    s &= mask;
-    const uint4 e = __ldg(reinterpret_cast<const uint4*>(v.table + s));
-    const unsigned long long k = ((unsigned long long)e.y << 32) | e.x;
-    if (k == key) return ((unsigned long long)e.z << 32) | e.w;
-    if (k == EMPTY_KEY) break;
-    ++s;
-  }
-  return ~0ull;
-}
-
-// N lookups at once: the first probes are all issued before any is used, so
-// their latencies overlap; further probes (rare at load factor <= 1/2) follow.
-template <int N>
-__device__ __forceinline__ void merge_lookup_n(const DevVocab& v, const uint32_t (&a)[N], const uint32_t (&b)[N],
-                                               uint32_t valid, unsigned long long (&out)[N]) {
-  uint4 e[N];
-  unsigned long long key[N];
-  uint32_t slot[N];
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    key[j] = ((unsigned long long)a[j] << 32) | b[j];
-    slot[j] = merge_slot(key[j], v.bits);
-    if ((valid >> j) & 1u) e[j] = __ldg(reinterpret_cast<const uint4*>(v.table + slot[j]));
-  }
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    out[j] = ~0ull;
-    if ((valid >> j) & 1u) {
-      const unsigned long long k = ((unsigned long long)e[j].y << 32) | e[j].x;
-      if (k == key[j]) out[j] = ((unsigned long long)e[j].z << 32) | e[j].w;
-      else if (k != EMPTY_KEY) out[j] = merge_lookup_from(v, key[j], slot[j] + 1);
-    }
-  }
-}
-
 __device__ __forceinline__ uint32_t kr_rank(unsigned long long kr) { return (uint32_t)(kr >> 32); }
 __device__ __forceinline__ uint32_t kr_result(unsigned long long kr) { return (uint32_t)kr; }
 
@@ -260,8 +215,7 @@ __device__ __forceinline__ int utf8_decode(const uint8_t* s, int avail, uint32_t
 // host-side launchers (defined in the kernel translation units)
 void launch_run_summary(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
-void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
-void launch_bpe_warp(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
+void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
 void launch_emit(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);

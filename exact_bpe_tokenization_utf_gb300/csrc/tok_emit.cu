@@ -3,8 +3,7 @@
 // an id array; Section 4.4: ids only, no byte offsets).
 //
 // Each CTA owns a 512-byte chunk and emits the ids of the fragments that start
-// in it; every BPE tier left a fragment's ids and their count at the
-// fragment's byte offset.  The number of tokens before the range comes from a
+// in it (K3 left them compacted; a long last fragment's ids come from K4).  The number of tokens before the range comes from a
 // decoupled look-back over the CTAs' published counts (Merrill and Garland,
 // "Single-pass parallel prefix scan with decoupled look-back", 2016): ranges
 // are taken in ticket order, so a CTA only waits on CTAs that already run;
@@ -12,28 +11,6 @@
 #include "tok_common.cuh"
 
 namespace tokgb {
-
-// block-wide exclusive sum (blockDim.x a multiple of 32; sh holds blockDim/32 ints)
-__device__ __forceinline__ int block_excl_sum(int v, int* total, int* sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += o;
-  }
-  if (lane == 31) sh[warp] = inc;
-  __syncthreads();
-  int pre = 0, tot = 0;
-  for (int k = 0; k < nw; ++k) {
-    const int x = sh[k];
-    pre += k < warp ? x : 0;
-    tot += x;
-  }
-  *total = tot;
-  __syncthreads();
-  return pre + inc - v;
-}
 
 // look-back word: epoch (30 bits) | flag (2 bits) | value (32 bits)
 constexpr unsigned long long LB_AGG = 1ull, LB_INC = 2ull;
@@ -55,59 +32,22 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
 }
 
 __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
-  __shared__ uint32_t bits[BCHUNK / 32];
-  __shared__ uint16_t fstart[BCHUNK];
-  __shared__ int fcount[BCHUNK];
-  __shared__ int foff[BCHUNK];
-  __shared__ uint16_t big[BCHUNK];
-  __shared__ int scan[B_THREADS / 32];
   __shared__ uint32_t s_chunk;
   __shared__ unsigned long long s_prefix;
-  __shared__ int s_item, s_nbig;
-  const int tid = threadIdx.x, T = B_THREADS;
+  __shared__ int s_item;
+  const int tid = threadIdx.x;
   const long long nch = n_bchunks(c.n);
   DevStatus* st = ws.st;
-  if (tid == 0) {
-    s_chunk = atomicAdd(&st->emit_ticket, 1u);
-    s_nbig = 0;
-  }
+  if (tid == 0) s_chunk = atomicAdd(&st->emit_ticket, 1u);
   __syncthreads();
   const long long chunk = s_chunk;
   const long long r0 = chunk * BCHUNK;
   const long long r1 = min(r0 + BCHUNK, c.n);
-  if (tid < BCHUNK / 32) {
-    const long long p = r0 + 32ll * tid;
-    uint32_t v = 0;
-    if (p < r1) {
-      v = ws.pstart[(r0 >> 5) + tid];
-      if (r1 - p < 32) v &= (1u << (r1 - p)) - 1u;
-    }
-    bits[tid] = v;
-  }
-  __syncthreads();
-  // the fragments that start in this chunk, and their id counts
-  const int q0 = tid * 4;
-  const uint32_t mine = (bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
-  int nf = 0;
-  int idx = block_excl_sum(__popc(mine), &nf, scan);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if ((mine >> q) & 1u) fstart[idx++] = (uint16_t)(q0 + q);
-  __syncthreads();
-  const int FB = (nf + T - 1) / T;
-  const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
-  int ids = 0;
-  for (int f = flo; f < fhi; ++f) {
-    const int k = ws.fcnt[r0 + fstart[f]];
-    fcount[f] = k;
-    ids += k;
-  }
-  int total = 0;
-  int o = block_excl_sum(ids, &total, scan);
-  for (int f = flo; f < fhi; ++f) {
-    foff[f] = o;
-    o += fcount[f];
-  }
+  const long long first = ws.cm_first[chunk];
+  const int n_short = first >= 0 ? ws.cm_count[chunk] : 0;
+  const long long lf = first >= 0 ? ws.cm_long[chunk] : -1;
+  const int n_long = lf >= 0 ? ws.cm_long_count[chunk] : 0;
+  const uint32_t total = (uint32_t)(n_short + n_long);
   if (tid < 32) {
     // warp 0: publish this chunk's count, then look back 32 predecessors at a
     // time until one has published its inclusive prefix
@@ -116,7 +56,7 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
     const uint32_t ep = c.epoch & 0x3FFFFFFFu;
     if (lane == 0 && chunk > 0) {
       __threadfence();
-      lb[chunk] = lb_pack(c.epoch, LB_AGG, (uint32_t)total);
+      lb[chunk] = lb_pack(c.epoch, LB_AGG, total);
     }
     unsigned long long prefix = 0;
     bool timed_out = false;
@@ -150,23 +90,10 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
   }
   __syncthreads();
   const unsigned long long base = s_prefix;
-  // ids in text order: short fragments by their thread, long ones by the CTA
-  for (int f = flo; f < fhi; ++f) {
-    const int k = fcount[f];
-    const long long a = r0 + fstart[f];
-    if (k <= 8) {
-      for (int j = 0; j < k; ++j) c.out[base + foff[f] + j] = ws.tok[a + j];
-    } else {
-      big[atomicAdd(&s_nbig, 1)] = (uint16_t)f;
-    }
-  }
-  __syncthreads();
-  for (int b = 0; b < s_nbig; ++b) {
-    const int f = big[b];
-    const long long a = r0 + fstart[f];
-    for (int j = tid; j < fcount[f]; j += T) c.out[base + foff[f] + j] = ws.tok[a + j];
-  }
-  // batch: ids before each item start in this chunk
+  // ids: the chunk's fragments, then its long fragment (always its last one)
+  for (int j = tid; j < n_short; j += B_THREADS) c.out[base + j] = ws.tok[first + j];
+  for (int j = tid; j < n_long; j += B_THREADS) c.out[base + n_short + j] = ws.tok[lf + j];
+  // batch: K3 stored the ids before each item start relative to its chunk
   if (c.item_off) {
     if (tid == 0) {
       int a = 0, b = c.n_items + 1;
@@ -177,15 +104,9 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
       s_item = a;
     }
     __syncthreads();
-    for (int k = s_item + tid; k <= c.n_items; k += T) {
-      const long long x = c.item[k];
-      if (x >= r1) break;
-      int a = 0, b = nf;  // the fragment that starts at x
-      while (a < b) {
-        const int mid = (a + b) >> 1;
-        if (r0 + fstart[mid] < x) a = mid + 1; else b = mid;
-      }
-      c.item_off[k] = (long long)base + (a < nf ? foff[a] : total);
+    for (int k = s_item + tid; k <= c.n_items; k += B_THREADS) {
+      if (c.item[k] >= r1) break;
+      c.item_off[k] += (long long)base;
     }
   }
   // the last CTA to finish completes the status
