@@ -7,10 +7,11 @@
 //                    "CR/LF later in this whitespace run")
 //   K2 boundaries    UTF-8 validation + per-code-point class + run
 //                    decomposition rules -> fragment-start bitmask (Section 4.1)
-//   K3 bpe_chunk     every fragment that starts in the chunk (and fits in
-//                    ENG_CAP symbols with its neighbours) is encoded by one CTA
-//                    in shared memory, merging all certified-safe pairs per
-//                    sweep; a longer last fragment is queued (Section 4.2)
+//   K3 bpe_chunk     every fragment that starts in a 512-byte chunk is encoded
+//                    by one CTA: single bytes and whole self-encoding tokens
+//                    with one probe, the rest in shared memory (batches of
+//                    B_CAP symbols, all certified-safe pairs merged per sweep);
+//                    a longer last fragment is queued (Section 4.2)
 //   K4 bpe_long      queued fragments, one CTA each, arrays in global memory
 //   K5 emit          per-chunk token counts -> offsets (decoupled look-back),
 //                    coalesced copy of the ids
@@ -25,10 +26,11 @@ constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K1 / K2
 constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
 constexpr int BCHUNK = 512;        // bytes per BPE / emit CTA (K3, K5)
-constexpr int B_RANGE = 2 * BCHUNK;// bytes a K3 CTA covers: its chunk + the tail of its last fragment
-constexpr int B_CAP = 512;         // engine symbols per batch; a longer last fragment goes to K4
-constexpr int B_THREADS = 128;
-constexpr int B_EPT = B_CAP / B_THREADS;  // engine symbols per thread at most
+constexpr int B_CAP = 256;         // engine symbols per batch; a longer last fragment goes to K4
+constexpr int B_RANGE = BCHUNK + B_CAP;  // bytes a K3 CTA covers: its chunk + the tail of its last fragment
+constexpr int B_THREADS = 128;     // K5
+constexpr int K3_THREADS = 128;    // K3: 4 warps
+constexpr int B_EPT = B_CAP / K3_THREADS;  // engine symbols per thread at most
 constexpr int LONG_THREADS = 1024; // K4
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
@@ -160,14 +162,23 @@ __device__ __forceinline__ unsigned long long merge_lookup(const DevVocab& v, ui
 }
 
 // Token whose bytes equal s[0..len) and whose own bytes encode to itself,
-// or -1.  The hash only selects candidates; the bytes are compared.
-__device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s, int len) {
-  if (len < 2 || len > 255 || len > (int)v.max_tok_len) return -1;
-  const unsigned long long h = bytes_hash(s, len);
+// or -1.  The hash only selects candidates; the bytes are compared.  Split in
+// parts so that a thread can issue the first probes of several strings before
+// it waits for any: whole_first_slot gives the first slot of a hash,
+// whole_lookup_at finishes from the loaded first entry.
+__device__ __forceinline__ bool whole_eligible(const DevVocab& v, int len) {
+  return len >= 2 && len <= 255 && len <= (int)v.max_tok_len;
+}
+
+__device__ __forceinline__ uint32_t whole_first_slot(const DevVocab& v, unsigned long long h) {
+  return (uint32_t)(h >> (64 - v.whole_bits));
+}
+
+__device__ __forceinline__ int whole_lookup_at(const DevVocab& v, const uint8_t* s, int len, unsigned long long h,
+                                               uint32_t slot, uint4 e) {
   const uint32_t mask = (1u << v.whole_bits) - 1u;
-  uint32_t slot = (uint32_t)(h >> (64 - v.whole_bits));
   for (uint32_t probe = 0; probe <= mask; ++probe) {
-    const uint4 e = __ldg(reinterpret_cast<const uint4*>(v.whole + slot));
+    if (probe) e = __ldg(reinterpret_cast<const uint4*>(v.whole + slot));
     if (e.w == 0u) return -1;
     if ((e.w & 255u) == (uint32_t)len && (((unsigned long long)e.y << 32) | e.x) == h) {
       const uint8_t* t = v.vocab_bytes + (e.w >> 8);
@@ -178,6 +189,13 @@ __device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s,
     slot = (slot + 1u) & mask;
   }
   return -1;
+}
+
+__device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s, int len) {
+  if (!whole_eligible(v, len)) return -1;
+  const unsigned long long h = bytes_hash(s, len);
+  const uint32_t slot = whole_first_slot(v, h);
+  return whole_lookup_at(v, s, len, h, slot, __ldg(reinterpret_cast<const uint4*>(v.whole + slot)));
 }
 
 __device__ __forceinline__ uint32_t kr_rank(unsigned long long kr) { return (uint32_t)(kr >> 32); }
