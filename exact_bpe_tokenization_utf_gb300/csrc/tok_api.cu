@@ -21,8 +21,9 @@ using namespace tokgb;
 
 namespace {
 
-constexpr int N_STAGES = 5;
-const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_bpe_chunk", "k_bpe_long", "k_emit"};
+constexpr int N_STAGES = 7;
+const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_settle", "k_bpe_engine",
+                                     "k_bpe_long",    "k_scan",       "k_emit"};
 
 thread_local std::string g_load_error;
 
@@ -107,9 +108,9 @@ cudaError_t dalloc(T** p, size_t count) {
 
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
-  void* ptrs[] = {w.text, w.csum, w.pstart, w.tok, w.cm_first, w.cm_count, w.cm_long, w.cm_long_count,
-                  w.longq, w.lb, w.st, w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1], w.e_kr[0], w.e_kr[1],
-                  w.e_fl, w.e_rs, h->d_out};
+  void* ptrs[] = {w.text,     w.csum,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,    w.sbatch,
+                  w.wq,       w.longq,    w.ctot,     w.cpre,     w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0],
+                  w.e_len[1], w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,     h->d_out};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   w = Workspace{};
@@ -132,12 +133,17 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.csum, nch + 2));
   chk(dalloc(&w.pstart, cap / 32 + pad));
   chk(dalloc(&w.tok, cap + pad));
-  chk(dalloc(&w.cm_first, nbch + 2));
-  chk(dalloc(&w.cm_count, nbch + 2));
-  chk(dalloc(&w.cm_long, nbch + 2));
-  chk(dalloc(&w.cm_long_count, nbch + 2));
-  chk(dalloc(&w.longq, nbch + 2));
-  chk(dalloc(&w.lb, nbch + 2));
+  // queue sizes: a queued short fragment has >= 2 bytes (a single byte always
+  // settles), a warp batch >= 1 short fragment, a wide fragment > SB_MAX
+  // bytes, a long one > B_CAP bytes (plus at most one of unknown length per
+  // chunk)
+  chk(dalloc(&w.fcnt, cap + pad));
+  chk(dalloc(&w.sfrag, cap / 2 + nbch + pad));
+  chk(dalloc(&w.sbatch, cap / 2 + nbch + pad));
+  chk(dalloc(&w.wq, cap / (SB_MAX + 1) + nbch + pad));
+  chk(dalloc(&w.longq, cap / (B_CAP + 1) + nbch + pad));
+  chk(dalloc(&w.ctot, nbch + 2));
+  chk(dalloc(&w.cpre, nbch + 2));
   chk(dalloc(&w.st, 1));
   for (int b = 0; b < 2; ++b) {
     chk(dalloc(&w.e_sym[b], cap + pad));
@@ -147,7 +153,6 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.e_fl, cap + pad));
   chk(dalloc(&w.e_rs, cap + pad));
   chk(dalloc(&h->d_out, cap + pad));
-  if (e == cudaSuccess) e = cudaMemset(w.lb, 0, (nbch + 2) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(w.pstart, 0, (cap / 32 + pad) * sizeof(uint32_t));
   if (e != cudaSuccess) {
     free_workspace(h);
@@ -180,6 +185,8 @@ int ensure_items(tok_handle* h, uint64_t n_items) {
 
 // Enqueue the whole chain for one call.
 int run_chain(tok_handle* h, Call c, cudaStream_t s) {
+  c.pf.p = h->d_table;
+  c.pf.bytes = sizeof(MergeEntry) << h->v.bits;
   c.pattern = h->pattern;
   c.epoch = ++h->epoch;
   if (h->epoch >= 0x3FFFFFFFu) h->epoch = 0;
@@ -194,12 +201,16 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
     if (tm) cudaEventRecord(h->ev[1], s);
     launch_boundaries(c, h->ws, s);
     if (tm) cudaEventRecord(h->ev[2], s);
-    launch_bpe_chunk(c, h->ws, h->v, s);
+    launch_settle(c, h->ws, h->v, s);
     if (tm) cudaEventRecord(h->ev[3], s);
-    launch_bpe_long(c, h->ws, h->v, h->n_sms, s);
+    launch_bpe_engine(c, h->ws, h->v, h->n_sms, s);
     if (tm) cudaEventRecord(h->ev[4], s);
-    launch_emit(c, h->ws, s);
+    launch_bpe_long(c, h->ws, h->v, h->n_sms, s);
     if (tm) cudaEventRecord(h->ev[5], s);
+    launch_scan(c, h->ws, s);
+    if (tm) cudaEventRecord(h->ev[6], s);
+    launch_emit(c, h->ws, s);
+    if (tm) cudaEventRecord(h->ev[7], s);
     h->launches += N_STAGES;
     h->have_times = tm;
   }

@@ -2,8 +2,11 @@
 // serving", Section 4.2): every fragment is encoded on its own by merging the
 // lowest-rank adjacent pair (leftmost on ties) until no adjacent pair is a
 // merge.  The pages tier fragments by length (one thread, one warp, one block
-// per fragment); here one CTA encodes all fragments of a 512-byte chunk at
-// once, and only fragments longer than 512 bytes get a CTA each.
+// per fragment).  Here most fragments are settled by one probe (single bytes,
+// whole self-encoding tokens); of the rest, those of at most 32 bytes share a
+// warp, one symbol per lane, several fragments per warp; fragments of
+// 33..B_CAP bytes get a CTA with shared memory, longer ones a CTA with global
+// memory.
 //
 // Sweep engine.  The symbols of many fragments sit in one array; the pair
 // between two fragments is a "wall" that never merges.  Let k be the rank of
@@ -234,27 +237,7 @@ __device__ int global_engine(const Call& c, const Workspace& ws, const DevVocab&
 }
 
 // ---------------------------------------------------------------------------
-// K3: the fragments that start in one 512-byte chunk
-//
-// Most fragments need no merge loop: a single byte is its byte token, and a
-// fragment whose bytes equal a token t with BPE(bytes(t)) == [t] (checked for
-// every token at load time) encodes to [t].  Each thread settles a few
-// fragments with one hash probe each, all its probes issued before it waits.
-// The rest are encoded by one of three engines, all running the same sweep
-// (every certified-safe pair merges):
-//   - fragments of at most 32 bytes, packed in order into batches of at most
-//     32 symbols, one batch per warp at a time: one symbol per lane,
-//     neighbours through shuffles, walls between fragments, no block barrier;
-//   - fragments of 33..B_CAP bytes: the whole CTA, in shared memory;
-//   - the one fragment longer than B_CAP a chunk can hold besides its last
-//     (two such would not both start within 512 bytes): the whole CTA, with
-//     the global-memory engine.
-// Engine results go to a per-byte scratch array at their fragment's offset
-// and are compacted into the chunk's ids at the end.
-
-constexpr int K3_WARPS = K3_THREADS / 32;
-constexpr int S_MAX = BCHUNK / 2 + 1;        // unresolved fragments of >= 2 bytes starting in a chunk
-constexpr int U_MAX = BCHUNK / 33 + 2;       // fragments of more than 32 bytes starting in a chunk
+// Engine storage
 
 struct WarpBuf {            // one warp's compaction buffer
   uint32_t sym[32];
@@ -274,31 +257,6 @@ struct CtaBatch {           // one batch of the CTA engine
   uint16_t ml[B_CAP];       // longest left operand of merges whose right operand is this symbol
   uint16_t mr[B_CAP];       // longest right operand of merges whose left operand is this symbol
   uint8_t fl[B_CAP];        // pair merges this sweep
-};
-
-struct ChunkEngine {
-  union {
-    WarpBuf wb[K3_WARPS];
-    CtaBatch cb;
-  } u;
-  // the CTA's bytes and fragment starts
-  uint8_t text[B_RANGE];
-  uint32_t bits[B_RANGE / 32];
-  // fragments that start in the chunk (at most BCHUNK)
-  uint16_t fstart[BCHUNK + 1];  // relative to `first`; then the span
-  int32_t ftok[BCHUNK];         // settled token, or -1
-  uint16_t fcnt[BCHUNK];        // ids of each fragment
-  uint16_t fout[BCHUNK];        // first id of each fragment
-  uint16_t feng[BCHUNK];        // first CTA-engine symbol of a fragment in its batch
-  uint16_t slist[S_MAX];        // unresolved fragments of <= 32 bytes, in order
-  uint16_t soff[S_MAX + 1];     // their byte offsets among themselves, then the total
-  uint16_t sbat[S_MAX + 1];     // first slist entry of each warp batch, then ns
-  uint16_t ulist[U_MAX];        // unresolved fragments of 33..B_CAP bytes, in order
-  uint16_t ueoff[U_MAX + 1];    // their byte offsets among themselves, then the total
-  int scan[K3_WARPS];
-  unsigned long long scan64[K3_WARPS];
-  long long first, end, longfrag, item0;
-  int nf, ns, nu, nb, sflags, batch_end, big;
 };
 
 // Sweep engine of one warp over a batch of M <= 32 symbols (lane i holds
@@ -479,25 +437,340 @@ __device__ __forceinline__ int warp_sweeps(WarpBuf& B, const DevVocab& V, DevSta
   return m;
 }
 
-// One warp encodes the short fragments slist[s0..s1) (at most 32 bytes in all).
-__device__ void warp_batch(ChunkEngine& E, WarpBuf& B, const Call& c, const DevVocab& V, DevStatus* st,
-                           uint32_t* eres, long long fs, int s0, int s1) {
+// ---------------------------------------------------------------------------
+// K3: settle the fragments that start in one 512-byte chunk
+//
+// Most fragments need no merge loop: a single byte is its byte token, and a
+// fragment whose bytes equal a token t with BPE(bytes(t)) == [t] (checked for
+// every token at load time) encodes to [t].  Each thread settles at most four
+// fragments with one hash probe each, all its probes issued before it waits
+// on any.  The others are queued for K3b / K4: fragments of at most 32 bytes
+// packed in text order into warp batches of at most 32 bytes, fragments of
+// 33..B_CAP bytes one by one, longer ones (and a last fragment whose end lies
+// beyond the staged bytes) for K4.
+
+constexpr int S_MAX = BCHUNK / 2 + 1;  // fragments of >= 2 bytes that start in a chunk
+
+__global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevVocab V) {
+  __shared__ __align__(16) uint8_t text[S_RANGE];
+  __shared__ uint32_t bits[S_RANGE / 32];
+  __shared__ uint16_t fstart[BCHUNK + 1];
+  __shared__ uint16_t slist[S_MAX];     // queued short fragments, in order
+  __shared__ uint16_t soff[S_MAX + 1];  // their byte offsets among themselves, then the total
+  __shared__ uint16_t sbat[S_MAX + 1];  // first slist entry of each warp batch, then ns
+  __shared__ int scan[B_THREADS / 32];
+  __shared__ long long s_last_end;
+  __shared__ unsigned long long s_sbase;
+  __shared__ uint32_t s_bbase, s_wbase, s_lbase;
+  __shared__ int s_ns, s_nb;
+  const int tid = threadIdx.x, T = B_THREADS;
+  const long long r0 = (long long)blockIdx.x * BCHUNK;
+  const long long r1 = min(r0 + BCHUNK, c.n);
+  const long long lim = min(r0 + S_RANGE, c.n);
+  const int nb = (int)(lim - r0);
+  {  // warm L2 with the merge table for K3b (DRAM is idle in this kernel)
+    const long long lines = (long long)((c.pf.bytes + 127) >> 7);
+    const char* base = static_cast<const char*>(c.pf.p);
+    for (long long g = (long long)blockIdx.x * T + tid; g < lines; g += (long long)gridDim.x * T)
+      asm volatile("prefetch.L2 [%0];" ::"l"(base + (g << 7)));
+  }
+  if (((reinterpret_cast<uintptr_t>(c.text) & 15u) == 0) && nb == S_RANGE) {
+    for (int k = tid; k < S_RANGE / 16; k += T)
+      reinterpret_cast<uint4*>(text)[k] = reinterpret_cast<const uint4*>(c.text + r0)[k];
+  } else {
+    for (int k = tid; k < nb; k += T) text[k] = c.text[r0 + k];
+  }
+  if (tid < S_RANGE / 32) {
+    const long long p = r0 + 32ll * tid;
+    uint32_t v = 0;
+    if (p < lim) {
+      v = ws.pstart[(r0 >> 5) + tid];
+      if (lim - p < 32) v &= (1u << (lim - p)) - 1u;
+    }
+    bits[tid] = v;
+  }
+  __syncthreads();
+  if (tid == 0) {  // end of the last fragment: the first start at or after r1
+    long long e = -1;
+    if (r1 >= c.n) {
+      e = c.n;
+    } else {
+      for (int w = BCHUNK / 32; w < S_RANGE / 32 && e < 0; ++w)
+        if (bits[w]) e = r0 + 32ll * w + (__ffs(bits[w]) - 1);
+      if (e < 0 && lim >= c.n) e = c.n;
+    }
+    s_last_end = e;
+  }
+  // fragment starts in [r0, r1): thread t looks at 4 bit positions
+  const int q0 = tid * 4;
+  const uint32_t mine = (bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
+  int nf = 0;
+  int idx = block_excl_sum(__popc(mine), &nf, scan);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if ((mine >> q) & 1u) fstart[idx++] = (uint16_t)(q0 + q);
+  __syncthreads();
+  // contiguous blocks of at most 4 fragments per thread (nf <= BCHUNK = 4 * T)
+  const int FB = (nf + T - 1) / T;
+  const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
+  int fa[4], fl[4], cls[4];  // start in the chunk, length (-1: unknown), queue (0 settled, 1 short, 2 wide, 3 long)
+  unsigned long long h[4];
+  uint32_t slot[4];
+  uint4 e[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int f = flo + q;
+    fa[q] = 0; fl[q] = 0; cls[q] = 0; h[q] = 0; slot[q] = 0;
+    e[q] = make_uint4(0u, 0u, 0u, 0u);
+    if (f < fhi) {
+      fa[q] = fstart[f];
+      const long long end = (f + 1 < nf) ? r0 + fstart[f + 1] : s_last_end;
+      fl[q] = end < 0 ? -1 : (int)(end - (r0 + fa[q]));
+      if (whole_eligible(V, fl[q])) {
+        h[q] = bytes_hash(text + fa[q], fl[q]);
+        slot[q] = whole_first_slot(V, h[q]);
+        e[q] = __ldg(reinterpret_cast<const uint4*>(V.whole + slot[q]));
+      }
+    }
+  }
+  int scount = 0, sbytes = 0, wcount = 0, lcount = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (flo + q < fhi) {
+      const int L = fl[q];
+      int t = -1;
+      if (L == 1) t = __ldg(V.byte_id + text[fa[q]]);
+      else if (whole_eligible(V, L)) t = whole_lookup_at(V, text + fa[q], L, h[q], slot[q], e[q]);
+      if (t >= 0) {
+        ws.tok[r0 + fa[q]] = t;
+        ws.fcnt[r0 + fa[q]] = 1;
+        cls[q] = 0;
+      } else if (L >= 1 && L <= SB_MAX) {
+        cls[q] = 1;
+        ++scount;
+        sbytes += L;
+      } else if (L > SB_MAX && L <= B_CAP) {
+        cls[q] = 2;
+        ++wcount;
+      } else {
+        cls[q] = 3;
+        ++lcount;
+      }
+    }
+  }
+  int ns = 0, sb_all = 0, nw = 0, nl = 0;
+  int si = block_excl_sum(scount, &ns, scan);
+  int so = block_excl_sum(sbytes, &sb_all, scan);
+  int wi = block_excl_sum(wcount, &nw, scan);
+  int li = block_excl_sum(lcount, &nl, scan);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (flo + q < fhi && cls[q] == 1) {
+      slist[si] = (uint16_t)(flo + q);
+      soff[si] = (uint16_t)so;
+      ++si;
+      so += fl[q];
+    }
+  }
+  __syncthreads();
+  // queue reservations, one per warp so that they overlap
+  if (tid == 0) {
+    // short fragments: greedy batches of at most SB_MAX bytes, in order
+    soff[ns] = (uint16_t)sb_all;
+    int nbat = 0, k = 0;
+    while (k < ns) {
+      sbat[nbat++] = (uint16_t)k;
+      const int b0 = soff[k];
+      ++k;
+      while (k < ns && soff[k + 1] - b0 <= SB_MAX) ++k;
+    }
+    sbat[nbat] = (uint16_t)ns;
+    s_ns = ns;
+    s_nb = nbat;
+    s_bbase = nbat ? atomicAdd(&ws.st->sbatch_count, (uint32_t)nbat) : 0u;
+    // ids of the settled fragments start the chunk's total; the engines add theirs
+    ws.ctot[blockIdx.x] = (uint32_t)(nf - ns - nw - nl);
+  } else if (tid == 32) {
+    s_sbase = ns ? atomicAdd(&ws.st->sfrag_count, (unsigned long long)ns) : 0ull;
+  } else if (tid == 64) {
+    s_wbase = nw ? atomicAdd(&ws.st->wide_count, (uint32_t)nw) : 0u;
+  } else if (tid == 96) {
+    s_lbase = nl ? atomicAdd(&ws.st->long_count, (uint32_t)nl) : 0u;
+  }
+  __syncthreads();
+  for (int k = tid; k < s_ns; k += T) {
+    const int f = slist[k];
+    ws.sfrag[s_sbase + k] = ((unsigned long long)(r0 + fstart[f]) << 8) | (unsigned)(soff[k + 1] - soff[k]);
+  }
+  for (int b = tid; b < s_nb; b += T)
+    ws.sbatch[s_bbase + b] = ((s_sbase + sbat[b]) << 5) | (unsigned)(sbat[b + 1] - sbat[b] - 1);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (flo + q >= fhi) continue;
+    if (cls[q] == 2) ws.wq[s_wbase + wi++] = Frag{r0 + fa[q], fl[q]};
+    else if (cls[q] == 3) ws.longq[s_lbase + li++] = Frag{r0 + fa[q], fl[q] > 0 ? fl[q] : -1};
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K3b: queued fragments of at most B_CAP bytes
+//
+// A persistent grid.  First every CTA takes fragments of 33..B_CAP bytes one
+// at a time through the shared-memory engine; then every warp takes batches
+// of short fragments through the warp engine.  Both write a fragment's ids at
+// its byte offset in `tok` and their number at the same offset in `fcnt`.
+
+// One fragment of M (33..B_CAP) bytes at byte offset a, all threads of the CTA.
+__device__ void cta_fragment(const Call& c, const Workspace& ws, const DevVocab& V, long long a, int M, CtaBatch& C,
+                             int* scan, unsigned long long* scan64, int* sflags) {
+  const int tid = threadIdx.x, T = B_THREADS, lane = tid & 31;
+  for (int i = tid; i < M; i += T) {
+    const int32_t id = __ldg(V.byte_id + c.text[a + i]);
+    C.sym[i] = (uint32_t)id;
+    C.len[i] = (uint16_t)(1u | (i == 0 ? FRAG_START : 0u));
+    C.ml[i] = __ldg(V.max_left + id);
+    C.mr[i] = __ldg(V.max_right + id);
+  }
+  if (tid == 0) *sflags = 0;
+  __syncthreads();
+  for (int i = tid; i < M; i += T) C.kr[i] = (i + 1 >= M) ? KR_WALL : merge_lookup(V, C.sym[i], C.sym[i + 1]);
+  __syncthreads();
+  int m = M;
+  for (int sweep = 0; sweep <= M; ++sweep) {
+    const int B = (m + T - 1) / T;
+    const int lo = min(tid * B, m), hi = min(lo + B, m);
+    // A: any mergeable pair left?  any overlapping equal-rank pairs?
+    int fl2 = 0;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t k = kr_rank(C.kr[i]);
+      if (mergeable(k)) {
+        fl2 |= 1;
+        if (i > 0 && kr_rank(C.kr[i - 1]) == k) fl2 |= 2;
+      }
+    }
+    fl2 = __reduce_or_sync(0xffffffffu, fl2);
+    if (lane == 0 && fl2) atomicOr(sflags, fl2);
+    __syncthreads();
+    const int flags = *sflags;
+    if (!(flags & 1)) break;
+    if (flags & 2) {
+      int lastrun = -1;
+      for (int i = lo; i < hi; ++i)
+        if (i == 0 || kr_rank(C.kr[i - 1]) != kr_rank(C.kr[i])) lastrun = i;
+      int run = block_excl_max(lastrun, scan);
+      for (int i = lo; i < hi; ++i) {
+        if (i == 0 || kr_rank(C.kr[i - 1]) != kr_rank(C.kr[i])) run = i;
+        C.rs[i] = (uint16_t)run;
+      }
+      __syncthreads();
+    }
+    // B: safe pairs
+    if (V.monotone) {
+      auto mlf = [&](int x) { return (int)C.ml[x]; };
+      auto mrf = [&](int x) { return (int)C.mr[x]; };
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t k = kr_rank(C.kr[i]);
+        const int u = (flags & 2) ? (int)C.rs[i] : i;
+        C.fl[i] = (mergeable(k) && pair_safe(C.len, C.kr, m, i, u, k, mlf, mrf)) ? 1 : 0;
+      }
+    } else {
+      unsigned long long best = ~0ull;
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t k = kr_rank(C.kr[i]);
+        if (mergeable(k)) {
+          const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
+          best = key < best ? key : best;
+        }
+      }
+      best = block_min_u64(best, scan64);
+      for (int i = lo; i < hi; ++i) C.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
+    }
+    __syncthreads();
+    // C: merge, look up the new pairs, compact
+    uint32_t nsym[B_EPT];
+    uint16_t nlen[B_EPT], nml[B_EPT], nmr[B_EPT];
+    unsigned long long nkr[B_EPT];
+    uint32_t keep = 0;
+#pragma unroll
+    for (int j = 0; j < B_EPT; ++j) {
+      const int i = lo + j;
+      nsym[j] = 0; nlen[j] = 0; nml[j] = 0; nmr[j] = 0; nkr[j] = KR_WALL;
+      if (i < hi && !(i > 0 && C.fl[i - 1])) {
+        keep |= 1u << j;
+        const bool mg = C.fl[i] != 0;
+        if (mg) {
+          const uint32_t r = kr_result(C.kr[i]);
+          nsym[j] = r;
+          nlen[j] = (uint16_t)(((C.len[i] & LEN_MASK) + (C.len[i + 1] & LEN_MASK)) | (C.len[i] & FRAG_START));
+          nml[j] = __ldg(V.max_left + r);
+          nmr[j] = __ldg(V.max_right + r);
+        } else {
+          nsym[j] = C.sym[i];
+          nlen[j] = C.len[i];
+          nml[j] = C.ml[i];
+          nmr[j] = C.mr[i];
+        }
+        const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
+        if (jn >= m) nkr[j] = KR_WALL;
+        else if (!mg && !C.fl[jn]) nkr[j] = C.kr[i];  // unchanged pair keeps its key
+        else nkr[j] = merge_lookup(V, nsym[j], C.fl[jn] ? kr_result(C.kr[jn]) : C.sym[jn]);
+      }
+    }
+    int newm = 0;
+    const int bpos = block_excl_sum(__popc(keep), &newm, scan);
+#pragma unroll
+    for (int j = 0; j < B_EPT; ++j) {
+      if ((keep >> j) & 1u) {
+        const int p = bpos + __popc(keep & ((1u << j) - 1u));
+        C.sym[p] = nsym[j];
+        C.len[p] = nlen[j];
+        C.kr[p] = nkr[j];
+        C.ml[p] = nml[j];
+        C.mr[p] = nmr[j];
+      }
+    }
+    if (tid == 0) *sflags = 0;
+    m = newm;
+    __syncthreads();
+    if (sweep == M && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
+  }
+  for (int i = tid; i < m; i += T) ws.tok[a + i] = (int32_t)C.sym[i];
+  if (tid == 0) {
+    ws.fcnt[a] = m;
+    atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
+  }
+  __syncthreads();
+}
+
+// One warp encodes a batch of short fragments (at most SB_MAX bytes in all).
+__device__ void short_batch(const Call& c, const Workspace& ws, const DevVocab& V, WarpBuf& B, uint8_t* owner,
+                            unsigned long long desc) {
   const int lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
-  const int base = E.soff[s0];
-  const int M = E.soff[s1] - base;
+  const unsigned long long first = desc >> 5;
+  const int nfr = (int)(desc & 31u) + 1;
+  const unsigned long long ent = lane < nfr ? ws.sfrag[first + lane] : 0ull;
+  const long long start = (long long)(ent >> 8);
+  const int len = (int)(ent & 255u);
+  int off = len;  // exclusive sum of the lengths over the lanes
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(FULL, off, d);
+    if (lane >= d) off += o;
+  }
+  const int M = __shfl_sync(FULL, off, 31);
+  off -= len;
+  for (int j = 0; j < len; ++j) owner[off + j] = (uint8_t)lane;
+  __syncwarp();
+  int fid = lane < M ? owner[lane] : 0;
+  __syncwarp();
+  const long long fpos = __shfl_sync(FULL, start, fid);
+  const int foff = __shfl_sync(FULL, off, fid);
   uint32_t sym = 0, lenb = 0, mlv = 0, mrv = 0;
   bool fst = false;
-  int fid = 0;
   if (lane < M) {
-    int a = s0, b = s1 - 1;  // entry with soff[a] <= base + lane < soff[a+1]
-    while (a < b) {
-      const int mid = (a + b + 1) >> 1;
-      if (E.soff[mid] <= base + lane) a = mid; else b = mid - 1;
-    }
-    fid = E.slist[a];
-    const int j = base + lane - E.soff[a];
-    const int32_t id = __ldg(V.byte_id + E.text[E.fstart[fid] + j]);
+    const int j = lane - foff;
+    const int32_t id = __ldg(V.byte_id + c.text[fpos + j]);
     sym = (uint32_t)id;
     lenb = 1;
     fst = j == 0;
@@ -508,412 +781,64 @@ __device__ void warp_batch(ChunkEngine& E, WarpBuf& B, const Call& c, const DevV
   const bool nfs = __shfl_down_sync(FULL, fst, 1);
   unsigned long long kr = KR_WALL;
   if (lane + 1 < M && !nfs) kr = merge_lookup(V, sym, nxt);
-  const int m = warp_sweeps(B, V, st, M, sym, lenb, fst, fid, mlv, mrv, kr);
-  // ids to the scratch at the fragment's byte offset, and their number
+  const int m = warp_sweeps(B, V, ws.st, M, sym, lenb, fst, fid, mlv, mrv, kr);
+  // ids at the fragment's byte offset, and their number
   const uint32_t fsm = __ballot_sync(FULL, lane < m && fst);
+  const long long pos = __shfl_sync(FULL, start, fid);
   if (lane < m) {
     const uint32_t upto = lane == 31 ? 0xffffffffu : ((2u << lane) - 1u);
-    const int first = 31 - __clz(fsm & upto);
-    eres[fs + E.fstart[fid] + (lane - first)] = sym;
+    const int firstlane = 31 - __clz(fsm & upto);
+    ws.tok[pos + (lane - firstlane)] = (int32_t)sym;
     if (fst) {
       const uint32_t after = fsm & ~upto;
       const int nx = after ? __ffs(after) - 1 : m;
-      E.fcnt[fid] = (uint16_t)(nx - lane);
+      ws.fcnt[pos] = nx - lane;
     }
   }
+  // every fragment of a batch starts in the same 512-byte chunk
+  if (lane == 0) atomicAdd(&ws.ctot[start / BCHUNK], (uint32_t)m);
+  __syncwarp();
 }
 
-// 228 KB of shared memory per SM less 1 KB reserved per CTA: at least 8 CTAs
-static_assert(8 * (sizeof(ChunkEngine) + 1024) <= 228 * 1024, "K3 shared memory exceeds 8 CTAs per SM");
+struct EngineSmem {
+  union {
+    CtaBatch cb;
+    WarpBuf wb[B_THREADS / 32];
+  } u;
+  uint8_t owner[B_THREADS / 32][SB_MAX];
+  int scan[B_THREADS / 32];
+  unsigned long long scan64[B_THREADS / 32];
+  int sflags;
+  uint32_t idx;
+};
 
-__global__ void __launch_bounds__(K3_THREADS) k_bpe_chunk(Call c, Workspace ws, DevVocab V) {
-  extern __shared__ __align__(16) uint8_t dsm[];
-  ChunkEngine& E = *reinterpret_cast<ChunkEngine*>(dsm);
-  const int tid = threadIdx.x, T = K3_THREADS, lane = tid & 31, warp = tid >> 5;
-  const long long chunk = blockIdx.x;
-  const long long r0 = chunk * BCHUNK;
-  const long long r1 = min(r0 + BCHUNK, c.n);
-  const long long lim = min(r0 + B_RANGE, c.n);
-  if (tid < B_RANGE / 32) {
-    const long long p = r0 + 32ll * tid;
-    uint32_t v = 0;
-    if (p < lim) {
-      v = ws.pstart[(r0 >> 5) + tid];
-      if (lim - p < 32) v &= (1u << (lim - p)) - 1u;
-    }
-    E.bits[tid] = v;
-  }
-  if (tid == 0) {
-    E.sflags = 0;
-    E.big = -1;
-  }
-  __syncthreads();
-  if (tid < 32) {
-    // first and last fragment start in [r0, r1) (words 0..15), first start in [r1, lim) (16..23)
-    const uint32_t w = lane < B_RANGE / 32 ? E.bits[lane] : 0u;
-    const uint32_t nz = __ballot_sync(0xffffffffu, lane < BCHUNK / 32 && w != 0u);
-    const uint32_t nz1 = __ballot_sync(0xffffffffu, lane >= BCHUNK / 32 && w != 0u) >> (BCHUNK / 32);
-    if (lane == 0) {
-      long long first = -1, last = -1, end = -1;
-      if (nz) {
-        const int a = __ffs(nz) - 1, b = 31 - __clz(nz);
-        first = r0 + 32ll * a + (__ffs(E.bits[a]) - 1);
-        last = r0 + 32ll * b + (31 - __clz(E.bits[b]));
-      }
-      if (r1 >= c.n) end = c.n;
-      else if (nz1) {
-        const int a = __ffs(nz1) - 1;
-        end = r1 + 32ll * a + (__ffs(E.bits[BCHUNK / 32 + a]) - 1);
-      } else if (lim >= c.n) end = c.n;
-      long long lf = -1;
-      if (first >= 0 && (end < 0 || end - last > B_CAP)) {  // the last fragment is long: queue it
-        lf = last;
-        end = last;
-        const uint32_t q = atomicAdd(&ws.st->long_count, 1u);
-        ws.longq[q] = Frag{last, chunk};
-      }
-      E.first = first;
-      E.end = end;
-      E.longfrag = lf;
-    }
-  }
-  __syncthreads();
-  const long long fs = E.first;
-  if (fs < 0) {  // no fragment starts here (the chunk lies inside a long fragment)
-    if (tid == 0) {
-      ws.cm_first[chunk] = -1;
-      ws.cm_count[chunk] = 0;
-      ws.cm_long[chunk] = -1;
-    }
-    return;
-  }
-  const int span = (int)(E.end - fs);
-  const int rel = (int)(fs - r0);
-  for (int i = tid; i < span; i += T) E.text[i] = c.text[fs + i];
-  {  // fragment starts in [fs, min(r1, end)): thread t looks at 4 bit positions
-    const int q0 = tid * 4;
-    const uint32_t nib = (E.bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
-    uint32_t mine = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (((nib >> q) & 1u) && r0 + q0 + q < E.end) mine |= 1u << q;
-    int nf = 0;
-    int idx = block_excl_sum(__popc(mine), &nf, E.scan);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if ((mine >> q) & 1u) E.fstart[idx++] = (uint16_t)(q0 + q - rel);
-    if (tid == 0) {
-      E.nf = nf;
-      E.fstart[nf] = (uint16_t)span;
-    }
-  }
-  __syncthreads();
-  const int nf = E.nf;
-  // settle single bytes and whole tokens: at most 4 fragments per thread,
-  // every first probe issued before any is used
-  const int FB = (nf + T - 1) / T;
-  const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
-  {
-    unsigned long long h[4];
-    uint32_t slot[4];
-    uint4 e[4];
-    int fa[4], fL[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int f = flo + q;
-      fa[q] = 0; fL[q] = 0; h[q] = 0; slot[q] = 0;
-      e[q] = make_uint4(0u, 0u, 0u, 0u);
-      if (f < fhi) {
-        fa[q] = E.fstart[f];
-        fL[q] = E.fstart[f + 1] - fa[q];
-        if (fL[q] > 1 && whole_eligible(V, fL[q])) {
-          h[q] = bytes_hash(E.text + fa[q], fL[q]);
-          slot[q] = whole_first_slot(V, h[q]);
-          e[q] = __ldg(reinterpret_cast<const uint4*>(V.whole + slot[q]));
-        }
-      }
-    }
-    int scount = 0, ucount = 0, sbytes = 0, ubytes = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int f = flo + q;
-      if (f < fhi) {
-        const int L = fL[q];
-        int t = -1;
-        if (L == 1) t = __ldg(V.byte_id + E.text[fa[q]]);
-        else if (whole_eligible(V, L)) t = whole_lookup_at(V, E.text + fa[q], L, h[q], slot[q], e[q]);
-        E.ftok[f] = t;
-        E.fcnt[f] = t >= 0 ? 1 : 0;
-        if (t < 0) {
-          if (L <= 32) { ++scount; sbytes += L; }
-          else if (L <= B_CAP) { ++ucount; ubytes += L; }
-          else E.big = f;  // at most one per chunk
-        }
-      }
-    }
-    int ns = 0, nu = 0, sb_all = 0, ub_all = 0;
-    int si = block_excl_sum(scount, &ns, E.scan);
-    int so = block_excl_sum(sbytes, &sb_all, E.scan);
-    int ui = block_excl_sum(ucount, &nu, E.scan);
-    int uo = block_excl_sum(ubytes, &ub_all, E.scan);
-    for (int f = flo; f < fhi; ++f) {
-      if (E.ftok[f] >= 0) continue;
-      const int L = E.fstart[f + 1] - E.fstart[f];
-      if (L <= 32) {
-        E.slist[si] = (uint16_t)f;
-        E.soff[si] = (uint16_t)so;
-        ++si;
-        so += L;
-      } else if (L <= B_CAP) {
-        E.ulist[ui] = (uint16_t)f;
-        E.ueoff[ui] = (uint16_t)uo;
-        ++ui;
-        uo += L;
-      }
-    }
-    if (tid == 0) {
-      E.soff[ns] = (uint16_t)sb_all;
-      E.ueoff[nu] = (uint16_t)ub_all;
-      E.ns = ns;
-      E.nu = nu;
-    }
-  }
-  __syncthreads();
-  // short fragments: greedy batches of at most 32 bytes, in order
-  if (tid == 0) {
-    const int ns = E.ns;
-    int nb = 0, k = 0;
-    while (k < ns) {
-      E.sbat[nb++] = (uint16_t)k;
-      const int b0 = E.soff[k];
-      ++k;
-      while (k < ns && E.soff[k + 1] - b0 <= 32) ++k;
-    }
-    E.sbat[nb] = (uint16_t)ns;
-    E.nb = nb;
-  }
-  __syncthreads();
-  uint32_t* const eres = ws.e_sym[0];  // engine results, at their fragment's byte offset
-  {
-    const int nb = E.nb;
-    for (int b = warp; b < nb; b += K3_WARPS) warp_batch(E, E.u.wb[warp], c, V, ws.st, eres, fs, E.sbat[b], E.sbat[b + 1]);
-  }
-  __syncthreads();
-  // fragments of 33..B_CAP bytes: CTA engine batches
-  const int nu = E.nu;
-  CtaBatch& C = E.u.cb;
-  for (int ub = 0; ub < nu;) {
-    if (tid == 0) {  // largest ue with ueoff[ue] - ueoff[ub] <= B_CAP
-      int a = ub + 1, b = nu;
-      while (a < b) {
-        const int mid = (a + b + 1) >> 1;
-        if (E.ueoff[mid] - E.ueoff[ub] <= B_CAP) a = mid; else b = mid - 1;
-      }
-      E.batch_end = a;
-    }
+__global__ void __launch_bounds__(B_THREADS) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
+  __shared__ EngineSmem S;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  DevStatus* st = ws.st;
+  const uint32_t nwide = *(volatile const uint32_t*)&st->wide_count;
+  while (true) {
+    if (tid == 0) S.idx = atomicAdd(&st->wide_taken, 1u);
     __syncthreads();
-    const int ue = E.batch_end;
-    const int base = E.ueoff[ub];
-    const int M = E.ueoff[ue] - base;
-    for (int i = tid; i < M; i += T) {
-      int a = ub, b = ue - 1;  // fragment k with ueoff[k] <= base + i < ueoff[k+1]
-      while (a < b) {
-        const int mid = (a + b + 1) >> 1;
-        if (E.ueoff[mid] <= base + i) a = mid; else b = mid - 1;
-      }
-      const int f = E.ulist[a];
-      const int j = base + i - E.ueoff[a];
-      const int32_t id = __ldg(V.byte_id + E.text[E.fstart[f] + j]);
-      C.sym[i] = (uint32_t)id;
-      C.len[i] = (uint16_t)(1u | (j == 0 ? FRAG_START : 0u));
-      C.fidx[i] = (uint16_t)f;
-      C.ml[i] = __ldg(V.max_left + id);
-      C.mr[i] = __ldg(V.max_right + id);
-    }
+    const uint32_t idx = S.idx;
     __syncthreads();
-    for (int i = tid; i < M; i += T)
-      C.kr[i] = (i + 1 >= M || (C.len[i + 1] & FRAG_START)) ? KR_WALL : merge_lookup(V, C.sym[i], C.sym[i + 1]);
-    __syncthreads();
-
-    int m = M;
-    for (int sweep = 0; sweep <= M; ++sweep) {
-      const int B = (m + T - 1) / T;
-      const int lo = min(tid * B, m), hi = min(lo + B, m);
-      // A: any mergeable pair left?  any overlapping equal-rank pairs?
-      int fl2 = 0;
-      for (int i = lo; i < hi; ++i) {
-        const uint32_t k = kr_rank(C.kr[i]);
-        if (mergeable(k)) {
-          fl2 |= 1;
-          if (i > 0 && kr_rank(C.kr[i - 1]) == k) fl2 |= 2;
-        }
-      }
-      fl2 = __reduce_or_sync(0xffffffffu, fl2);
-      if (lane == 0 && fl2) atomicOr(&E.sflags, fl2);
-      __syncthreads();
-      const int flags = E.sflags;
-      if (!(flags & 1)) break;
-      if (flags & 2) {
-        int lastrun = -1;
-        for (int i = lo; i < hi; ++i)
-          if (i == 0 || kr_rank(C.kr[i - 1]) != kr_rank(C.kr[i])) lastrun = i;
-        int run = block_excl_max(lastrun, E.scan);
-        for (int i = lo; i < hi; ++i) {
-          if (i == 0 || kr_rank(C.kr[i - 1]) != kr_rank(C.kr[i])) run = i;
-          C.rs[i] = (uint16_t)run;
-        }
-        __syncthreads();
-      }
-      // B: safe pairs
-      if (V.monotone) {
-        auto mlf = [&](int x) { return (int)C.ml[x]; };
-        auto mrf = [&](int x) { return (int)C.mr[x]; };
-        for (int i = lo; i < hi; ++i) {
-          const uint32_t k = kr_rank(C.kr[i]);
-          const int u = (flags & 2) ? (int)C.rs[i] : i;
-          C.fl[i] = (mergeable(k) && pair_safe(C.len, C.kr, m, i, u, k, mlf, mrf)) ? 1 : 0;
-        }
-      } else {
-        unsigned long long best = ~0ull;
-        for (int i = lo; i < hi; ++i) {
-          const uint32_t k = kr_rank(C.kr[i]);
-          if (mergeable(k)) {
-            const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
-            best = key < best ? key : best;
-          }
-        }
-        best = block_min_u64(best, E.scan64);
-        for (int i = lo; i < hi; ++i) C.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
-      }
-      __syncthreads();
-      // C: merge, look up the new pairs, compact
-      uint32_t nsym[B_EPT];
-      uint16_t nlen[B_EPT], nfi[B_EPT], nml[B_EPT], nmr[B_EPT];
-      unsigned long long nkr[B_EPT];
-      uint32_t keep = 0;
-#pragma unroll
-      for (int j = 0; j < B_EPT; ++j) {
-        const int i = lo + j;
-        nsym[j] = 0; nlen[j] = 0; nfi[j] = 0; nml[j] = 0; nmr[j] = 0; nkr[j] = KR_WALL;
-        if (i < hi && !(i > 0 && C.fl[i - 1])) {
-          keep |= 1u << j;
-          const bool mg = C.fl[i] != 0;
-          if (mg) {
-            const uint32_t r = kr_result(C.kr[i]);
-            nsym[j] = r;
-            nlen[j] = (uint16_t)(((C.len[i] & LEN_MASK) + (C.len[i + 1] & LEN_MASK)) | (C.len[i] & FRAG_START));
-            nml[j] = __ldg(V.max_left + r);
-            nmr[j] = __ldg(V.max_right + r);
-          } else {
-            nsym[j] = C.sym[i];
-            nlen[j] = C.len[i];
-            nml[j] = C.ml[i];
-            nmr[j] = C.mr[i];
-          }
-          nfi[j] = C.fidx[i];
-          const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
-          if (jn >= m || (C.len[jn] & FRAG_START)) nkr[j] = KR_WALL;
-          else if (!mg && !C.fl[jn]) nkr[j] = C.kr[i];  // unchanged pair keeps its key
-          else nkr[j] = merge_lookup(V, nsym[j], C.fl[jn] ? kr_result(C.kr[jn]) : C.sym[jn]);
-        }
-      }
-      int newm = 0;
-      const int bpos = block_excl_sum(__popc(keep), &newm, E.scan);
-#pragma unroll
-      for (int j = 0; j < B_EPT; ++j) {
-        if ((keep >> j) & 1u) {
-          const int p = bpos + __popc(keep & ((1u << j) - 1u));
-          C.sym[p] = nsym[j];
-          C.len[p] = nlen[j];
-          C.kr[p] = nkr[j];
-          C.fidx[p] = nfi[j];
-          C.ml[p] = nml[j];
-          C.mr[p] = nmr[j];
-        }
-      }
-      if (tid == 0) E.sflags = 0;
-      m = newm;
-      __syncthreads();
-      if (sweep == M && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
-    }
-    // this batch's results: ids per fragment, symbols to the per-byte scratch
-    for (int i = tid; i < m; i += T)
-      if (C.len[i] & FRAG_START) E.feng[C.fidx[i]] = (uint16_t)i;
-    __syncthreads();
-    for (int k = ub + tid; k < ue; k += T) {
-      const int f = E.ulist[k];
-      const int nx = (k + 1 < ue) ? E.feng[E.ulist[k + 1]] : m;
-      E.fcnt[f] = (uint16_t)(nx - E.feng[f]);
-    }
-    for (int i = tid; i < m; i += T) {
-      const int f = C.fidx[i];
-      eres[fs + E.fstart[f] + (i - E.feng[f])] = C.sym[i];
-    }
-    if (tid == 0) E.sflags = 0;
-    __syncthreads();
-    ub = ue;
+    if (idx >= nwide) break;
+    const Frag f = ws.wq[idx];
+    cta_fragment(c, ws, V, f.start, (int)f.len, S.u.cb, S.scan, S.scan64, &S.sflags);
   }
-  // an unresolved fragment longer than a batch holds
-  const int big = E.big;
-  if (big >= 0) {
-    const long long a = fs + E.fstart[big];
-    const int L = E.fstart[big + 1] - E.fstart[big];
-    const int m = global_engine(c, ws, V, a, L, reinterpret_cast<int32_t*>(eres) + a, E.scan, E.scan64);
-    if (tid == 0) E.fcnt[big] = (uint16_t)m;
-    __syncthreads();
-  }
-  // first id of each fragment, then the ids
-  int ids = 0;
-  for (int f = flo; f < fhi; ++f) ids += E.fcnt[f];
-  int total = 0;
-  int oo = block_excl_sum(ids, &total, E.scan);
-  for (int f = flo; f < fhi; ++f) {
-    E.fout[f] = (uint16_t)oo;
-    oo += E.fcnt[f];
-  }
-  __syncthreads();
-  for (int f = tid; f < nf; f += T) {
-    const int o = E.fout[f];
-    if (E.ftok[f] >= 0) {
-      ws.tok[fs + o] = E.ftok[f];
-    } else {
-      const long long e0 = fs + E.fstart[f];
-      const int cnt = E.fcnt[f];
-      for (int j = 0; j < cnt; ++j) ws.tok[fs + o + j] = (int32_t)eres[e0 + j];
-    }
-  }
-  if (tid == 0) {
-    ws.cm_first[chunk] = fs;
-    ws.cm_count[chunk] = total;
-    ws.cm_long[chunk] = E.longfrag;
-  }
-  // batch: ids before each item start in this chunk (K5 adds the chunk's offset)
-  if (c.item_off) {
-    if (tid == 0) {
-      int a = 0, b = c.n_items + 1;  // first item start >= r0
-      while (a < b) {
-        const int mid = (a + b) >> 1;
-        if (c.item[mid] < r0) a = mid + 1; else b = mid;
-      }
-      E.item0 = a;
-    }
-    __syncthreads();
-    for (int k = (int)E.item0 + tid; k <= c.n_items; k += T) {
-      const long long x = c.item[k];
-      if (x >= r1) break;
-      int a = 0, b = nf;  // fragment starting at x (or the long fragment after the last)
-      while (a < b) {
-        const int mid = (a + b) >> 1;
-        if (fs + E.fstart[mid] < x) a = mid + 1; else b = mid;
-      }
-      c.item_off[k] = a < nf ? E.fout[a] : total;
-    }
+  const uint32_t nbat = *(volatile const uint32_t*)&st->sbatch_count;
+  while (true) {
+    uint32_t b = 0;
+    if (lane == 0) b = atomicAdd(&st->sbatch_taken, 1u);
+    b = __shfl_sync(0xffffffffu, b, 0);
+    if (b >= nbat) break;
+    short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
   }
 }
 
 // ---------------------------------------------------------------------------
-// K4: the queued long last fragments of chunks, one CTA each, with the
-// global-memory engine; ids at the fragment's byte offset
+// K4: fragments longer than B_CAP bytes, one CTA each, with the global-memory
+// engine; ids at the fragment's byte offset, their number in fcnt
 
 __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws, DevVocab V) {
   __shared__ int sh[LONG_THREADS / 32];
@@ -929,39 +854,42 @@ __global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws,
     __syncthreads();
     if (idx >= count) break;
     const Frag f = ws.longq[idx];
-    // end: the next fragment start after f.start, or the text end
-    if (tid == 0) s_end = (unsigned long long)c.n;
+    // end: known from the queue entry, or the next fragment start after
+    // f.start (or the text end)
+    if (tid == 0) s_end = f.len > 0 ? (unsigned long long)(f.start + f.len) : (unsigned long long)c.n;
     __syncthreads();
-    const long long w0 = (f.start + 1) >> 5, wn = (c.n + 31) >> 5;
-    for (long long base = w0; base < wn; base += T) {
-      const long long wi = base + tid;
-      if (wi < wn) {
-        uint32_t wv = ws.pstart[wi];
-        if (wi == w0) wv &= ~0u << ((f.start + 1) & 31);
-        if (wi * 32 + 32 > c.n) wv &= (c.n - wi * 32 >= 32) ? ~0u : ((1u << (c.n - wi * 32)) - 1u);
-        if (wv) atomicMin(&s_end, (unsigned long long)(wi * 32 + __ffs(wv) - 1));
+    if (f.len <= 0) {
+      const long long w0 = (f.start + 1) >> 5, wn = (c.n + 31) >> 5;
+      for (long long base = w0; base < wn; base += T) {
+        const long long wi = base + tid;
+        if (wi < wn) {
+          uint32_t wv = ws.pstart[wi];
+          if (wi == w0) wv &= ~0u << ((f.start + 1) & 31);
+          if (wi * 32 + 32 > c.n) wv &= (c.n - wi * 32 >= 32) ? ~0u : ((1u << (c.n - wi * 32)) - 1u);
+          if (wv) atomicMin(&s_end, (unsigned long long)(wi * 32 + __ffs(wv) - 1));
+        }
+        __syncthreads();
+        const bool found = s_end < (unsigned long long)c.n;
+        __syncthreads();
+        if (found) break;
       }
-      __syncthreads();
-      const bool found = s_end < (unsigned long long)c.n;
-      __syncthreads();
-      if (found) break;
     }
     const long long a = f.start;
     const int m = global_engine(c, ws, V, a, (int)((long long)s_end - a), ws.tok + a, sh, sh64);
-    if (tid == 0) ws.cm_long_count[f.chunk] = m;
+    if (tid == 0) {
+      ws.fcnt[a] = m;
+      atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
+    }
     __syncthreads();
   }
 }
 
-void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaFuncSetAttribute(k_bpe_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ChunkEngine));
-    attr_set[dev] = true;
-  }
-  k_bpe_chunk<<<(unsigned)n_bchunks(c.n), K3_THREADS, sizeof(ChunkEngine), s>>>(c, w, v);
+void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
+  k_settle<<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
+}
+
+void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
+  k_bpe_engine<<<n_sms * 12, B_THREADS, 0, s>>>(c, w, v);  // 12 CTAs of 40 registers per SM
 }
 
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {

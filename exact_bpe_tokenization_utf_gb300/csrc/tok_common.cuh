@@ -1,20 +1,28 @@
 // Shared definitions of the GB300 exact BPE tokenizer library.
 //
 // Pipeline (one pass over a text or a packed batch; "TokTier: exact stateful
-// tokenization for agentic LLM serving", Section 4), all on 1 KiB chunks:
-//   K1 run_summary   the chunk's effect on three run states (digit-run offset
-//                    mod 3, "CR/LF-only since an O-run" whitespace prefix,
-//                    "CR/LF later in this whitespace run")
-//   K2 boundaries    UTF-8 validation + per-code-point class + run
-//                    decomposition rules -> fragment-start bitmask (Section 4.1)
-//   K3 bpe_chunk     every fragment that starts in a 512-byte chunk is encoded
-//                    by one CTA: single bytes and whole self-encoding tokens
-//                    with one probe, the rest in shared memory (batches of
-//                    B_CAP symbols, all certified-safe pairs merged per sweep);
-//                    a longer last fragment is queued (Section 4.2)
-//   K4 bpe_long      queued fragments, one CTA each, arrays in global memory
-//   K5 emit          per-chunk token counts -> offsets (decoupled look-back),
-//                    coalesced copy of the ids
+// tokenization for agentic LLM serving", Section 4):
+//   K1 run_summary   per 1 KiB chunk: its effect on three run states (digit-run
+//                    offset mod 3, "CR/LF-only since an O-run" whitespace
+//                    prefix, "CR/LF later in this whitespace run")
+//   K2 boundaries    per 1 KiB chunk: UTF-8 validation + per-code-point class +
+//                    run decomposition rules -> fragment-start bitmask
+//                    (Section 4.1)
+//   K3 settle        per 512-byte chunk: every fragment that is one byte, or
+//                    whose bytes are a token that encodes to itself, is
+//                    settled with one probe; the others are queued: those of
+//                    at most 32 bytes packed into warp batches, 33..B_CAP
+//                    bytes one by one, longer ones for K4 (Section 4.2)
+//   K3b bpe_engine   persistent: CTAs take 33..B_CAP-byte fragments (shared-
+//                    memory engine), then warps take short batches (one symbol
+//                    per lane); every sweep merges all certified-safe pairs
+//   K4 bpe_long      longer fragments, one CTA each, arrays in global memory
+//   K5a scan         every stage adds the ids it produced to its fragment's
+//                    512-byte chunk total; one CTA scans the totals
+//   K5 emit          per chunk: fragment counts -> offsets, copy of the ids
+//                    in text order
+// Every stage leaves a fragment's ids at the fragment's byte offset in `tok`
+// and their number at the same offset in `fcnt`.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -25,12 +33,12 @@ constexpr int CHUNK = 1024;        // bytes per chunk (every per-chunk kernel)
 constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K1 / K2
 constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
-constexpr int BCHUNK = 512;        // bytes per BPE / emit CTA (K3, K5)
-constexpr int B_CAP = 256;         // engine symbols per batch; a longer last fragment goes to K4
-constexpr int B_RANGE = BCHUNK + B_CAP;  // bytes a K3 CTA covers: its chunk + the tail of its last fragment
-constexpr int B_THREADS = 128;     // K5
-constexpr int K3_THREADS = 128;    // K3: 4 warps
-constexpr int B_EPT = B_CAP / K3_THREADS;  // engine symbols per thread at most
+constexpr int BCHUNK = 512;        // bytes per settle / emit CTA (K3, K5)
+constexpr int B_THREADS = 128;     // K3, K3b, K5
+constexpr int B_CAP = 256;         // longest fragment of the K3b shared-memory engine; longer ones go to K4
+constexpr int S_RANGE = BCHUNK + B_CAP;  // bytes K3 stages: its chunk + the tail of its last fragment
+constexpr int B_EPT = B_CAP / B_THREADS; // engine symbols per thread at most
+constexpr int SB_MAX = 32;         // bytes (symbols) of a warp batch
 constexpr int LONG_THREADS = 1024; // K4
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
@@ -73,10 +81,11 @@ struct DevVocab {
   int monotone;               // every merge that uses a token comes after every merge making it
 };
 
-// one queued long fragment: its start; the chunk whose last fragment it is
+// a queued fragment: its first byte and its length (-1: ends at the next
+// fragment start, to be found)
 struct Frag {
   long long start;
-  long long chunk;
+  long long len;
 };
 
 // device-side per-call status and work counters
@@ -85,22 +94,26 @@ struct DevStatus {
   uint32_t epoch;
   unsigned long long err_off;   // first malformed UTF-8 byte (atomicMin), ~0 if none
   unsigned long long n_ids;
-  uint32_t long_count, long_taken;
+  unsigned long long sfrag_count;  // short fragments queued
+  uint32_t sbatch_count, sbatch_taken;  // warp batches of short fragments
+  uint32_t wide_count, wide_taken;      // fragments of 33..B_CAP bytes
+  uint32_t long_count, long_taken;      // longer fragments
   uint32_t emit_ticket, emit_done;
-  uint32_t pad[8];
+  uint32_t pad[4];
 };
 
 struct Workspace {
   uint8_t* text;            // device copy of host input (host entry points)
   uint32_t* csum;           // K1 chunk summaries
   uint32_t* pstart;         // fragment-start bitmask
-  int32_t* tok;             // token ids, compacted per chunk at the chunk's first fragment start
-  long long* cm_first;      // per chunk: first fragment start in it, or -1
-  int32_t* cm_count;        // per chunk: ids K3 produced  (K3 / K5 chunks are BCHUNK bytes)
-  long long* cm_long;       // per chunk: start of its queued long fragment, or -1
-  int32_t* cm_long_count;   // per chunk: ids K4 produced for it
-  Frag* longq;              // K4 queue
-  unsigned long long* lb;   // K5 look-back words
+  int32_t* tok;             // a fragment's ids, at the fragment's byte offset
+  int32_t* fcnt;            // a fragment's number of ids, at its byte offset
+  unsigned long long* sfrag;   // short fragments: start << 8 | length, in batch order
+  unsigned long long* sbatch;  // warp batches: first sfrag index << 4 | (fragments - 1)
+  Frag* wq;                 // fragments of 33..B_CAP bytes
+  Frag* longq;              // longer fragments (K4)
+  uint32_t* ctot;           // ids of the fragments that start in each 512-byte chunk (added up as they finish)
+  unsigned long long* cpre; // ids before each 512-byte chunk (K5a scan)
   DevStatus* st;
   // K4 engine storage, indexed by byte position of the fragment
   uint32_t* e_sym[2];
@@ -110,6 +123,12 @@ struct Workspace {
   int32_t* e_rs;
   uint64_t cap_bytes;       // capacity in bytes of the per-byte arrays
   uint64_t cap_chunks;
+};
+
+// device range K3 prefetches into L2 for K3b (the merge table)
+struct Prefetch {
+  const void* p;
+  unsigned long long bytes;
 };
 
 struct Call {
@@ -122,6 +141,7 @@ struct Call {
   int32_t* out;               // device ids
   long long* item_off;        // device, n_items + 1 (batch) or nullptr
   long long* user_status;     // device int64[4] or nullptr
+  Prefetch pf;
 };
 
 __host__ __device__ inline uint32_t merge_slot(unsigned long long key, uint32_t bits) {
@@ -233,8 +253,10 @@ __device__ __forceinline__ int utf8_decode(const uint8_t* s, int avail, uint32_t
 // host-side launchers (defined in the kernel translation units)
 void launch_run_summary(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
-void launch_bpe_chunk(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
+void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
+void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
 void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
+void launch_scan(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_emit(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);
 

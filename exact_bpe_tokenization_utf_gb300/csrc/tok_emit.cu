@@ -2,22 +2,41 @@
 // exact stateful tokenization for agentic LLM serving", Section 4.3 returns
 // an id array; Section 4.4: ids only, no byte offsets).
 //
-// Each CTA owns a 512-byte chunk and emits the ids of the fragments that start
-// in it (K3 left them compacted; a long last fragment's ids come from K4).  The number of tokens before the range comes from a
-// decoupled look-back over the CTAs' published counts (Merrill and Garland,
-// "Single-pass parallel prefix scan with decoupled look-back", 2016): ranges
-// are taken in ticket order, so a CTA only waits on CTAs that already run;
-// every wait is bounded and reports TOK_ETIMEOUT instead of hanging.
+// Every BPE stage left a fragment's ids and their count at the fragment's byte
+// offset, and added the count to the total of the 512-byte chunk the fragment
+// starts in.  K5a scans the chunk totals in one CTA (ids before each chunk);
+// K5 then copies, one CTA per chunk, the ids of the fragments that start in
+// it.  Neither waits on another CTA.
 #include "tok_common.cuh"
 
 namespace tokgb {
 
-// look-back word: epoch (30 bits) | flag (2 bits) | value (32 bits)
-constexpr unsigned long long LB_AGG = 1ull, LB_INC = 2ull;
-constexpr int LB_SPIN_LIMIT = 1 << 22;
+namespace {
 
-__device__ __forceinline__ unsigned long long lb_pack(uint32_t epoch, unsigned long long flag, uint32_t v) {
-  return ((unsigned long long)(epoch & 0x3FFFFFFFu) << 34) | (flag << 32) | v;
+constexpr int SCAN_THREADS = 1024;
+constexpr int SCAN_PER_THREAD = 4;
+
+// block-wide exclusive sums (blockDim.x a multiple of 32; sh holds blockDim/32 words)
+template <class T>
+__device__ __forceinline__ T block_excl_sum_t(T v, T* total, T* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  T inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const T o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  T pre = 0, tot = 0;
+  for (int k = 0; k < nw; ++k) {
+    const T x = sh[k];
+    pre += k < warp ? x : T(0);
+    tot += x;
+  }
+  *total = tot;
+  __syncthreads();
+  return pre + inc - v;
 }
 
 __device__ void write_user_status(const Call& c, const DevStatus* st) {
@@ -31,69 +50,116 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
   c.user_status[3] = 0;
 }
 
-__global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
-  __shared__ uint32_t s_chunk;
-  __shared__ unsigned long long s_prefix;
-  __shared__ int s_item;
+}  // namespace
+
+// K5a: exclusive scan of the chunk totals, one CTA, SCAN_PER_THREAD
+// consecutive chunks per thread per tile
+__global__ void __launch_bounds__(SCAN_THREADS) k_scan(Call c, Workspace ws) {
+  __shared__ unsigned long long sh[SCAN_THREADS / 32];
+  const long long nch = n_bchunks(c.n);
   const int tid = threadIdx.x;
+  unsigned long long carry = 0;
+  for (long long base = 0; base < nch; base += (long long)SCAN_THREADS * SCAN_PER_THREAD) {
+    const long long i0 = base + (long long)tid * SCAN_PER_THREAD;
+    unsigned long long v[SCAN_PER_THREAD], sum = 0;
+#pragma unroll
+    for (int q = 0; q < SCAN_PER_THREAD; ++q) {
+      v[q] = i0 + q < nch ? ws.ctot[i0 + q] : 0u;
+      sum += v[q];
+    }
+    unsigned long long tile = 0;
+    unsigned long long pre = carry + block_excl_sum_t(sum, &tile, sh);
+#pragma unroll
+    for (int q = 0; q < SCAN_PER_THREAD; ++q) {
+      if (i0 + q < nch) ws.cpre[i0 + q] = pre;
+      pre += v[q];
+    }
+    carry += tile;
+  }
+  if (tid == 0) ws.st->n_ids = carry;
+}
+
+// K5: the ids of the fragments that start in one 512-byte chunk
+__global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
+  __shared__ uint32_t bits[BCHUNK / 32];
+  __shared__ uint16_t fstart[BCHUNK];
+  __shared__ int fcount[BCHUNK];
+  __shared__ int foff[BCHUNK];
+  __shared__ uint16_t big[BCHUNK];
+  __shared__ int scan[B_THREADS / 32];
+  __shared__ int s_item, s_nbig;
+  const int tid = threadIdx.x, T = B_THREADS;
   const long long nch = n_bchunks(c.n);
   DevStatus* st = ws.st;
-  if (tid == 0) s_chunk = atomicAdd(&st->emit_ticket, 1u);
-  __syncthreads();
-  const long long chunk = s_chunk;
+  const long long chunk = blockIdx.x;
   const long long r0 = chunk * BCHUNK;
   const long long r1 = min(r0 + BCHUNK, c.n);
-  const long long first = ws.cm_first[chunk];
-  const int n_short = first >= 0 ? ws.cm_count[chunk] : 0;
-  const long long lf = first >= 0 ? ws.cm_long[chunk] : -1;
-  const int n_long = lf >= 0 ? ws.cm_long_count[chunk] : 0;
-  const uint32_t total = (uint32_t)(n_short + n_long);
-  if (tid < 32) {
-    // warp 0: publish this chunk's count, then look back 32 predecessors at a
-    // time until one has published its inclusive prefix
-    const int lane = tid;
-    volatile unsigned long long* lb = ws.lb;
-    const uint32_t ep = c.epoch & 0x3FFFFFFFu;
-    if (lane == 0 && chunk > 0) {
-      __threadfence();
-      lb[chunk] = lb_pack(c.epoch, LB_AGG, total);
+  if (tid == 0) s_nbig = 0;
+  if (tid < BCHUNK / 32) {
+    const long long p = r0 + 32ll * tid;
+    uint32_t v = 0;
+    if (p < r1) {
+      v = ws.pstart[(r0 >> 5) + tid];
+      if (r1 - p < 32) v &= (1u << (r1 - p)) - 1u;
     }
-    unsigned long long prefix = 0;
-    bool timed_out = false;
-    for (long long top = chunk - 1; top >= 0; top -= 32) {
-      const long long j = top - lane;
-      unsigned long long v = j >= 0 ? lb[j] : lb_pack(c.epoch, LB_INC, 0u);
-      int spins = 0;
-      while (true) {
-        const bool ready = (uint32_t)(v >> 34) == ep;
-        if (__all_sync(0xffffffffu, ready)) break;
-        if (++spins > LB_SPIN_LIMIT) { timed_out = true; break; }
-        __nanosleep(64);
-        if (!ready) v = lb[j];
-      }
-      if (timed_out) break;
-      const uint32_t inc = __ballot_sync(0xffffffffu, ((v >> 32) & 3ull) == LB_INC);
-      const int stop = inc ? __ffs(inc) - 1 : 31;  // nearest predecessor with an inclusive prefix
-      unsigned long long x = lane <= stop ? (uint32_t)v : 0ull;
+    bits[tid] = v;
+  }
+  __syncthreads();
+  // the fragments that start in this chunk, and their id counts
+  const int q0 = tid * 4;
+  const uint32_t mine = (bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
+  int nf = 0;
+  int idx = block_excl_sum_t(__popc(mine), &nf, scan);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-      prefix += x;
-      if (inc) break;
+  for (int q = 0; q < 4; ++q)
+    if ((mine >> q) & 1u) fstart[idx++] = (uint16_t)(q0 + q);
+  __syncthreads();
+  const int FB = (nf + T - 1) / T;
+  const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
+  int ids = 0;
+  for (int f = flo; f < fhi; ++f) {
+    // a fragment has between 1 and (bytes to the text end) ids; anything else
+    // would be a bug upstream, reported instead of written out of bounds
+    int k = ws.fcnt[r0 + fstart[f]];
+    if (k < 1 || k > c.n - (r0 + fstart[f])) {
+      atomicExch(&st->code, ST_EINTERNAL);
+      k = 0;
     }
-    if (lane == 0) {
-      if (timed_out) atomicExch(&st->code, ST_ETIMEOUT);
-      __threadfence();
-      lb[chunk] = lb_pack(c.epoch, LB_INC, (uint32_t)(prefix + total));
-      s_prefix = prefix;
-      if (chunk == nch - 1) st->n_ids = prefix + total;
+    fcount[f] = k;
+    ids += k;
+  }
+  int total = 0;
+  int o = block_excl_sum_t(ids, &total, scan);
+  for (int f = flo; f < fhi; ++f) {
+    foff[f] = o;
+    o += fcount[f];
+  }
+  const unsigned long long base = ws.cpre[chunk];
+  const unsigned long long n_ids = st->n_ids;
+  if (base + (unsigned long long)total > n_ids) {  // the chunk totals disagree with the counts: a bug upstream
+    if (tid == 0) atomicExch(&st->code, ST_EINTERNAL);
+    total = 0;
+  }
+  __syncthreads();
+  // ids in text order: short fragments by their thread, long ones by the CTA
+  if (total > 0) {
+    for (int f = flo; f < fhi; ++f) {
+      const int k = fcount[f];
+      const long long a = r0 + fstart[f];
+      if (k <= 8) {
+        for (int j = 0; j < k; ++j) c.out[base + foff[f] + j] = ws.tok[a + j];
+      } else {
+        big[atomicAdd(&s_nbig, 1)] = (uint16_t)f;
+      }
     }
   }
   __syncthreads();
-  const unsigned long long base = s_prefix;
-  // ids: the chunk's fragments, then its long fragment (always its last one)
-  for (int j = tid; j < n_short; j += B_THREADS) c.out[base + j] = ws.tok[first + j];
-  for (int j = tid; j < n_long; j += B_THREADS) c.out[base + n_short + j] = ws.tok[lf + j];
-  // batch: K3 stored the ids before each item start relative to its chunk
+  for (int b = 0; b < s_nbig; ++b) {
+    const int f = big[b];
+    const long long a = r0 + fstart[f];
+    for (int j = tid; j < fcount[f]; j += T) c.out[base + foff[f] + j] = ws.tok[a + j];
+  }
+  // batch: ids before each item start in this chunk
   if (c.item_off) {
     if (tid == 0) {
       int a = 0, b = c.n_items + 1;
@@ -104,9 +170,15 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
       s_item = a;
     }
     __syncthreads();
-    for (int k = s_item + tid; k <= c.n_items; k += B_THREADS) {
-      if (c.item[k] >= r1) break;
-      c.item_off[k] += (long long)base;
+    for (int k = s_item + tid; k <= c.n_items; k += T) {
+      const long long x = c.item[k];
+      if (x >= r1) break;
+      int a = 0, b = nf;  // the fragment that starts at x
+      while (a < b) {
+        const int mid = (a + b) >> 1;
+        if (r0 + fstart[mid] < x) a = mid + 1; else b = mid;
+      }
+      c.item_off[k] = (long long)base + (a < nf ? foff[a] : total);
     }
   }
   // the last CTA to finish completes the status
@@ -116,9 +188,8 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
     const uint32_t done = atomicAdd(&st->emit_done, 1u);
     if (done == (uint32_t)(nch - 1)) {
       __threadfence();
-      const unsigned long long nid = *(volatile unsigned long long*)&st->n_ids;
       if (c.item_off) {
-        for (int k = c.n_items; k >= 0 && c.item[k] >= c.n; --k) c.item_off[k] = (long long)nid;
+        for (int k = c.n_items; k >= 0 && c.item[k] >= c.n; --k) c.item_off[k] = (long long)n_ids;
       }
       write_user_status(c, st);
     }
@@ -134,6 +205,10 @@ __global__ void k_status_only(Call c, Workspace ws) {
   if (c.item_off)
     for (int k = 0; k <= c.n_items; ++k) c.item_off[k] = 0;
   write_user_status(c, st);
+}
+
+void launch_scan(const Call& c, const Workspace& w, cudaStream_t s) {
+  k_scan<<<1, SCAN_THREADS, 0, s>>>(c, w);
 }
 
 void launch_emit(const Call& c, const Workspace& w, cudaStream_t s) {
