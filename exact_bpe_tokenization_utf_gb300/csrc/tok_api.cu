@@ -21,9 +21,8 @@ using namespace tokgb;
 
 namespace {
 
-constexpr int N_STAGES = 7;
-const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_settle", "k_bpe_engine",
-                                     "k_bpe_long",    "k_scan",       "k_emit"};
+constexpr int N_STAGES = 5;
+const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_settle", "k_bpe_engine", "k_emit"};
 
 thread_local std::string g_load_error;
 
@@ -205,12 +204,8 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
     if (tm) cudaEventRecord(h->ev[3], s);
     launch_bpe_engine(c, h->ws, h->v, h->n_sms, s);
     if (tm) cudaEventRecord(h->ev[4], s);
-    launch_bpe_long(c, h->ws, h->v, h->n_sms, s);
-    if (tm) cudaEventRecord(h->ev[5], s);
-    launch_scan(c, h->ws, s);
-    if (tm) cudaEventRecord(h->ev[6], s);
     launch_emit(c, h->ws, s);
-    if (tm) cudaEventRecord(h->ev[7], s);
+    if (tm) cudaEventRecord(h->ev[5], s);
     h->launches += N_STAGES;
     h->have_times = tm;
   }

@@ -123,6 +123,28 @@ __device__ __forceinline__ int block_excl_max(int v, int* sh) {
   return lane == 0 ? pre : max(pre, ex);
 }
 
+__device__ __forceinline__ unsigned long long block_excl_sum64(unsigned long long v, unsigned long long* total,
+                                                               unsigned long long* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  unsigned long long inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  unsigned long long pre = 0, tot = 0;
+  for (int k = 0; k < nw; ++k) {
+    const unsigned long long x = sh[k];
+    pre += k < warp ? x : 0ull;
+    tot += x;
+  }
+  *total = tot;
+  __syncthreads();
+  return pre + inc - v;
+}
+
 __device__ __forceinline__ unsigned long long block_min_u64(unsigned long long v, unsigned long long* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
@@ -451,7 +473,7 @@ __device__ __forceinline__ int warp_sweeps(WarpBuf& B, const DevVocab& V, DevSta
 
 constexpr int S_MAX = BCHUNK / 2 + 1;  // fragments of >= 2 bytes that start in a chunk
 
-__global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevVocab V) {
+__global__ void __launch_bounds__(B_THREADS, 10) k_settle(Call c, Workspace ws, DevVocab V) {
   __shared__ __align__(16) uint8_t text[S_RANGE];
   __shared__ uint32_t bits[S_RANGE / 32];
   __shared__ uint16_t fstart[BCHUNK + 1];
@@ -459,6 +481,7 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
   __shared__ uint16_t soff[S_MAX + 1];  // their byte offsets among themselves, then the total
   __shared__ uint16_t sbat[S_MAX + 1];  // first slist entry of each warp batch, then ns
   __shared__ int scan[B_THREADS / 32];
+  __shared__ unsigned long long scan64[B_THREADS / 32];
   __shared__ long long s_last_end;
   __shared__ unsigned long long s_sbase;
   __shared__ uint32_t s_bbase, s_wbase, s_lbase;
@@ -558,11 +581,16 @@ __global__ void __launch_bounds__(B_THREADS) k_settle(Call c, Workspace ws, DevV
       }
     }
   }
-  int ns = 0, sb_all = 0, nw = 0, nl = 0;
-  int si = block_excl_sum(scount, &ns, scan);
-  int so = block_excl_sum(sbytes, &sb_all, scan);
-  int wi = block_excl_sum(wcount, &nw, scan);
-  int li = block_excl_sum(lcount, &nl, scan);
+  // one scan for the four counts, 16 bits each (every count of a chunk is < 2^16)
+  unsigned long long tot4 = 0;
+  const unsigned long long pre4 = block_excl_sum64(
+      (unsigned long long)scount | ((unsigned long long)sbytes << 16) | ((unsigned long long)wcount << 32) |
+          ((unsigned long long)lcount << 48),
+      &tot4, scan64);
+  int si = (int)(pre4 & 0xFFFFu), so = (int)((pre4 >> 16) & 0xFFFFu);
+  int wi = (int)((pre4 >> 32) & 0xFFFFu), li = (int)(pre4 >> 48);
+  const int ns = (int)(tot4 & 0xFFFFu), sb_all = (int)((tot4 >> 16) & 0xFFFFu);
+  const int nw = (int)((tot4 >> 32) & 0xFFFFu), nl = (int)(tot4 >> 48);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     if (flo + q < fhi && cls[q] == 1) {
@@ -810,12 +838,95 @@ struct EngineSmem {
   unsigned long long scan64[B_THREADS / 32];
   int sflags;
   uint32_t idx;
+  unsigned long long end;
+  int last;
 };
 
-__global__ void __launch_bounds__(B_THREADS) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
+// Exclusive scan of the 512-byte chunk totals into cpre, and the number of
+// ids; all threads of one CTA.
+__device__ void scan_chunk_totals(const Call& c, const Workspace& ws, unsigned long long* sh64) {
+  const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = T >> 5;
+  const long long nch = n_bchunks(c.n);
+  constexpr int PER = 8;
+  unsigned long long carry = 0;
+  for (long long base = 0; base < nch; base += (long long)T * PER) {
+    const long long i0 = base + (long long)tid * PER;
+    unsigned long long v[PER], sum = 0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      v[q] = i0 + q < nch ? ws.ctot[i0 + q] : 0u;
+      sum += v[q];
+    }
+    unsigned long long inc = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += o;
+    }
+    if (lane == 31) sh64[warp] = inc;
+    __syncthreads();
+    unsigned long long pre = carry, tile = 0;
+    for (int k = 0; k < nw; ++k) {
+      pre += k < warp ? sh64[k] : 0ull;
+      tile += sh64[k];
+    }
+    __syncthreads();
+    pre += inc - sum;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      if (i0 + q < nch) ws.cpre[i0 + q] = pre;
+      pre += v[q];
+    }
+    carry += tile;
+  }
+  if (tid == 0) ws.st->n_ids = carry;
+}
+
+// K3b: a persistent grid.  Longest work first: fragments of more than B_CAP
+// bytes (global-memory engine), then those of 33..B_CAP bytes (shared-memory
+// engine), both one fragment per CTA at a time; then every warp takes batches
+// of short fragments (warp engine).  The last CTA to finish scans the chunk
+// totals for K5.
+__global__ void __launch_bounds__(B_THREADS, 12) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
   __shared__ EngineSmem S;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = B_THREADS;
   DevStatus* st = ws.st;
+  const uint32_t nlong = *(volatile const uint32_t*)&st->long_count;
+  while (true) {
+    if (tid == 0) S.idx = atomicAdd(&st->long_taken, 1u);
+    __syncthreads();
+    const uint32_t idx = S.idx;
+    __syncthreads();
+    if (idx >= nlong) break;
+    const Frag f = ws.longq[idx];
+    // end: known from the queue entry, or the next fragment start after
+    // f.start (or the text end)
+    if (tid == 0) S.end = f.len > 0 ? (unsigned long long)(f.start + f.len) : (unsigned long long)c.n;
+    __syncthreads();
+    if (f.len <= 0) {
+      const long long w0 = (f.start + 1) >> 5, wn = (c.n + 31) >> 5;
+      for (long long base = w0; base < wn; base += T) {
+        const long long wi = base + tid;
+        if (wi < wn) {
+          uint32_t wv = ws.pstart[wi];
+          if (wi == w0) wv &= ~0u << ((f.start + 1) & 31);
+          if (wi * 32 + 32 > c.n) wv &= (c.n - wi * 32 >= 32) ? ~0u : ((1u << (c.n - wi * 32)) - 1u);
+          if (wv) atomicMin(&S.end, (unsigned long long)(wi * 32 + __ffs(wv) - 1));
+        }
+        __syncthreads();
+        const bool found = S.end < (unsigned long long)c.n;
+        __syncthreads();
+        if (found) break;
+      }
+    }
+    const long long a = f.start;
+    const int m = global_engine(c, ws, V, a, (int)((long long)S.end - a), ws.tok + a, S.scan, S.scan64);
+    if (tid == 0) {
+      ws.fcnt[a] = m;
+      atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
+    }
+    __syncthreads();
+  }
   const uint32_t nwide = *(volatile const uint32_t*)&st->wide_count;
   while (true) {
     if (tid == 0) S.idx = atomicAdd(&st->wide_taken, 1u);
@@ -834,53 +945,14 @@ __global__ void __launch_bounds__(B_THREADS) k_bpe_engine(Call c, Workspace ws, 
     if (b >= nbat) break;
     short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
   }
-}
-
-// ---------------------------------------------------------------------------
-// K4: fragments longer than B_CAP bytes, one CTA each, with the global-memory
-// engine; ids at the fragment's byte offset, their number in fcnt
-
-__global__ void __launch_bounds__(LONG_THREADS) k_bpe_long(Call c, Workspace ws, DevVocab V) {
-  __shared__ int sh[LONG_THREADS / 32];
-  __shared__ unsigned long long sh64[LONG_THREADS / 32];
-  __shared__ uint32_t s_idx;
-  __shared__ unsigned long long s_end;
-  const int tid = threadIdx.x, T = blockDim.x;
-  const uint32_t count = *(volatile uint32_t*)&ws.st->long_count;
-  while (true) {
-    if (tid == 0) s_idx = atomicAdd(&ws.st->long_taken, 1u);
-    __syncthreads();
-    const uint32_t idx = s_idx;
-    __syncthreads();
-    if (idx >= count) break;
-    const Frag f = ws.longq[idx];
-    // end: known from the queue entry, or the next fragment start after
-    // f.start (or the text end)
-    if (tid == 0) s_end = f.len > 0 ? (unsigned long long)(f.start + f.len) : (unsigned long long)c.n;
-    __syncthreads();
-    if (f.len <= 0) {
-      const long long w0 = (f.start + 1) >> 5, wn = (c.n + 31) >> 5;
-      for (long long base = w0; base < wn; base += T) {
-        const long long wi = base + tid;
-        if (wi < wn) {
-          uint32_t wv = ws.pstart[wi];
-          if (wi == w0) wv &= ~0u << ((f.start + 1) & 31);
-          if (wi * 32 + 32 > c.n) wv &= (c.n - wi * 32 >= 32) ? ~0u : ((1u << (c.n - wi * 32)) - 1u);
-          if (wv) atomicMin(&s_end, (unsigned long long)(wi * 32 + __ffs(wv) - 1));
-        }
-        __syncthreads();
-        const bool found = s_end < (unsigned long long)c.n;
-        __syncthreads();
-        if (found) break;
-      }
-    }
-    const long long a = f.start;
-    const int m = global_engine(c, ws, V, a, (int)((long long)s_end - a), ws.tok + a, sh, sh64);
-    if (tid == 0) {
-      ws.fcnt[a] = m;
-      atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
-    }
-    __syncthreads();
+  // the last CTA to finish scans the chunk totals
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) S.last = atomicAdd(&st->engine_done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (S.last) {
+    __threadfence();
+    scan_chunk_totals(c, ws, S.scan64);
   }
 }
 
@@ -890,10 +962,6 @@ void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStr
 
 void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
   k_bpe_engine<<<n_sms * 12, B_THREADS, 0, s>>>(c, w, v);  // 12 CTAs of 40 registers per SM
-}
-
-void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
-  k_bpe_long<<<n_sms, LONG_THREADS, 0, s>>>(c, w, v);
 }
 
 }  // namespace tokgb

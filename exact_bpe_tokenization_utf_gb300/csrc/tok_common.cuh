@@ -13,12 +13,12 @@
 //                    settled with one probe; the others are queued: those of
 //                    at most 32 bytes packed into warp batches, 33..B_CAP
 //                    bytes one by one, longer ones for K4 (Section 4.2)
-//   K3b bpe_engine   persistent: CTAs take 33..B_CAP-byte fragments (shared-
-//                    memory engine), then warps take short batches (one symbol
-//                    per lane); every sweep merges all certified-safe pairs
-//   K4 bpe_long      longer fragments, one CTA each, arrays in global memory
-//   K5a scan         every stage adds the ids it produced to its fragment's
-//                    512-byte chunk total; one CTA scans the totals
+//   K3b bpe_engine   persistent: CTAs take fragments longer than B_CAP bytes
+//                    (arrays in global memory), then 33..B_CAP-byte fragments
+//                    (shared memory), then warps take short batches (one
+//                    symbol per lane); every sweep merges all certified-safe
+//                    pairs.  Every fragment's id count is added to the total
+//                    of its 512-byte chunk; the last CTA scans the totals.
 //   K5 emit          per chunk: fragment counts -> offsets, copy of the ids
 //                    in text order
 // Every stage leaves a fragment's ids at the fragment's byte offset in `tok`
@@ -39,7 +39,6 @@ constexpr int B_CAP = 256;         // longest fragment of the K3b shared-memory 
 constexpr int S_RANGE = BCHUNK + B_CAP;  // bytes K3 stages: its chunk + the tail of its last fragment
 constexpr int B_EPT = B_CAP / B_THREADS; // engine symbols per thread at most
 constexpr int SB_MAX = 32;         // bytes (symbols) of a warp batch
-constexpr int LONG_THREADS = 1024; // K4
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
 
@@ -98,7 +97,8 @@ struct DevStatus {
   uint32_t sbatch_count, sbatch_taken;  // warp batches of short fragments
   uint32_t wide_count, wide_taken;      // fragments of 33..B_CAP bytes
   uint32_t long_count, long_taken;      // longer fragments
-  uint32_t emit_ticket, emit_done;
+  uint32_t engine_done;                 // K3b CTAs finished
+  uint32_t emit_done;
   uint32_t pad[4];
 };
 
@@ -113,7 +113,7 @@ struct Workspace {
   Frag* wq;                 // fragments of 33..B_CAP bytes
   Frag* longq;              // longer fragments (K4)
   uint32_t* ctot;           // ids of the fragments that start in each 512-byte chunk (added up as they finish)
-  unsigned long long* cpre; // ids before each 512-byte chunk (K5a scan)
+  unsigned long long* cpre; // ids before each 512-byte chunk (scanned at the end of K3b)
   DevStatus* st;
   // K4 engine storage, indexed by byte position of the fragment
   uint32_t* e_sym[2];
@@ -255,8 +255,6 @@ void launch_run_summary(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
 void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
-void launch_bpe_long(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
-void launch_scan(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_emit(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);
 

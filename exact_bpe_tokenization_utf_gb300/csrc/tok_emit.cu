@@ -4,17 +4,14 @@
 //
 // Every BPE stage left a fragment's ids and their count at the fragment's byte
 // offset, and added the count to the total of the 512-byte chunk the fragment
-// starts in.  K5a scans the chunk totals in one CTA (ids before each chunk);
-// K5 then copies, one CTA per chunk, the ids of the fragments that start in
-// it.  Neither waits on another CTA.
+// starts in; the last CTA of K3b scanned the totals (ids before each chunk).
+// K5 copies, one CTA per chunk, the ids of the fragments that start in it,
+// without waiting on another CTA.
 #include "tok_common.cuh"
 
 namespace tokgb {
 
 namespace {
-
-constexpr int SCAN_THREADS = 1024;
-constexpr int SCAN_PER_THREAD = 4;
 
 // block-wide exclusive sums (blockDim.x a multiple of 32; sh holds blockDim/32 words)
 template <class T>
@@ -51,33 +48,6 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
 }
 
 }  // namespace
-
-// K5a: exclusive scan of the chunk totals, one CTA, SCAN_PER_THREAD
-// consecutive chunks per thread per tile
-__global__ void __launch_bounds__(SCAN_THREADS) k_scan(Call c, Workspace ws) {
-  __shared__ unsigned long long sh[SCAN_THREADS / 32];
-  const long long nch = n_bchunks(c.n);
-  const int tid = threadIdx.x;
-  unsigned long long carry = 0;
-  for (long long base = 0; base < nch; base += (long long)SCAN_THREADS * SCAN_PER_THREAD) {
-    const long long i0 = base + (long long)tid * SCAN_PER_THREAD;
-    unsigned long long v[SCAN_PER_THREAD], sum = 0;
-#pragma unroll
-    for (int q = 0; q < SCAN_PER_THREAD; ++q) {
-      v[q] = i0 + q < nch ? ws.ctot[i0 + q] : 0u;
-      sum += v[q];
-    }
-    unsigned long long tile = 0;
-    unsigned long long pre = carry + block_excl_sum_t(sum, &tile, sh);
-#pragma unroll
-    for (int q = 0; q < SCAN_PER_THREAD; ++q) {
-      if (i0 + q < nch) ws.cpre[i0 + q] = pre;
-      pre += v[q];
-    }
-    carry += tile;
-  }
-  if (tid == 0) ws.st->n_ids = carry;
-}
 
 // K5: the ids of the fragments that start in one 512-byte chunk
 __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
@@ -205,10 +175,6 @@ __global__ void k_status_only(Call c, Workspace ws) {
   if (c.item_off)
     for (int k = 0; k <= c.n_items; ++k) c.item_off[k] = 0;
   write_user_status(c, st);
-}
-
-void launch_scan(const Call& c, const Workspace& w, cudaStream_t s) {
-  k_scan<<<1, SCAN_THREADS, 0, s>>>(c, w);
 }
 
 void launch_emit(const Call& c, const Workspace& w, cudaStream_t s) {
