@@ -851,7 +851,8 @@ __device__ void scan_chunk_totals(const Call& c, const Workspace& ws, unsigned l
   unsigned long long carry = 0;
   for (long long base = 0; base < nch; base += (long long)T * PER) {
     const long long i0 = base + (long long)tid * PER;
-    unsigned long long v[PER], sum = 0;
+    uint32_t v[PER];
+    unsigned long long sum = 0;
 #pragma unroll
     for (int q = 0; q < PER; ++q) {
       v[q] = i0 + q < nch ? ws.ctot[i0 + q] : 0u;
@@ -883,17 +884,22 @@ __device__ void scan_chunk_totals(const Call& c, const Workspace& ws, unsigned l
 }
 
 // K3b: a persistent grid.  Longest work first: fragments of more than B_CAP
-// bytes (global-memory engine), then those of 33..B_CAP bytes (shared-memory
-// engine), both one fragment per CTA at a time; then every warp takes batches
-// of short fragments (warp engine).  The last CTA to finish scans the chunk
-// totals for K5.
+// bytes (global-memory engine, taken one at a time), then those of 33..B_CAP
+// bytes (shared-memory engine, fragment i to CTA i mod grid), then batches of
+// short fragments (warp engine, batch b to warp b mod warps, counted from
+// the last CTA so that the CTAs with a 33..B_CAP-byte fragment get fewer).
+// Static assignment keeps thousands of warps off one contended counter.  The
+// last CTA to finish scans the chunk totals for K5.
 __global__ void __launch_bounds__(B_THREADS, 12) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
   __shared__ EngineSmem S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = B_THREADS;
   DevStatus* st = ws.st;
   const uint32_t nlong = *(volatile const uint32_t*)&st->long_count;
-  while (true) {
-    if (tid == 0) S.idx = atomicAdd(&st->long_taken, 1u);
+  while (nlong) {
+    // one thread decides for the CTA (the loop has barriers); the plain read
+    // first keeps CTAs without work off the contended counter
+    if (tid == 0)
+      S.idx = *(volatile const uint32_t*)&st->long_taken < nlong ? atomicAdd(&st->long_taken, 1u) : nlong;
     __syncthreads();
     const uint32_t idx = S.idx;
     __syncthreads();
@@ -928,23 +934,15 @@ __global__ void __launch_bounds__(B_THREADS, 12) k_bpe_engine(Call c, Workspace 
     __syncthreads();
   }
   const uint32_t nwide = *(volatile const uint32_t*)&st->wide_count;
-  while (true) {
-    if (tid == 0) S.idx = atomicAdd(&st->wide_taken, 1u);
-    __syncthreads();
-    const uint32_t idx = S.idx;
-    __syncthreads();
-    if (idx >= nwide) break;
-    const Frag f = ws.wq[idx];
+  for (uint32_t i = blockIdx.x; i < nwide; i += gridDim.x) {
+    const Frag f = ws.wq[i];
     cta_fragment(c, ws, V, f.start, (int)f.len, S.u.cb, S.scan, S.scan64, &S.sflags);
   }
+  __syncthreads();
   const uint32_t nbat = *(volatile const uint32_t*)&st->sbatch_count;
-  while (true) {
-    uint32_t b = 0;
-    if (lane == 0) b = atomicAdd(&st->sbatch_taken, 1u);
-    b = __shfl_sync(0xffffffffu, b, 0);
-    if (b >= nbat) break;
-    short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
-  }
+  const uint32_t nwarps = gridDim.x * (T / 32);
+  const uint32_t gw = (gridDim.x - 1 - blockIdx.x) * (T / 32) + warp;
+  for (uint32_t b = gw; b < nbat; b += nwarps) short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
   // the last CTA to finish scans the chunk totals
   __threadfence();
   __syncthreads();
