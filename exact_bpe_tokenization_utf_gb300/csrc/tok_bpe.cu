@@ -261,13 +261,15 @@ __device__ int global_engine(const Call& c, const Workspace& ws, const DevVocab&
 // ---------------------------------------------------------------------------
 // Engine storage
 
-struct WarpBuf {            // one warp's compaction buffer
+struct WarpBuf {            // one warp's compaction buffer, and the pair ranks for window walks
   uint32_t sym[32];
   unsigned long long kr[32];
   uint16_t len[32];         // byte length | FRAG_START
   uint16_t fidx[32];
   uint16_t ml[32];
   uint16_t mr[32];
+  uint32_t rank[32];        // rank of pair (i, i+1) this sweep
+  uint16_t blen[32];        // byte length of symbol i this sweep
 };
 
 struct CtaBatch {           // one batch of the CTA engine
@@ -353,44 +355,39 @@ __device__ __forceinline__ int warp_sweeps(WarpBuf& B, const DevVocab& V, DevSta
         safe = nbr_ok && left_clear && right_clear;
         need = nbr_ok && !(left_clear && right_clear);
       }
-      // a lower rank further away: walk the length-bounded windows
+      // a lower rank further away: walk the length-bounded windows, each lane
+      // on its own through the ranks and lengths in shared memory
       if (__any_sync(FULL, need)) {
-        bool ok = need;
-        // left: a token grown from pair q <= u-2 ends at symbol u-1
-        int cum = (int)__shfl_sync(FULL, lenb, max(u - 1, 0));
-        bool done = !(need && has_l && u >= 2);
-        for (int step = 2; step < 32; ++step) {
-          const int q = u - step;
-          const uint32_t kq = __shfl_sync(FULL, k, max(q, 0));
-          const int lq = (int)__shfl_sync(FULL, lenb, max(q, 0));
-          if (!done) {
-            if (q < 0 || kq == RANK_WALL) done = true;
-            else {
-              cum += lq;
-              if (cum > (int)ml_u) done = true;
-              else if (kq < k) { ok = false; done = true; }
+        B.rank[lane] = k;
+        B.blen[lane] = (uint16_t)lenb;
+        __syncwarp();
+        if (need) {
+          bool ok = true;
+          if (has_l && u >= 2) {
+            // left: a token grown from pair q <= u-2 ends at symbol u-1
+            int cum = B.blen[u - 1];
+            for (int q = u - 2; q >= 0; --q) {
+              const uint32_t kq = B.rank[q];
+              if (kq == RANK_WALL) break;
+              cum += B.blen[q];
+              if (cum > (int)ml_u) break;
+              if (kq < k) { ok = false; break; }
             }
           }
-          if (!__any_sync(FULL, !done)) break;
-        }
-        // right: a token grown from pair q >= i+2 starts at symbol i+2
-        cum = (int)__shfl_sync(FULL, lenb, min(lane + 2, 31));
-        done = !(need && ok && has_r);
-        for (int step = 2; step < 32; ++step) {
-          const int q = lane + step;
-          const uint32_t kq = __shfl_sync(FULL, k, min(q, 31));
-          const int lq = (int)__shfl_sync(FULL, lenb, min(q + 1, 31));
-          if (!done) {
-            if (q > 31 || kq == RANK_WALL) done = true;
-            else {
-              cum += lq;
-              if (cum > (int)mr_i1) done = true;
-              else if (kq < k) { ok = false; done = true; }
+          if (ok && has_r) {
+            // right: a token grown from pair q >= i+2 starts at symbol i+2
+            int cum = lane + 2 < 32 ? B.blen[lane + 2] : 0;
+            for (int q = lane + 2; q < 31; ++q) {
+              const uint32_t kq = B.rank[q];
+              if (kq == RANK_WALL) break;
+              cum += B.blen[q + 1];
+              if (cum > (int)mr_i1) break;
+              if (kq < k) { ok = false; break; }
             }
           }
-          if (!__any_sync(FULL, !done)) break;
+          safe = ok;
         }
-        if (need) safe = ok;
+        __syncwarp();
       }
     } else {
       // the rule itself: the leftmost lowest-rank pair of the batch
