@@ -887,7 +887,7 @@ __device__ void scan_chunk_totals(const Call& c, const Workspace& ws, unsigned l
 // the last CTA so that the CTAs with a 33..B_CAP-byte fragment get fewer).
 // Static assignment keeps thousands of warps off one contended counter.  The
 // last CTA to finish scans the chunk totals for K5.
-__global__ void __launch_bounds__(B_THREADS, 12) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
+__global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
   __shared__ EngineSmem S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = B_THREADS;
   DevStatus* st = ws.st;
@@ -956,7 +956,7 @@ void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStr
 }
 
 void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
-  k_bpe_engine<<<n_sms * 12, B_THREADS, 0, s>>>(c, w, v);  // 12 CTAs of 40 registers per SM
+  k_bpe_engine<<<n_sms * 16, B_THREADS, 0, s>>>(c, w, v);  // 16 CTAs of 32 registers per SM
 }
 
 }  // namespace tokgb
