@@ -31,9 +31,10 @@ _NAMES = {0: "TOK_OK", -1: "TOK_EINVAL", -2: "TOK_EUTF8", -3: "TOK_ENOMEM", -4: 
           -6: "TOK_ETIMEOUT", -7: "TOK_EMERGES"}
 
 # every symbol include/tok.h declares
-SYMBOLS = ["tok_load", "tok_encode", "tok_encode_batch", "tok_encode_device", "tok_encode_batch_device",
-           "tok_pretokenize", "tok_pretokenize_batch", "tok_last_error", "tok_error_offset", "tok_content_hash", "tok_set_timing",
-           "tok_stage_times", "tok_launch_count", "tok_free", "tok_pretokenize_device_noalloc"]
+SYMBOLS = ["tok_load", "tok_encode", "tok_encode_offsets", "tok_encode_batch", "tok_encode_device",
+           "tok_encode_offsets_device", "tok_encode_batch_device", "tok_pretokenize", "tok_pretokenize_batch",
+           "tok_last_error", "tok_error_offset", "tok_content_hash", "tok_set_timing", "tok_stage_times",
+           "tok_launch_count", "tok_free", "tok_pretokenize_device_noalloc"]
 
 
 class TokError(RuntimeError):
@@ -62,8 +63,10 @@ def lib():
     L.tok_load.argtypes = [U8P, U64P, U32, ctypes.POINTER(ctypes.c_uint32), U32, ctypes.c_int,
                            ctypes.POINTER(P)]
     L.tok_encode.argtypes = [P, U8P, U64, I32P, U64, U64P]
+    L.tok_encode_offsets.argtypes = [P, U8P, U64, I32P, I64P, U64, U64P]
     L.tok_encode_batch.argtypes = [P, ctypes.POINTER(U8P), U64P, U32, I32P, U64, U64P]
     L.tok_encode_device.argtypes = [P, P, U64, P, U64, P, P]
+    L.tok_encode_offsets_device.argtypes = [P, P, U64, P, P, U64, P, P]
     L.tok_encode_batch_device.argtypes = [P, P, U64, P, U32, P, U64, P, P, P]
     L.tok_pretokenize.argtypes = [P, U8P, U64, I64P, U64, U64P]
     L.tok_pretokenize_batch.argtypes = [P, ctypes.POINTER(U8P), U64P, U32, I64P, U64, U64P]
@@ -81,8 +84,9 @@ def lib():
     L.tok_launch_count.restype = ctypes.c_uint64
     L.tok_free.argtypes = [P]
     L.tok_free.restype = None
-    for fn in ("tok_load", "tok_encode", "tok_encode_batch", "tok_encode_device", "tok_encode_batch_device",
-               "tok_pretokenize", "tok_pretokenize_batch", "tok_set_timing", "tok_stage_times"):
+    for fn in ("tok_load", "tok_encode", "tok_encode_offsets", "tok_encode_batch", "tok_encode_device",
+               "tok_encode_offsets_device", "tok_encode_batch_device", "tok_pretokenize", "tok_pretokenize_batch",
+               "tok_set_timing", "tok_stage_times"):
         getattr(L, fn).restype = ctypes.c_int
     _lib = L
     return L
@@ -174,6 +178,19 @@ class Tokenizer:
                                        len(ids), ctypes.byref(n)))
         return ids[:n.value].copy()
 
+    def encode_with_offsets(self, data):
+        """(ids, offsets): offsets[k] is the byte offset where token k starts."""
+        data = bytes(data)
+        arr, p = _u8(data) if data else (None, None)
+        ids = np.empty(max(len(data), 1), dtype=np.int32)
+        offs = np.empty(max(len(data), 1), dtype=np.int64)
+        n = ctypes.c_uint64()
+        self._check(self._L.tok_encode_offsets(self._h, p, len(data),
+                                               ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                               offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(ids),
+                                               ctypes.byref(n)))
+        return ids[:n.value].copy(), offs[:n.value].copy()
+
     def encode_batch(self, items):
         items = [bytes(x) for x in items]
         arrs = [np.frombuffer(x, dtype=np.uint8) if x else np.zeros(1, np.uint8) for x in items]
@@ -230,6 +247,12 @@ class Tokenizer:
         stream); no host sync.  Pointers are ints (e.g. tensor.data_ptr());
         d_status is a device int64[4]."""
         self._check(self._L.tok_encode_device(self._h, d_text, n_bytes, d_ids, cap, d_status, stream or None))
+
+    def encode_offsets_device(self, d_text, n_bytes, d_ids, d_offsets, cap, d_status, stream=0):
+        """encode_device that also writes every token's byte offset (device
+        int64, capacity cap) to d_offsets."""
+        self._check(self._L.tok_encode_offsets_device(self._h, d_text, n_bytes, d_ids, d_offsets, cap, d_status,
+                                                      stream or None))
 
     def encode_batch_device(self, d_text, n_bytes, d_item_start, n_items, d_ids, cap, d_item_off, d_status,
                             stream=0):

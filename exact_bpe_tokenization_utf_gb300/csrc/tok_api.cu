@@ -52,6 +52,7 @@ struct tok_handle {
   // workspace
   Workspace ws{};
   int32_t* d_out = nullptr;           // ids of host-side calls
+  long long* d_off = nullptr;         // token byte offsets of host-side calls (allocated on first use)
   long long* d_items = nullptr;       // item starts of host-side batch calls
   long long* d_item_off = nullptr;
   uint64_t cap_items = 0;
@@ -109,11 +110,12 @@ void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
   void* ptrs[] = {w.text,     w.csum,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,    w.sbatch,
                   w.wq,       w.longq,    w.ctot,     w.cpre,     w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0],
-                  w.e_len[1], w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,     h->d_out};
+                  w.e_len[1], w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,     h->d_out,   h->d_off};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   w = Workspace{};
   h->d_out = nullptr;
+  h->d_off = nullptr;
 }
 
 // Grow the workspace to hold n bytes (no-op when it already does).
@@ -204,7 +206,7 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
     if (tm) cudaEventRecord(h->ev[3], s);
     launch_bpe_engine(c, h->ws, h->v, h->n_sms, s);
     if (tm) cudaEventRecord(h->ev[4], s);
-    launch_emit(c, h->ws, s);
+    launch_emit(c, h->ws, h->v, s);
     if (tm) cudaEventRecord(h->ev[5], s);
     h->launches += N_STAGES;
     h->have_times = tm;
@@ -465,12 +467,25 @@ int tok_stage_times(tok_handle* h, float* ms, const char** names, int cap) {
   return n;
 }
 
-int tok_encode(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, uint64_t cap, uint64_t* n_ids) {
+}  // extern "C"
+
+namespace {
+
+// host in, host out; offsets (or nullptr) receive every token's byte offset
+int encode_host(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, int64_t* offsets, uint64_t cap,
+                uint64_t* n_ids) {
   if (!h || !n_ids || (len && !text)) return fail(h, TOK_EINVAL, "bad argument");
   DeviceGuard g(h->dev);
   *n_ids = 0;
   int rc = ensure_workspace(h, len);
   if (rc) return rc;
+  if (offsets && !h->d_off) {
+    const cudaError_t e = dalloc(&h->d_off, h->ws.cap_bytes + 256);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, TOK_ENOMEM, "offset buffer allocation failed");
+    }
+  }
   cudaStream_t s = h->stream;
   if (len) {
     const cudaError_t e = cudaMemcpyAsync(h->ws.text, text, len, cudaMemcpyHostToDevice, s);
@@ -478,6 +493,7 @@ int tok_encode(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, u
   }
   Call c = base_call(h, h->ws.text, len);
   c.out = h->d_out;
+  c.out_off = offsets ? h->d_off : nullptr;
   rc = run_chain(h, c, s);
   if (rc) return rc;
   rc = read_status(h, s);
@@ -488,10 +504,26 @@ int tok_encode(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, u
   if (n) {
     if (!ids) return fail(h, TOK_EINVAL, "ids is NULL");
     cudaError_t e = cudaMemcpyAsync(ids, h->d_out, n * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && offsets)
+      e = cudaMemcpyAsync(offsets, h->d_off, n * sizeof(int64_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(h, e, "id copy");
   }
   return TOK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tok_encode(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, uint64_t cap, uint64_t* n_ids) {
+  return encode_host(h, text, len, ids, nullptr, cap, n_ids);
+}
+
+int tok_encode_offsets(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, int64_t* offsets,
+                       uint64_t cap, uint64_t* n_ids) {
+  if (!offsets) return fail(h, TOK_EINVAL, "offsets is NULL");
+  return encode_host(h, text, len, ids, offsets, cap, n_ids);
 }
 
 int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t* lens, uint32_t n, int32_t* ids,
@@ -546,6 +578,11 @@ int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t*
 
 int tok_encode_device(tok_handle* h, const uint8_t* d_text, uint64_t len, int32_t* d_ids, uint64_t cap,
                       int64_t* d_status, void* stream) {
+  return tok_encode_offsets_device(h, d_text, len, d_ids, nullptr, cap, d_status, stream);
+}
+
+int tok_encode_offsets_device(tok_handle* h, const uint8_t* d_text, uint64_t len, int32_t* d_ids,
+                              int64_t* d_offsets, uint64_t cap, int64_t* d_status, void* stream) {
   if (!h || !d_status || (len && (!d_text || !d_ids))) return fail(h, TOK_EINVAL, "bad argument");
   if (cap < len) return fail(h, TOK_EBUF, "cap must be >= len");
   DeviceGuard g(h->dev);
@@ -554,6 +591,7 @@ int tok_encode_device(tok_handle* h, const uint8_t* d_text, uint64_t len, int32_
   cudaStream_t s = static_cast<cudaStream_t>(stream);  // NULL: the CUDA default stream
   Call c = base_call(h, d_text, len);
   c.out = d_ids;
+  c.out_off = reinterpret_cast<long long*>(d_offsets);
   c.user_status = reinterpret_cast<long long*>(d_status);
   return run_chain(h, c, s);
 }

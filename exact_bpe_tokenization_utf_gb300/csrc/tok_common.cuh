@@ -139,6 +139,7 @@ struct Call {
   int pattern;
   uint32_t epoch;
   int32_t* out;               // device ids
+  long long* out_off;         // device: byte offset of every id's token (nullptr: not wanted)
   long long* item_off;        // device, n_items + 1 (batch) or nullptr
   long long* user_status;     // device int64[4] or nullptr
   Prefetch pf;
@@ -255,7 +256,7 @@ void launch_run_summary(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
 void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
-void launch_emit(const Call& c, const Workspace& w, cudaStream_t s);
+void launch_emit(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);
 
 __host__ __device__ inline long long n_chunks(long long n) { return (n + CHUNK - 1) / CHUNK; }

@@ -6,7 +6,10 @@
 // offset, and added the count to the total of the 512-byte chunk the fragment
 // starts in; the last CTA of K3b scanned the totals (ids before each chunk).
 // K5 copies, one CTA per chunk, the ids of the fragments that start in it,
-// without waiting on another CTA.
+// without waiting on another CTA.  On request it also writes every token's
+// byte offset: a fragment's first token starts at the fragment, each next
+// one where the previous token's bytes end (the session state of Sections
+// 3.1 and 3.4 keeps these offsets).
 #include "tok_common.cuh"
 
 namespace tokgb {
@@ -50,7 +53,7 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
 }  // namespace
 
 // K5: the ids of the fragments that start in one 512-byte chunk
-__global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
+__global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVocab V) {
   __shared__ uint32_t bits[BCHUNK / 32];
   __shared__ uint16_t fstart[BCHUNK];
   __shared__ int fcount[BCHUNK];
@@ -118,6 +121,13 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
       const long long a = r0 + fstart[f];
       if (k <= 8) {
         for (int j = 0; j < k; ++j) c.out[base + foff[f] + j] = ws.tok[a + j];
+        if (c.out_off) {
+          long long off = a;
+          for (int j = 0; j < k; ++j) {
+            c.out_off[base + foff[f] + j] = off;
+            off += __ldg(V.tok_len + ws.tok[a + j]);
+          }
+        }
       } else {
         big[atomicAdd(&s_nbig, 1)] = (uint16_t)f;
       }
@@ -128,6 +138,18 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws) {
     const int f = big[b];
     const long long a = r0 + fstart[f];
     for (int j = tid; j < fcount[f]; j += T) c.out[base + foff[f] + j] = ws.tok[a + j];
+    if (c.out_off) {
+      // offsets: exclusive scan of the token lengths, one tile of T ids at a time
+      long long carry = a;
+      for (int j0 = 0; j0 < fcount[f]; j0 += T) {
+        const int j = j0 + tid;
+        const int len = j < fcount[f] ? (int)__ldg(V.tok_len + ws.tok[a + j]) : 0;
+        int tile = 0;
+        const int ex = block_excl_sum_t(len, &tile, scan);
+        if (j < fcount[f]) c.out_off[base + foff[f] + j] = carry + ex;
+        carry += tile;
+      }
+    }
   }
   // batch: ids before each item start in this chunk
   if (c.item_off) {
@@ -177,8 +199,8 @@ __global__ void k_status_only(Call c, Workspace ws) {
   write_user_status(c, st);
 }
 
-void launch_emit(const Call& c, const Workspace& w, cudaStream_t s) {
-  k_emit<<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w);
+void launch_emit(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
+  k_emit<<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
 }
 
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s) {

@@ -84,6 +84,18 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
 int tok_encode(tok_handle* h, const uint8_t* text, uint64_t len,
                int32_t* ids, uint64_t cap, uint64_t* n_ids);
 
+/* tok_encode_offsets -- tok_encode that also returns where each token starts.
+ * The session state of Sections 3.1 and 3.4 keeps every token's byte
+ * offsets; Section 4.4's GPU path returns ids only and sends requests that
+ * need offsets to the CPU.  Here the device writes them: a fragment's first
+ * token starts at the fragment's first byte, every next one where the
+ * previous token's bytes end (token k ends at offsets[k+1], the last at len).
+ * offsets: host int64 array of capacity cap, filled like ids.
+ * Errors: as tok_encode; TOK_EINVAL if offsets is NULL.
+ */
+int tok_encode_offsets(tok_handle* h, const uint8_t* text, uint64_t len,
+                       int32_t* ids, int64_t* offsets, uint64_t cap, uint64_t* n_ids);
+
 /* tok_encode_batch -- encode n independent texts in one pass (host in, host
  * out).  Item k is texts[k][0..lens[k]); items never interact: every item
  * starts and ends a fragment exactly as a separate tok_encode call would.
@@ -108,6 +120,14 @@ int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t*
  */
 int tok_encode_device(tok_handle* h, const uint8_t* d_text, uint64_t len,
                       int32_t* d_ids, uint64_t cap, int64_t* d_status, void* stream);
+
+/* tok_encode_offsets_device -- tok_encode_device that also writes every
+ * token's byte offset (as tok_encode_offsets) to d_offsets (device, int64,
+ * capacity cap; NULL: none, which is tok_encode_device).
+ */
+int tok_encode_offsets_device(tok_handle* h, const uint8_t* d_text, uint64_t len,
+                              int32_t* d_ids, int64_t* d_offsets, uint64_t cap,
+                              int64_t* d_status, void* stream);
 
 /* tok_encode_batch_device -- device-resident batch.  d_text holds the items
  * back to back; d_item_start (device, n+1 int64) gives item k's bytes as

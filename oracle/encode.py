@@ -25,3 +25,20 @@ def encode(data, vocab, pattern_id, bpe=bpe_heap):
 
 def decode(ids, vocab):
     return b"".join(vocab.token_bytes[i] for i in ids)
+
+
+def token_offsets(ids, vocab):
+    """Byte offset where each token of an encoding starts: decoding
+    concatenates token bytes, so token k starts where the bytes of tokens
+    0..k-1 end (the byte offsets a session keeps, TokTier Sections 3.1, 3.4)."""
+    out, pos = [], 0
+    for i in ids:
+        out.append(pos)
+        pos += len(vocab.token_bytes[i])
+    return out
+
+
+def encode_with_offsets(data, vocab, pattern_id, bpe=bpe_heap):
+    ids = encode(data, vocab, pattern_id, bpe)
+    return ids, token_offsets(ids, vocab)
+

@@ -15,7 +15,7 @@ import pytest
 
 import textgen
 from oracle.bpe import bpe_heap
-from oracle.encode import decode, encode, pretoken_byte_spans
+from oracle.encode import decode, encode, encode_with_offsets, pretoken_byte_spans
 from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2
 from oracle.utf8 import Utf8Error
 from oracle.vocab import Vocab
@@ -111,6 +111,37 @@ def test_encode_session_1m_chars_100k_merges(pkg):
 def _token_starts(ids, v):
     lens = np.array([len(v.token_bytes[i]) for i in ids], dtype=np.int64)
     return np.concatenate([[0], np.cumsum(lens)])
+
+
+def test_token_offsets_match_oracle(pkg):
+    # the device's token byte offsets against the oracle's definition
+    for name, pat, data in (("gpt2_code_1k", PATTERN_GPT2, textgen.code_ascii(16384, 1001).encode()),
+                            ("cl100k_session_100k", PATTERN_CL100K, textgen.agentic_session(200_000, 1003).encode()),
+                            ("cl100k_session_100k", PATTERN_CL100K, textgen.adversarial(1 << 20, 1005, 0.02).encode())):
+        v, tok = pair(pkg, name, pat)
+        ids, offs = tok.encode_with_offsets(data)
+        want_ids, want_offs = encode_with_offsets(data, v, pat)
+        assert ids.tolist() == want_ids
+        assert offs.tolist() == want_offs
+
+
+def test_token_offsets_device_entry(pkg):
+    import torch
+    v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
+    data = textgen.agentic_session(50_000, 1013).encode()
+    n = len(data)
+    d_text = torch.frombuffer(bytearray(data), dtype=torch.uint8).cuda()
+    d_ids = torch.empty(n, dtype=torch.int32, device="cuda")
+    d_off = torch.empty(n, dtype=torch.int64, device="cuda")
+    d_st = torch.zeros(4, dtype=torch.int64, device="cuda")
+    tok.encode_offsets_device(d_text.data_ptr(), n, d_ids.data_ptr(), d_off.data_ptr(), n, d_st.data_ptr(),
+                              torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    st = d_st.cpu().tolist()
+    assert st[0] == 0
+    want_ids, want_offs = encode_with_offsets(data, v, PATTERN_CL100K)
+    assert d_ids[:st[1]].cpu().tolist() == want_ids
+    assert d_off[:st[1]].cpu().tolist() == want_offs
 
 
 def test_encode_batch_64_sessions(pkg):

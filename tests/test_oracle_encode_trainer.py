@@ -9,7 +9,7 @@ import pytest
 
 import textgen
 from oracle.bpe import bpe_heap, bpe_textbook
-from oracle.encode import decode, encode, pretoken_byte_spans
+from oracle.encode import decode, encode, encode_with_offsets, pretoken_byte_spans
 from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2
 from oracle.trainer import TrainError, fragment_counts, train, train_from_counts, train_naive
 from oracle.utf8 import Utf8Error
@@ -59,6 +59,21 @@ def test_splice_theorem(small_vocab):
                 certified += 1
                 assert encode(data[:c], v, pat) + encode(data[c:], v, pat) == whole
         assert certified > 20
+
+
+def test_token_offsets(small_vocab):
+    # each token's bytes sit at its offset; every fragment start is a token
+    # start (fragments are encoded independently, Appendix A.1)
+    v = small_vocab
+    for pat in (PATTERN_GPT2, PATTERN_CL100K):
+        data = textgen.agentic_session(8000, 9).encode()
+        ids, offs = encode_with_offsets(data, v, pat)
+        assert len(offs) == len(ids) and (not offs or offs[0] == 0)
+        ends = offs[1:] + [len(data)]
+        for i, a, b in zip(ids, offs, ends):
+            assert data[a:b] == v.token_bytes[i]
+        assert {a for a, _ in pretoken_byte_spans(data, pat)} <= set(offs)
+    assert encode_with_offsets(b"", v, PATTERN_GPT2) == ([], [])
 
 
 def test_utf8_error_offset():
