@@ -21,8 +21,8 @@ using namespace tokgb;
 
 namespace {
 
-constexpr int N_STAGES = 5;
-const char* kStageNames[N_STAGES] = {"k_run_summary", "k_boundaries", "k_settle", "k_bpe_engine", "k_emit"};
+constexpr int N_STAGES = 4;
+const char* kStageNames[N_STAGES] = {"k_boundaries", "k_settle", "k_bpe_engine", "k_emit"};
 
 thread_local std::string g_load_error;
 
@@ -62,6 +62,7 @@ struct tok_handle {
   uint32_t epoch = 0;
   std::string err;
   int64_t err_off = -1;
+  uint32_t last_epoch = 0;            // epoch of the latest call
   uint64_t launches = 0;
   bool timing = false;
   cudaEvent_t ev[N_STAGES + 1] = {};
@@ -108,7 +109,7 @@ cudaError_t dalloc(T** p, size_t count) {
 
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
-  void* ptrs[] = {w.text,     w.csum,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,    w.sbatch,
+  void* ptrs[] = {w.text,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,    w.sbatch,
                   w.wq,       w.longq,    w.ctot,     w.cpre,     w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0],
                   w.e_len[1], w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,     h->d_out,   h->d_off};
   for (void* p : ptrs)
@@ -131,7 +132,6 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   cudaError_t e = cudaSuccess;
   auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
   chk(dalloc(&w.text, cap + pad));
-  chk(dalloc(&w.csum, nch + 2));
   chk(dalloc(&w.pstart, cap / 32 + pad));
   chk(dalloc(&w.tok, cap + pad));
   // queue sizes: a queued short fragment has >= 2 bytes (a single byte always
@@ -155,6 +155,7 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.e_rs, cap + pad));
   chk(dalloc(&h->d_out, cap + pad));
   if (e == cudaSuccess) e = cudaMemset(w.pstart, 0, (cap / 32 + pad) * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(w.st, 0, sizeof(DevStatus));
   if (e != cudaSuccess) {
     free_workspace(h);
     cudaGetLastError();
@@ -184,13 +185,22 @@ int ensure_items(tok_handle* h, uint64_t n_items) {
   return TOK_OK;
 }
 
+// The epoch of a new call.  The UTF-8 error word is keyed by the low 24 bits
+// of the epoch (err_key): when they wrap, the word is cleared first.
+uint32_t next_epoch(tok_handle* h, cudaStream_t s) {
+  uint32_t e = ++h->epoch;
+  if (e >= 0x3FFFFFFFu) h->epoch = e = 1;
+  if ((e & 0xFFFFFFu) <= 1u) cudaMemsetAsync(&h->ws.st->err_off, 0, sizeof(unsigned long long), s);
+  h->last_epoch = e;
+  return e;
+}
+
 // Enqueue the whole chain for one call.
 int run_chain(tok_handle* h, Call c, cudaStream_t s) {
   c.pf.p = h->d_table;
   c.pf.bytes = sizeof(MergeEntry) << h->v.bits;
   c.pattern = h->pattern;
-  c.epoch = ++h->epoch;
-  if (h->epoch >= 0x3FFFFFFFu) h->epoch = 0;
+  c.epoch = next_epoch(h, s);
   if (c.n == 0) {
     launch_status_only(c, h->ws, s);
     h->launches += 1;
@@ -198,16 +208,14 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
   } else {
     const bool tm = h->timing;
     if (tm) cudaEventRecord(h->ev[0], s);
-    launch_run_summary(c, h->ws, s);
-    if (tm) cudaEventRecord(h->ev[1], s);
     launch_boundaries(c, h->ws, s);
-    if (tm) cudaEventRecord(h->ev[2], s);
+    if (tm) cudaEventRecord(h->ev[1], s);
     launch_settle(c, h->ws, h->v, s);
-    if (tm) cudaEventRecord(h->ev[3], s);
+    if (tm) cudaEventRecord(h->ev[2], s);
     launch_bpe_engine(c, h->ws, h->v, h->n_sms, s);
-    if (tm) cudaEventRecord(h->ev[4], s);
+    if (tm) cudaEventRecord(h->ev[3], s);
     launch_emit(c, h->ws, h->v, s);
-    if (tm) cudaEventRecord(h->ev[5], s);
+    if (tm) cudaEventRecord(h->ev[4], s);
     h->launches += N_STAGES;
     h->have_times = tm;
   }
@@ -230,9 +238,8 @@ int read_status(tok_handle* h, cudaStream_t s) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(h, e, "status read");
   collect_times(h);
-  h->err_off = -1;
-  if (h->h_status->err_off != ~0ull) {
-    h->err_off = (int64_t)h->h_status->err_off;
+  h->err_off = err_offset(h->last_epoch, h->h_status->err_off);
+  if (h->err_off >= 0) {
     char buf[96];
     snprintf(buf, sizeof buf, "invalid UTF-8 at byte %lld", (long long)h->err_off);
     return fail(h, TOK_EUTF8, buf);
@@ -625,10 +632,10 @@ static int pretokenize_impl(tok_handle* h, uint64_t len, uint32_t n_items, bool 
     c.item = h->d_items;
     c.n_items = (int)n_items;
   }
-  c.epoch = ++h->epoch;
-  launch_run_summary(c, h->ws, s);
+  c.pattern = h->pattern;
+  c.epoch = next_epoch(h, s);
   launch_boundaries(c, h->ws, s);
-  h->launches += 2;
+  h->launches += 1;
   h->have_times = false;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");

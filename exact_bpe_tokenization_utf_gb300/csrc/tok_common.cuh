@@ -2,12 +2,10 @@
 //
 // Pipeline (one pass over a text or a packed batch; "TokTier: exact stateful
 // tokenization for agentic LLM serving", Section 4):
-//   K1 run_summary   per 1 KiB chunk: its effect on three run states (digit-run
-//                    offset mod 3, "CR/LF-only since an O-run" whitespace
-//                    prefix, "CR/LF later in this whitespace run")
 //   K2 boundaries    per 1 KiB chunk: UTF-8 validation + per-code-point class +
 //                    run decomposition rules -> fragment-start bitmask
-//                    (Section 4.1)
+//                    (Section 4.1); the run states at the chunk's edges come
+//                    from the text just beyond them
 //   K3 settle        per 512-byte chunk: every fragment that is one byte, or
 //                    whose bytes are a token that encodes to itself, is
 //                    settled with one probe; the others are queued: those of
@@ -91,7 +89,7 @@ struct Frag {
 struct DevStatus {
   int32_t code;
   uint32_t epoch;
-  unsigned long long err_off;   // first malformed UTF-8 byte (atomicMin), ~0 if none
+  unsigned long long err_off;   // first malformed UTF-8 byte of the latest call that had one: err_key
   unsigned long long n_ids;
   unsigned long long sfrag_count;  // short fragments queued
   uint32_t sbatch_count, sbatch_taken;  // warp batches of short fragments
@@ -104,7 +102,6 @@ struct DevStatus {
 
 struct Workspace {
   uint8_t* text;            // device copy of host input (host entry points)
-  uint32_t* csum;           // K1 chunk summaries
   uint32_t* pstart;         // fragment-start bitmask
   int32_t* tok;             // a fragment's ids, at the fragment's byte offset
   int32_t* fcnt;            // a fragment's number of ids, at its byte offset
@@ -144,6 +141,21 @@ struct Call {
   long long* user_status;     // device int64[4] or nullptr
   Prefetch pf;
 };
+
+// The first malformed UTF-8 byte of a call, as one word that atomicMax keeps
+// across calls without a reset: the call's epoch (24 bits) above the
+// complement of the offset (40 bits).  A later call's key is larger (until
+// the epoch wraps, when the host clears the word); within a call the smallest
+// offset gives the largest key.
+constexpr unsigned long long ERR_OFF_MASK = (1ull << 40) - 1ull;
+__host__ __device__ inline unsigned long long err_key(uint32_t epoch, unsigned long long off) {
+  return ((unsigned long long)(epoch & 0xFFFFFFu) << 40) | (ERR_OFF_MASK - off);
+}
+// the offset in a key written by the call with this epoch, or -1
+__host__ __device__ inline long long err_offset(uint32_t epoch, unsigned long long key) {
+  if ((key >> 40) != (epoch & 0xFFFFFFu) || (key & ERR_OFF_MASK) == 0) return -1;
+  return (long long)(ERR_OFF_MASK - (key & ERR_OFF_MASK));
+}
 
 __host__ __device__ inline uint32_t merge_slot(unsigned long long key, uint32_t bits) {
   return (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> (64 - bits));
@@ -252,7 +264,6 @@ __device__ __forceinline__ int utf8_decode(const uint8_t* s, int avail, uint32_t
 #endif
 
 // host-side launchers (defined in the kernel translation units)
-void launch_run_summary(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
 void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
 void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);

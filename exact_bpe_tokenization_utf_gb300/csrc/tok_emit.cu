@@ -41,18 +41,19 @@ __device__ __forceinline__ T block_excl_sum_t(T v, T* total, T* sh) {
 
 __device__ void write_user_status(const Call& c, const DevStatus* st) {
   if (!c.user_status) return;
-  const unsigned long long eo = st->err_off;
+  const long long eo = err_offset(c.epoch, st->err_off);
   long long code = st->code;
-  if (eo != ~0ull) code = ST_EUTF8;
+  if (eo >= 0) code = ST_EUTF8;
   c.user_status[0] = code;
   c.user_status[1] = (long long)st->n_ids;
-  c.user_status[2] = eo == ~0ull ? -1 : (long long)eo;
+  c.user_status[2] = eo;
   c.user_status[3] = 0;
 }
 
 }  // namespace
 
 // K5: the ids of the fragments that start in one 512-byte chunk
+template <bool OFFS>
 __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVocab V) {
   __shared__ uint32_t bits[BCHUNK / 32];
   __shared__ uint16_t fstart[BCHUNK];
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
       const long long a = r0 + fstart[f];
       if (k <= 8) {
         for (int j = 0; j < k; ++j) c.out[base + foff[f] + j] = ws.tok[a + j];
-        if (c.out_off) {
+        if (OFFS) {
           long long off = a;
           for (int j = 0; j < k; ++j) {
             c.out_off[base + foff[f] + j] = off;
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
     const int f = big[b];
     const long long a = r0 + fstart[f];
     for (int j = tid; j < fcount[f]; j += T) c.out[base + foff[f] + j] = ws.tok[a + j];
-    if (c.out_off) {
+    if (OFFS) {
       // offsets: exclusive scan of the token lengths, one tile of T ids at a time
       long long carry = a;
       for (int j0 = 0; j0 < fcount[f]; j0 += T) {
@@ -192,7 +193,6 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
 __global__ void k_status_only(Call c, Workspace ws) {
   DevStatus* st = ws.st;
   st->code = ST_OK;
-  st->err_off = ~0ull;
   st->n_ids = 0;
   if (c.item_off)
     for (int k = 0; k <= c.n_items; ++k) c.item_off[k] = 0;
@@ -200,7 +200,8 @@ __global__ void k_status_only(Call c, Workspace ws) {
 }
 
 void launch_emit(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
-  k_emit<<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
+  if (c.out_off) k_emit<true><<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
+  else k_emit<false><<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
 }
 
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s) {

@@ -7,9 +7,9 @@
 // (cudaMalloc/cudaFree can serialise with in-flight work), and hosts that run
 // with a fixed, pre-reserved memory budget.  This entry point takes device
 // input and output buffers from the caller and keeps the only scratch it
-// needs (the per-chunk run-state summaries and a status block) in a
-// file-scope __device__ array of fixed size, which every GPU that loads the
-// library holds until the process exits.
+// needs (the status block the boundary kernel writes) in a file-scope
+// __device__ array of fixed size, which every GPU that loads the library
+// holds until the process exits.
 #include "../../include/tok.h"
 #include "tok_common.cuh"
 
@@ -17,27 +17,23 @@ using namespace tokgb;
 
 namespace {
 
-// Longest text one call accepts (64 MiB); the scratch holds one summary word
-// per pre-tokenizer chunk of that text plus the status block.
-constexpr uint64_t kNoAllocMaxBytes = 64ull << 20;
-constexpr uint64_t kNoAllocSummaryWords = kNoAllocMaxBytes / CHUNK + 2;
-
 struct NoAllocScratch {
   DevStatus st;
-  uint32_t csum[kNoAllocSummaryWords];
 };
 
 static __device__ __align__(256) NoAllocScratch g_noalloc_scratch;
 
-// Host-side stand-in for g_noalloc_scratch is not a device address: the
-// device address is looked up once per device with cudaGetSymbolAddress.
+// The device address of g_noalloc_scratch is looked up once per device with
+// cudaGetSymbolAddress; each device also counts its calls (the epoch keys the
+// UTF-8 error word, see err_key).
 constexpr int kMaxDevices = 64;
 NoAllocScratch* g_scratch_addr[kMaxDevices] = {};
+uint32_t g_epoch[kMaxDevices] = {};
 
-__global__ void k_noalloc_status(const NoAllocScratch* s, long long* d_status) {
-  const unsigned long long eo = s->st.err_off;
-  d_status[0] = eo != ~0ull ? TOK_EUTF8 : TOK_OK;
-  d_status[1] = eo != ~0ull ? (long long)eo : -1;
+__global__ void k_noalloc_status(const NoAllocScratch* s, uint32_t epoch, long long* d_status) {
+  const long long eo = err_offset(epoch, s->st.err_off);
+  d_status[0] = eo >= 0 ? TOK_EUTF8 : TOK_OK;
+  d_status[1] = eo;
 }
 
 }  // namespace
@@ -46,7 +42,6 @@ extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_t
                                               uint32_t* d_start_bits, int64_t* d_status, void* stream) {
   if (pattern_id != TOK_PAT_GPT2 && pattern_id != TOK_PAT_CL100K_STYLE) return TOK_EINVAL;
   if (!d_status || (len && (!d_text || !d_start_bits))) return TOK_EINVAL;
-  if (len > kNoAllocMaxBytes) return TOK_EBUF;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TOK_ECUDA;
   if (!g_scratch_addr[dev]) {
@@ -61,8 +56,14 @@ extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_t
   }
   NoAllocScratch* scratch = g_scratch_addr[dev];
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t epoch = ++g_epoch[dev];
+  if (epoch >= 0x3FFFFFFFu) g_epoch[dev] = epoch = 1;
+  if ((epoch & 0xFFFFFFu) <= 1u &&
+      cudaMemsetAsync(&scratch->st.err_off, 0, sizeof(unsigned long long), s) != cudaSuccess) {
+    cudaGetLastError();
+    return TOK_ECUDA;
+  }
   Workspace w{};
-  w.csum = scratch->csum;
   w.st = &scratch->st;
   w.pstart = d_start_bits;
   Call c{};
@@ -71,12 +72,10 @@ extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_t
   c.item = nullptr;
   c.n_items = 1;
   c.pattern = pattern_id;
-  c.epoch = 1;
+  c.epoch = epoch;
   if (len) {
-    // the summary kernel also resets the status block before anything reads it
-    launch_run_summary(c, w, s);
     launch_boundaries(c, w, s);
-    k_noalloc_status<<<1, 1, 0, s>>>(scratch, reinterpret_cast<long long*>(d_status));
+    k_noalloc_status<<<1, 1, 0, s>>>(scratch, epoch, reinterpret_cast<long long*>(d_status));
   } else {
     const long long ok[2] = {TOK_OK, -1};
     if (cudaMemcpyAsync(d_status, ok, sizeof ok, cudaMemcpyHostToDevice, s) != cudaSuccess) {

@@ -160,12 +160,12 @@ int tok_pretokenize_batch(tok_handle* h, const uint8_t* const* texts, const uint
  * synchronisation cudaMalloc/cudaFree can cause, hosts with a fixed memory
  * budget).  The paper has no counterpart: it is an integration entry point of
  * this library, not a step of the method.
- * Needs no handle and allocates nothing: its scratch (per-chunk run-state
- * summaries and a status block) lives in a fixed __device__ array of this
- * library that every GPU loading it holds until exit, sized for texts of at
- * most 64 MiB; longer texts return TOK_EBUF.  The first call on a device
- * looks up that array's device address (cudaGetSymbolAddress, with the device
- * current); make that first call before any stream capture.
+ * Needs no handle and allocates nothing: its scratch (the status block the
+ * boundary kernel writes) lives in a fixed __device__ array of this library
+ * that every GPU loading it holds until exit.  Calls on one device share that
+ * array: do not run two at once.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with the device current);
+ * make that first call before any stream capture.
  * d_text: device, len bytes.  d_start_bits: device uint32 words, at least
  *   ceil(len / 32) of them; bit p % 32 of word p / 32 is set iff a fragment
  *   starts at byte p (bits at p >= len are 0).

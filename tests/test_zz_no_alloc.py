@@ -57,7 +57,9 @@ def test_noalloc_pretokenizer_matches_allocating_entry_point():
         with pytest.raises(pkg.TokError) as e:
             tok.pretokenize(bad)
         assert rc == pkg.TOK_OK and d_st.cpu().tolist() == [pkg.TOK_EUTF8, e.value.offset]
-        # longer than the scratch allows: rejected before touching the device
-        assert L.tok_pretokenize_device_noalloc(pattern, d_text.data_ptr(), (64 << 20) + 1, d_bits.data_ptr(),
-                                                d_st.data_ptr(), ctypes.c_void_p(stream)) == pkg.TOK_EBUF
+        # invalid arguments are rejected before touching the device
+        assert L.tok_pretokenize_device_noalloc(pattern, d_text.data_ptr(), len(bad), d_bits.data_ptr(),
+                                                None, ctypes.c_void_p(stream)) == pkg.TOK_EINVAL
+        assert L.tok_pretokenize_device_noalloc(7, d_text.data_ptr(), len(bad), d_bits.data_ptr(),
+                                                d_st.data_ptr(), ctypes.c_void_p(stream)) == pkg.TOK_EINVAL
         tok.close()
