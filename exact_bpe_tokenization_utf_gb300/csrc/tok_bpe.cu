@@ -835,6 +835,7 @@ struct EngineSmem {
   unsigned long long scan64[B_THREADS / 32];
   int sflags;
   uint32_t idx;
+  uint32_t nq[3];           // queue sizes: long, 33..B_CAP bytes, short batches
   unsigned long long end;
   int last;
 };
@@ -891,7 +892,13 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
   __shared__ EngineSmem S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = B_THREADS;
   DevStatus* st = ws.st;
-  const uint32_t nlong = *(volatile const uint32_t*)&st->long_count;
+  if (tid == 0) {  // the queue sizes, loaded together (settle wrote them)
+    S.nq[0] = st->long_count;
+    S.nq[1] = st->wide_count;
+    S.nq[2] = st->sbatch_count;
+  }
+  __syncthreads();
+  const uint32_t nlong = S.nq[0];
   while (nlong) {
     // one thread decides for the CTA (the loop has barriers); the plain read
     // first keeps CTAs without work off the contended counter
@@ -930,13 +937,13 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
     }
     __syncthreads();
   }
-  const uint32_t nwide = *(volatile const uint32_t*)&st->wide_count;
+  const uint32_t nwide = S.nq[1];
   for (uint32_t i = blockIdx.x; i < nwide; i += gridDim.x) {
     const Frag f = ws.wq[i];
     cta_fragment(c, ws, V, f.start, (int)f.len, S.u.cb, S.scan, S.scan64, &S.sflags);
   }
   __syncthreads();
-  const uint32_t nbat = *(volatile const uint32_t*)&st->sbatch_count;
+  const uint32_t nbat = S.nq[2];
   const uint32_t nwarps = gridDim.x * (T / 32);
   const uint32_t gw = (gridDim.x - 1 - blockIdx.x) * (T / 32) + warp;
   for (uint32_t b = gw; b < nbat; b += nwarps) short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
