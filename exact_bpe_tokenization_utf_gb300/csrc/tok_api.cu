@@ -57,6 +57,8 @@ struct tok_handle {
   long long* d_item_off = nullptr;
   uint64_t cap_items = 0;
   DevStatus* h_status = nullptr;      // pinned
+  long long* h_ustatus = nullptr;     // pinned, written by the device: code, ids, UTF-8 error offset
+  long long* d_ustatus = nullptr;     // its device address
   long long* h_items = nullptr;       // pinned
   uint64_t cap_h_items = 0;
   uint32_t epoch = 0;
@@ -395,6 +397,8 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   if (e == cudaSuccess) e = cudaMemcpy(h->d_max_left, max_left.data(), n_vocab * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->d_max_right, max_right.data(), n_vocab * 2, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&h->h_status), sizeof(DevStatus));
+  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&h->h_ustatus), 4 * sizeof(long long));
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&h->d_ustatus), h->h_ustatus, 0);
   for (int k = 0; k <= N_STAGES && e == cudaSuccess; ++k) e = cudaEventCreate(&h->ev[k]);
   if (e != cudaSuccess) {
     const int code = (e == cudaErrorMemoryAllocation) ? TOK_ENOMEM : TOK_ECUDA;
@@ -440,6 +444,7 @@ void tok_free(tok_handle* h) {
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_status) cudaFreeHost(h->h_status);
+  if (h->h_ustatus) cudaFreeHost(h->h_ustatus);
   if (h->h_items) cudaFreeHost(h->h_items);
   for (int k = 0; k <= N_STAGES; ++k)
     if (h->ev[k]) cudaEventDestroy(h->ev[k]);
@@ -478,6 +483,17 @@ int tok_stage_times(tok_handle* h, float* ms, const char** names, int cap) {
 
 namespace {
 
+// The device address of a pinned (page-locked, mapped) host buffer, or
+// nullptr for any other memory.
+void* mapped_device_ptr(const void* p) {
+  cudaPointerAttributes a{};
+  if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // host in, host out; offsets (or nullptr) receive every token's byte offset
 int encode_host(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, int64_t* offsets, uint64_t cap,
                 uint64_t* n_ids) {
@@ -499,6 +515,32 @@ int encode_host(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, 
     if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
   }
   Call c = base_call(h, h->ws.text, len);
+  // pinned output buffers large enough for any result: the emit kernel writes
+  // the ids (and offsets) and the status straight into host memory, and one
+  // synchronisation ends the call
+  int32_t* dir_ids = len && cap >= len ? static_cast<int32_t*>(mapped_device_ptr(ids)) : nullptr;
+  long long* dir_off = dir_ids && offsets ? static_cast<long long*>(mapped_device_ptr(offsets)) : nullptr;
+  if (dir_ids && (!offsets || dir_off)) {
+    c.out = dir_ids;
+    c.out_off = dir_off;
+    c.user_status = h->d_ustatus;
+    rc = run_chain(h, c, s);
+    if (rc) return rc;
+    const cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "encode");
+    collect_times(h);
+    const long long code = h->h_ustatus[0];
+    h->err_off = h->h_ustatus[2];
+    if (code == TOK_EUTF8) {
+      char buf[96];
+      snprintf(buf, sizeof buf, "invalid UTF-8 at byte %lld", (long long)h->err_off);
+      return fail(h, TOK_EUTF8, buf);
+    }
+    if (code == ST_ETIMEOUT) return fail(h, TOK_ETIMEOUT, "device-side wait gave up");
+    if (code != ST_OK) return fail(h, TOK_ECUDA, "device-side internal error");
+    *n_ids = (uint64_t)h->h_ustatus[1];
+    return TOK_OK;
+  }
   c.out = h->d_out;
   c.out_off = offsets ? h->d_off : nullptr;
   rc = run_chain(h, c, s);

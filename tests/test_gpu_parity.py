@@ -144,6 +144,38 @@ def test_token_offsets_device_entry(pkg):
     assert d_off[:st[1]].cpu().tolist() == want_offs
 
 
+def test_pinned_host_buffers(pkg):
+    # pinned output buffers take the direct path (the device writes ids,
+    # offsets and status into host memory); same results as the oracle
+    import ctypes
+    import torch
+    v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
+    L = pkg.lib()
+    for data in (textgen.agentic_session(100_000, 1021).encode(), b"x", b"  \r\n\t 12345 abc"):
+        n = len(data)
+        h_text = torch.frombuffer(bytearray(data), dtype=torch.uint8).pin_memory()
+        h_ids = torch.empty(n, dtype=torch.int32).pin_memory()
+        h_off = torch.empty(n, dtype=torch.int64).pin_memory()
+        got = ctypes.c_uint64()
+        tp = ctypes.cast(h_text.data_ptr(), ctypes.POINTER(ctypes.c_uint8))
+        ip = ctypes.cast(h_ids.data_ptr(), ctypes.POINTER(ctypes.c_int32))
+        op = ctypes.cast(h_off.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+        assert L.tok_encode(tok._h, tp, n, ip, n, ctypes.byref(got)) == 0
+        want_ids, want_offs = encode_with_offsets(data, v, PATTERN_CL100K)
+        assert h_ids[:got.value].tolist() == want_ids
+        assert L.tok_encode_offsets(tok._h, tp, n, ip, op, n, ctypes.byref(got)) == 0
+        assert h_ids[:got.value].tolist() == want_ids and h_off[:got.value].tolist() == want_offs
+    bad = b"abc " * 1000 + b"\xf0\x28\x8c\x28" + b" tail"
+    h_text = torch.frombuffer(bytearray(bad), dtype=torch.uint8).pin_memory()
+    h_ids = torch.empty(len(bad), dtype=torch.int32).pin_memory()
+    got = ctypes.c_uint64()
+    rc = L.tok_encode(tok._h, ctypes.cast(h_text.data_ptr(), ctypes.POINTER(ctypes.c_uint8)), len(bad),
+                      ctypes.cast(h_ids.data_ptr(), ctypes.POINTER(ctypes.c_int32)), len(bad), ctypes.byref(got))
+    with pytest.raises(Utf8Error) as e:
+        encode(bad, v, PATTERN_CL100K)
+    assert rc == pkg.TOK_EUTF8 and L.tok_error_offset(tok._h) == e.value.offset
+
+
 def test_encode_batch_64_sessions(pkg):
     v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
     items = [s.encode() for s in textgen.session_batch(64, 1004)]
