@@ -31,7 +31,7 @@ _NAMES = {0: "TOK_OK", -1: "TOK_EINVAL", -2: "TOK_EUTF8", -3: "TOK_ENOMEM", -4: 
           -6: "TOK_ETIMEOUT", -7: "TOK_EMERGES"}
 
 # every symbol include/tok.h declares
-SYMBOLS = ["tok_load", "tok_encode", "tok_encode_offsets", "tok_encode_batch", "tok_encode_device",
+SYMBOLS = ["tok_load", "tok_encode", "tok_encode_offsets", "tok_repair_append", "tok_encode_batch", "tok_encode_device",
            "tok_encode_offsets_device", "tok_encode_batch_device", "tok_pretokenize", "tok_pretokenize_batch",
            "tok_last_error", "tok_error_offset", "tok_content_hash", "tok_set_timing", "tok_stage_times",
            "tok_launch_count", "tok_free", "tok_pretokenize_device_noalloc"]
@@ -64,6 +64,7 @@ def lib():
                            ctypes.POINTER(P)]
     L.tok_encode.argtypes = [P, U8P, U64, I32P, U64, U64P]
     L.tok_encode_offsets.argtypes = [P, U8P, U64, I32P, I64P, U64, U64P]
+    L.tok_repair_append.argtypes = [P, U8P, U64, U64, I32P, I64P, U64, I32P, I64P, U64, U64P, U64P]
     L.tok_encode_batch.argtypes = [P, ctypes.POINTER(U8P), U64P, U32, I32P, U64, U64P]
     L.tok_encode_device.argtypes = [P, P, U64, P, U64, P, P]
     L.tok_encode_offsets_device.argtypes = [P, P, U64, P, P, U64, P, P]
@@ -84,7 +85,7 @@ def lib():
     L.tok_launch_count.restype = ctypes.c_uint64
     L.tok_free.argtypes = [P]
     L.tok_free.restype = None
-    for fn in ("tok_load", "tok_encode", "tok_encode_offsets", "tok_encode_batch", "tok_encode_device",
+    for fn in ("tok_load", "tok_encode", "tok_encode_offsets", "tok_repair_append", "tok_encode_batch", "tok_encode_device",
                "tok_encode_offsets_device", "tok_encode_batch_device", "tok_pretokenize", "tok_pretokenize_batch",
                "tok_set_timing", "tok_stage_times"):
         getattr(L, fn).restype = ctypes.c_int
@@ -190,6 +191,25 @@ class Tokenizer:
                                                offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(ids),
                                                ctypes.byref(n)))
         return ids[:n.value].copy(), offs[:n.value].copy()
+
+    def repair_append(self, old, old_ids, old_offsets, delta):
+        """Encoding of old + delta from old's ids and token offsets (only the
+        tail from the last certified cut is encoded).  Returns (ids,
+        offsets, reencoded_bytes)."""
+        text = bytes(old) + bytes(delta)
+        arr, p = _u8(text) if text else (None, None)
+        old_ids = np.ascontiguousarray(old_ids, dtype=np.int32)
+        old_offsets = np.ascontiguousarray(old_offsets, dtype=np.int64)
+        cap = max(len(old_ids) + len(delta) + len(old), 1)
+        ids = np.empty(cap, dtype=np.int32)
+        offs = np.empty(cap, dtype=np.int64)
+        n, re = ctypes.c_uint64(), ctypes.c_uint64()
+        self._check(self._L.tok_repair_append(
+            self._h, p, len(old), len(text), old_ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+            old_offsets.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), len(old_ids),
+            ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+            cap, ctypes.byref(n), ctypes.byref(re)))
+        return ids[:n.value].copy(), offs[:n.value].copy(), re.value
 
     def encode_batch(self, items):
         items = [bytes(x) for x in items]

@@ -261,6 +261,69 @@ Call base_call(tok_handle* h, const uint8_t* d_text, uint64_t n) {
   return c;
 }
 
+// ---------------------------------------------------------------------------
+// Session repair after an append (Section 3.3; Appendix A.2's splice theorem).
+// The cut p is the last position inside the old text whose previous code
+// point is a letter or a number and whose own code point has another class.
+// Every alternative of both patterns that consumes letters or numbers matches
+// a maximal run of them, so the match covering p - 1 ends at p whatever
+// follows; the fragments before p depend on the text up to the code point at
+// p, and (no pattern looks behind) the fragments from p on only on the text
+// from p on.  So the old tokens before p stay, and text[p:] is encoded anew.
+
+namespace hostucd {
+#define TOK_UCD_QUAL static const
+#include "ucd_table.inc"
+#undef TOK_UCD_QUAL
+}  // namespace hostucd
+
+uint32_t host_class(uint32_t cp) {
+  if (cp < 128u) {
+    if ((cp | 32u) - 'a' < 26u) return CLS_L;
+    if (cp - '0' < 10u) return CLS_N;
+    if (cp == 32u || cp - 9u < 5u) return CLS_W;
+    return CLS_O;
+  }
+  if (cp > 0x10FFFFu) return CLS_O;
+  const uint32_t blk = hostucd::tok_ucd_stage1[cp >> 8];
+  const uint32_t w = hostucd::tok_ucd_stage2[blk * 16u + ((cp & 255u) >> 4)];
+  return (w >> ((cp & 15u) * 2u)) & 3u;
+}
+
+// class of the code point that starts at byte k of s[0..n) (its sequence is
+// taken as given: the old text of a session has been encoded before)
+uint32_t host_class_at(const uint8_t* s, uint64_t n, uint64_t k) {
+  const uint32_t b = s[k];
+  if (b < 0x80u) return host_class(b);
+  int need = b >= 0xF0u ? 3 : b >= 0xE0u ? 2 : b >= 0xC0u ? 1 : 0;
+  if (!need || k + (uint64_t)need >= n + 1) return CLS_O;
+  uint32_t cp = b & (0x3Fu >> need);
+  for (int i = 1; i <= need; ++i) {
+    if (k + (uint64_t)i >= n) return CLS_O;
+    cp = (cp << 6) | (s[k + i] & 0x3Fu);
+  }
+  return host_class(cp);
+}
+
+// the last certified cut inside old[0..n), or 0; looks back at most `limit` bytes
+uint64_t last_cut(const uint8_t* old, uint64_t n, uint64_t limit) {
+  if (n == 0) return 0;
+  const uint64_t stop = n > limit ? n - limit : 0;
+  uint64_t k = n;  // start of the code point after the previous one
+  long long cur = -1;
+  uint32_t cur_cls = 0;
+  while (k > stop) {
+    uint64_t j = k - 1;  // start of the code point before k
+    while (j > 0 && (old[j] & 0xC0u) == 0x80u && k - j < 4) --j;
+    const uint32_t c = host_class_at(old, n, j);
+    if (cur >= 0 && (c == CLS_L || c == CLS_N) && cur_cls != c) return (uint64_t)cur;
+    cur = (long long)j;
+    cur_cls = c;
+    k = j;
+  }
+  return 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -573,6 +636,37 @@ int tok_encode_offsets(tok_handle* h, const uint8_t* text, uint64_t len, int32_t
                        uint64_t cap, uint64_t* n_ids) {
   if (!offsets) return fail(h, TOK_EINVAL, "offsets is NULL");
   return encode_host(h, text, len, ids, offsets, cap, n_ids);
+}
+
+int tok_repair_append(tok_handle* h, const uint8_t* text, uint64_t old_len, uint64_t len, const int32_t* old_ids,
+                      const int64_t* old_offsets, uint64_t old_n, int32_t* ids, int64_t* offsets, uint64_t cap,
+                      uint64_t* n_ids, uint64_t* reencoded) {
+  if (!h || !n_ids || !ids || !offsets || (len && !text) || old_len > len || (old_n && (!old_ids || !old_offsets)))
+    return fail(h, TOK_EINVAL, "bad argument");
+  *n_ids = 0;
+  if (reencoded) *reencoded = 0;
+  const uint64_t p = last_cut(text, old_len, 1ull << 20);
+  // the old tokens before the cut; the cut must be a token start of them
+  const uint64_t k = (uint64_t)(std::lower_bound(old_offsets, old_offsets + old_n, (int64_t)p) - old_offsets);
+  if (p && (k >= old_n || (uint64_t)old_offsets[k] != p))
+    return fail(h, TOK_EINVAL, "the old token offsets do not belong to this text");
+  if (k > cap) {
+    *n_ids = k;
+    return fail(h, TOK_EBUF, "output buffer too small");
+  }
+  if (ids != old_ids) std::copy(old_ids, old_ids + k, ids);
+  if (offsets != old_offsets) std::copy(old_offsets, old_offsets + k, offsets);
+  uint64_t m = 0;
+  const int rc = encode_host(h, text + p, len - p, ids + k, offsets + k, cap - k, &m);
+  if (rc == TOK_EBUF) *n_ids = k + m;
+  if (rc) {
+    if (rc == TOK_EUTF8) h->err_off += (int64_t)p;
+    return rc;
+  }
+  for (uint64_t i = 0; i < m; ++i) offsets[k + i] += (int64_t)p;
+  *n_ids = k + m;
+  if (reencoded) *reencoded = len - p;
+  return TOK_OK;
 }
 
 int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t* lens, uint32_t n, int32_t* ids,

@@ -96,6 +96,29 @@ int tok_encode(tok_handle* h, const uint8_t* text, uint64_t len,
 int tok_encode_offsets(tok_handle* h, const uint8_t* text, uint64_t len,
                        int32_t* ids, int64_t* offsets, uint64_t cap, uint64_t* n_ids);
 
+/* tok_repair_append -- the encoding of a session after an append, from the
+ * session's previous encoding (Section 3.3: repair instead of a full encode;
+ * Section 3.4: a session keeps ids and byte offsets).
+ * text: host, len bytes = the old text (old_len bytes) followed by the
+ *   appended bytes.  old_ids / old_offsets: host, old_n entries: the ids and
+ *   token byte offsets of the old text as tok_encode_offsets returns them.
+ * The old text is cut at its last position whose previous code point is a
+ * letter or a number and whose own code point has another class (looking
+ * back at most 1 MiB; with no such position the whole text is encoded).  A
+ * fragment starts there whatever follows, so the old tokens before the cut
+ * are kept and only text[cut..len) is encoded (Appendix A.2's splice theorem
+ * with a certified cut).  The result equals tok_encode_offsets(text).
+ * ids / offsets: host, capacity cap; they may be old_ids / old_offsets
+ *   themselves (the kept tokens are then not copied).
+ * *n_ids: number of ids; *reencoded (may be NULL): bytes encoded anew.
+ * Errors: TOK_EINVAL (including old offsets that do not fit the text),
+ *   TOK_EBUF (*n_ids = the required capacity), and those of tok_encode.
+ */
+int tok_repair_append(tok_handle* h, const uint8_t* text, uint64_t old_len, uint64_t len,
+                      const int32_t* old_ids, const int64_t* old_offsets, uint64_t old_n,
+                      int32_t* ids, int64_t* offsets, uint64_t cap, uint64_t* n_ids,
+                      uint64_t* reencoded);
+
 /* tok_encode_batch -- encode n independent texts in one pass (host in, host
  * out).  Item k is texts[k][0..lens[k]); items never interact: every item
  * starts and ends a fragment exactly as a separate tok_encode call would.

@@ -16,6 +16,7 @@ import pytest
 import textgen
 from oracle.bpe import bpe_heap
 from oracle.encode import decode, encode, encode_with_offsets, pretoken_byte_spans
+from oracle.repair import repair_append as oracle_repair_append
 from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2
 from oracle.utf8 import Utf8Error
 from oracle.vocab import Vocab
@@ -174,6 +175,33 @@ def test_pinned_host_buffers(pkg):
     with pytest.raises(Utf8Error) as e:
         encode(bad, v, PATTERN_CL100K)
     assert rc == pkg.TOK_EUTF8 and L.tok_error_offset(tok._h) == e.value.offset
+
+
+def test_repair_append_matches_full_encoding(pkg):
+    # session repair (Section 3.3): appends of agent-session text, of text that
+    # extends the old text's last run (letters, digits, whitespace, CR/LF),
+    # and to an old text without any cut
+    rng = random.Random(17)
+    for name, pat in (("cl100k_session_100k", PATTERN_CL100K), ("gpt2_session_100k", PATTERN_GPT2)):
+        v, tok = pair(pkg, name, pat)
+        s = textgen.agentic_session(400_000, 1031).encode()
+        cases = []
+        for _ in range(6):
+            a = rng.randrange(1000, len(s) - 5000)
+            cases.append((s[:a], s[a:a + rng.randrange(1, 3000)]))
+        cases += [(b"the pipe", b"line"), (b"x = 12345", b"678 + 9"), (b"end  ", b"  \r\n\r\nmore"),
+                  (b"abc", b"def"), ("caf\u00e9".encode(), "\u0301s".encode()), (b"", b"fresh start")]
+        for old, delta in cases:
+            try:
+                old.decode("utf-8"), delta.decode("utf-8")
+            except UnicodeDecodeError:
+                continue
+            oi, oo = tok.encode_with_offsets(old)
+            ids, offs, re = tok.repair_append(old, oi, oo, delta)
+            want = encode_with_offsets(old + delta, v, pat)
+            assert (ids.tolist(), offs.tolist()) == want, (old[-20:], delta[:20])
+            o_ids, o_offs, o_re = oracle_repair_append(old, oi.tolist(), oo.tolist(), delta, v, pat)
+            assert re == o_re
 
 
 def test_encode_batch_64_sessions(pkg):
