@@ -112,7 +112,7 @@ cudaError_t dalloc(T** p, size_t count) {
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
   void* ptrs[] = {w.text,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,    w.sbatch,
-                  w.wq,       w.longq,    w.ctot,     w.cpre,     w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0],
+                  w.wq,       w.longq,    w.ctot,     w.gtot,     w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0],
                   w.e_len[1], w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,     h->d_out,   h->d_off};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -146,7 +146,7 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.wq, cap / (SB_MAX + 1) + nbch + pad));
   chk(dalloc(&w.longq, cap / (B_CAP + 1) + nbch + pad));
   chk(dalloc(&w.ctot, nbch + 2));
-  chk(dalloc(&w.cpre, nbch + 2));
+  chk(dalloc(&w.gtot, nbch / CTOT_GROUP + 2));
   chk(dalloc(&w.st, 1));
   for (int b = 0; b < 2; ++b) {
     chk(dalloc(&w.e_sym[b], cap + pad));

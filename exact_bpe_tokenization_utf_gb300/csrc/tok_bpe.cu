@@ -615,6 +615,7 @@ __global__ void __launch_bounds__(B_THREADS, 10) k_settle(Call c, Workspace ws, 
     s_bbase = nbat ? atomicAdd(&ws.st->sbatch_count, (uint32_t)nbat) : 0u;
     // ids of the settled fragments start the chunk's total; the engines add theirs
     ws.ctot[blockIdx.x] = (uint32_t)(nf - ns - nw - nl);
+    if (nf - ns - nw - nl) atomicAdd(&ws.gtot[blockIdx.x / CTOT_GROUP], (uint32_t)(nf - ns - nw - nl));
   } else if (tid == 32) {
     s_sbase = ns ? atomicAdd(&ws.st->sfrag_count, (unsigned long long)ns) : 0ull;
   } else if (tid == 64) {
@@ -763,6 +764,7 @@ __device__ void cta_fragment(const Call& c, const Workspace& ws, const DevVocab&
   if (tid == 0) {
     ws.fcnt[a] = m;
     atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
+    atomicAdd(&ws.gtot[a / BCHUNK / CTOT_GROUP], (uint32_t)m);
   }
   __syncthreads();
 }
@@ -821,7 +823,10 @@ __device__ void short_batch(const Call& c, const Workspace& ws, const DevVocab& 
     }
   }
   // every fragment of a batch starts in the same 512-byte chunk
-  if (lane == 0) atomicAdd(&ws.ctot[start / BCHUNK], (uint32_t)m);
+  if (lane == 0) {
+    atomicAdd(&ws.ctot[start / BCHUNK], (uint32_t)m);
+    atomicAdd(&ws.gtot[start / BCHUNK / CTOT_GROUP], (uint32_t)m);
+  }
   __syncwarp();
 }
 
@@ -837,57 +842,14 @@ struct EngineSmem {
   uint32_t idx;
   uint32_t nq[3];           // queue sizes: long, 33..B_CAP bytes, short batches
   unsigned long long end;
-  int last;
 };
-
-// Exclusive scan of the 512-byte chunk totals into cpre, and the number of
-// ids; all threads of one CTA.
-__device__ void scan_chunk_totals(const Call& c, const Workspace& ws, unsigned long long* sh64) {
-  const int tid = threadIdx.x, T = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = T >> 5;
-  const long long nch = n_bchunks(c.n);
-  constexpr int PER = 8;
-  unsigned long long carry = 0;
-  for (long long base = 0; base < nch; base += (long long)T * PER) {
-    const long long i0 = base + (long long)tid * PER;
-    uint32_t v[PER];
-    unsigned long long sum = 0;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      v[q] = i0 + q < nch ? ws.ctot[i0 + q] : 0u;
-      sum += v[q];
-    }
-    unsigned long long inc = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
-      if (lane >= off) inc += o;
-    }
-    if (lane == 31) sh64[warp] = inc;
-    __syncthreads();
-    unsigned long long pre = carry, tile = 0;
-    for (int k = 0; k < nw; ++k) {
-      pre += k < warp ? sh64[k] : 0ull;
-      tile += sh64[k];
-    }
-    __syncthreads();
-    pre += inc - sum;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      if (i0 + q < nch) ws.cpre[i0 + q] = pre;
-      pre += v[q];
-    }
-    carry += tile;
-  }
-  if (tid == 0) ws.st->n_ids = carry;
-}
 
 // K3b: a persistent grid.  Longest work first: fragments of more than B_CAP
 // bytes (global-memory engine, taken one at a time), then those of 33..B_CAP
 // bytes (shared-memory engine, fragment i to CTA i mod grid), then batches of
 // short fragments (warp engine, batch b to warp b mod warps, counted from
 // the last CTA so that the CTAs with a 33..B_CAP-byte fragment get fewer).
-// Static assignment keeps thousands of warps off one contended counter.  The
-// last CTA to finish scans the chunk totals for K5.
+// Static assignment keeps thousands of warps off one contended counter.
 __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
   __shared__ EngineSmem S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = B_THREADS;
@@ -934,6 +896,7 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
     if (tid == 0) {
       ws.fcnt[a] = m;
       atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
+      atomicAdd(&ws.gtot[a / BCHUNK / CTOT_GROUP], (uint32_t)m);
     }
     __syncthreads();
   }
@@ -947,15 +910,6 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
   const uint32_t nwarps = gridDim.x * (T / 32);
   const uint32_t gw = (gridDim.x - 1 - blockIdx.x) * (T / 32) + warp;
   for (uint32_t b = gw; b < nbat; b += nwarps) short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
-  // the last CTA to finish scans the chunk totals
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) S.last = atomicAdd(&st->engine_done, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (S.last) {
-    __threadfence();
-    scan_chunk_totals(c, ws, S.scan64);
-  }
 }
 
 void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {

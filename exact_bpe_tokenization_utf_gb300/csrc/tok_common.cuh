@@ -16,9 +16,10 @@
 //                    (shared memory), then warps take short batches (one
 //                    symbol per lane); every sweep merges all certified-safe
 //                    pairs.  Every fragment's id count is added to the total
-//                    of its 512-byte chunk; the last CTA scans the totals.
-//   K5 emit          per chunk: fragment counts -> offsets, copy of the ids
-//                    in text order
+//                    of its 512-byte chunk and of that chunk's group.
+//   K5 emit          per chunk: ids before it (group totals, then chunk
+//                    totals), fragment counts -> offsets, copy of the ids in
+//                    text order
 // Every stage leaves a fragment's ids at the fragment's byte offset in `tok`
 // and their number at the same offset in `fcnt`.
 #pragma once
@@ -37,6 +38,7 @@ constexpr int B_CAP = 256;         // longest fragment of the K3b shared-memory 
 constexpr int S_RANGE = BCHUNK + B_CAP;  // bytes K3 stages: its chunk + the tail of its last fragment
 constexpr int B_EPT = B_CAP / B_THREADS; // engine symbols per thread at most
 constexpr int SB_MAX = 32;         // bytes (symbols) of a warp batch
+constexpr int CTOT_GROUP = 64;     // chunks per group total (K5 sums group totals, then chunk totals)
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
 
@@ -95,7 +97,6 @@ struct DevStatus {
   uint32_t sbatch_count, sbatch_taken;  // warp batches of short fragments
   uint32_t wide_count, wide_taken;      // fragments of 33..B_CAP bytes
   uint32_t long_count, long_taken;      // longer fragments
-  uint32_t engine_done;                 // K3b CTAs finished
   uint32_t emit_done;
   uint32_t pad[4];
 };
@@ -110,7 +111,7 @@ struct Workspace {
   Frag* wq;                 // fragments of 33..B_CAP bytes
   Frag* longq;              // longer fragments (K4)
   uint32_t* ctot;           // ids of the fragments that start in each 512-byte chunk (added up as they finish)
-  unsigned long long* cpre; // ids before each 512-byte chunk (scanned at the end of K3b)
+  uint32_t* gtot;           // the same for each group of CTOT_GROUP chunks
   DevStatus* st;
   // K4 engine storage, indexed by byte position of the fragment
   uint32_t* e_sym[2];

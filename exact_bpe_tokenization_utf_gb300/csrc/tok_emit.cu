@@ -4,9 +4,10 @@
 //
 // Every BPE stage left a fragment's ids and their count at the fragment's byte
 // offset, and added the count to the total of the 512-byte chunk the fragment
-// starts in; the last CTA of K3b scanned the totals (ids before each chunk).
-// K5 copies, one CTA per chunk, the ids of the fragments that start in it,
-// without waiting on another CTA.  On request it also writes every token's
+// starts in and to that of the chunk's group of CTOT_GROUP chunks.  K5 takes,
+// one CTA per chunk, the ids before the chunk as the sum of the group totals
+// before its group and the chunk totals before it in its group, and copies
+// the ids of the fragments that start in it, without waiting on another CTA.  On request it also writes every token's
 // byte offset: a fragment's first token starts at the fragment, each next
 // one where the previous token's bytes end (the session state of Sections
 // 3.1 and 3.4 keeps these offsets).
@@ -61,7 +62,8 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
   __shared__ int foff[BCHUNK];
   __shared__ uint16_t big[BCHUNK];
   __shared__ int scan[B_THREADS / 32];
-  __shared__ int s_item, s_nbig;
+  __shared__ unsigned long long scan64[B_THREADS / 32];
+  __shared__ int s_item, s_nbig, s_last;
   const int tid = threadIdx.x, T = B_THREADS;
   const long long nch = n_bchunks(c.n);
   DevStatus* st = ws.st;
@@ -108,9 +110,14 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
     foff[f] = o;
     o += fcount[f];
   }
-  const unsigned long long base = ws.cpre[chunk];
-  const unsigned long long n_ids = st->n_ids;
-  if (base + (unsigned long long)total > n_ids) {  // the chunk totals disagree with the counts: a bug upstream
+  // ids before this chunk: group totals before its group, chunk totals before it in its group
+  unsigned long long part = 0;
+  const long long grp = chunk / CTOT_GROUP;
+  for (long long i = tid; i < grp; i += T) part += ws.gtot[i];
+  for (long long i = grp * CTOT_GROUP + tid; i < chunk; i += T) part += ws.ctot[i];
+  unsigned long long base = 0;
+  block_excl_sum_t(part, &base, scan64);
+  if ((unsigned long long)total != ws.ctot[chunk]) {  // the counts disagree with the chunk total: a bug upstream
     if (tid == 0) atomicExch(&st->code, ST_EINTERNAL);
     total = 0;
   }
@@ -174,13 +181,22 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
       c.item_off[k] = (long long)base + (a < nf ? foff[a] : total);
     }
   }
-  // the last CTA to finish completes the status
+  // the last CTA to finish completes the status: the number of ids is the
+  // sum of the group totals
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    const uint32_t done = atomicAdd(&st->emit_done, 1u);
-    if (done == (uint32_t)(nch - 1)) {
-      __threadfence();
+    s_last = atomicAdd(&st->emit_done, 1u) == (uint32_t)(nch - 1);
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    unsigned long long all = 0;
+    for (long long i = tid; i <= (nch - 1) / CTOT_GROUP; i += T) all += ws.gtot[i];
+    unsigned long long n_ids = 0;
+    block_excl_sum_t(all, &n_ids, scan64);
+    if (tid == 0) {
+      st->n_ids = n_ids;
       if (c.item_off) {
         for (int k = c.n_items; k >= 0 && c.item[k] >= c.n; --k) c.item_off[k] = (long long)n_ids;
       }
