@@ -8,6 +8,7 @@
 // ("TokTier: exact stateful tokenization for agentic LLM serving", Section
 // 4.3, cuts a request from eight host syncs to two).
 #include <algorithm>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -21,8 +22,8 @@ using namespace tokgb;
 
 namespace {
 
-constexpr int N_STAGES = 4;
-const char* kStageNames[N_STAGES] = {"k_boundaries", "k_settle", "k_bpe_engine", "k_emit"};
+constexpr int N_STAGES = 3;
+const char* kStageNames[N_STAGES] = {"k_boundaries", "k_bpe_engine", "k_emit"};
 
 thread_local std::string g_load_error;
 
@@ -46,6 +47,7 @@ struct tok_handle {
   uint16_t* d_max_right = nullptr;
   WholeEntry* d_whole = nullptr;
   uint8_t* d_vocab_bytes = nullptr;
+  uint64_t vocab_bytes_len = 0;
   uint32_t* d_vocab_off = nullptr;
   uint32_t n_whole = 0;
   uint64_t hash = 0;
@@ -111,9 +113,11 @@ cudaError_t dalloc(T** p, size_t count) {
 
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
-  void* ptrs[] = {w.text,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,    w.sbatch,
-                  w.wq,       w.longq,    w.ctot,     w.gtot,     w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0],
-                  w.e_len[1], w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,     h->d_out,   h->d_off};
+  // (the group totals live in the status allocation)
+  void* ptrs[] = {w.text,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,    w.sbatch,   w.wq,
+                  w.longq,    w.ctot,     w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1],
+                  w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,     w.elast,    w.efirst,   w.eflag,
+                  h->d_out,   h->d_off};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   w = Workspace{};
@@ -146,8 +150,16 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.wq, cap / (SB_MAX + 1) + nbch + pad));
   chk(dalloc(&w.longq, cap / (B_CAP + 1) + nbch + pad));
   chk(dalloc(&w.ctot, nbch + 2));
-  chk(dalloc(&w.gtot, nbch / CTOT_GROUP + 2));
-  chk(dalloc(&w.st, 1));
+  // the status, then the group totals: the part cleared before a call is one range
+  {
+    uint8_t* p = nullptr;
+    chk(dalloc(&p, sizeof(DevStatus) + (nbch / CTOT_GROUP + 2) * sizeof(uint32_t)));
+    w.st = reinterpret_cast<DevStatus*>(p);
+    w.gtot = p ? reinterpret_cast<uint32_t*>(p + sizeof(DevStatus)) : nullptr;
+  }
+  chk(dalloc(&w.elast, nch + 2));
+  chk(dalloc(&w.efirst, nch + 2));
+  chk(dalloc(&w.eflag, nch + 2));
   for (int b = 0; b < 2; ++b) {
     chk(dalloc(&w.e_sym[b], cap + pad));
     chk(dalloc(&w.e_len[b], cap + pad));
@@ -158,6 +170,7 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&h->d_out, cap + pad));
   if (e == cudaSuccess) e = cudaMemset(w.pstart, 0, (cap / 32 + pad) * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(w.st, 0, sizeof(DevStatus));
+  if (e == cudaSuccess) e = cudaMemset(w.eflag, 0, (nch + 2) * sizeof(unsigned long long));
   if (e != cudaSuccess) {
     free_workspace(h);
     cudaGetLastError();
@@ -188,19 +201,32 @@ int ensure_items(tok_handle* h, uint64_t n_items) {
 }
 
 // The epoch of a new call.  The UTF-8 error word is keyed by the low 24 bits
-// of the epoch (err_key): when they wrap, the word is cleared first.
+// of the epoch (err_key), the chunk-edge words by the whole epoch: when the
+// low bits wrap, both are cleared first.
 uint32_t next_epoch(tok_handle* h, cudaStream_t s) {
   uint32_t e = ++h->epoch;
   if (e >= 0x3FFFFFFFu) h->epoch = e = 1;
-  if ((e & 0xFFFFFFu) <= 1u) cudaMemsetAsync(&h->ws.st->err_off, 0, sizeof(unsigned long long), s);
+  if ((e & 0xFFFFFFu) <= 1u) {
+    cudaMemsetAsync(&h->ws.st->err_off, 0, sizeof(unsigned long long), s);
+    cudaMemsetAsync(h->ws.eflag, 0, (h->ws.cap_chunks + 2) * sizeof(unsigned long long), s);
+  }
   h->last_epoch = e;
   return e;
 }
 
+// Clear the status counters and the group totals of a call over n bytes
+// (they follow err_off in one allocation).
+void clear_counters(tok_handle* h, uint64_t n, cudaStream_t s) {
+  constexpr size_t lo = offsetof(DevStatus, code);
+  const size_t ng = (size_t)(n_bchunks((long long)n) / CTOT_GROUP + 1);
+  cudaMemsetAsync(reinterpret_cast<uint8_t*>(h->ws.st) + lo, 0, sizeof(DevStatus) - lo + ng * sizeof(uint32_t), s);
+}
+
 // Enqueue the whole chain for one call.
 int run_chain(tok_handle* h, Call c, cudaStream_t s) {
-  c.pf.p = h->d_table;
-  c.pf.bytes = sizeof(MergeEntry) << h->v.bits;
+  c.pf[0] = Prefetch{h->d_whole, (unsigned long long)sizeof(WholeEntry) << h->v.whole_bits};
+  c.pf[1] = Prefetch{h->d_vocab_bytes, h->vocab_bytes_len};
+  c.pf[2] = Prefetch{h->d_table, (unsigned long long)sizeof(MergeEntry) << h->v.bits};
   c.pattern = h->pattern;
   c.epoch = next_epoch(h, s);
   if (c.n == 0) {
@@ -209,15 +235,15 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
     h->have_times = false;
   } else {
     const bool tm = h->timing;
+    clear_counters(h, c.n, s);
+    c.settle = 1;
     if (tm) cudaEventRecord(h->ev[0], s);
-    launch_boundaries(c, h->ws, s);
+    launch_boundaries(c, h->ws, h->v, s);
     if (tm) cudaEventRecord(h->ev[1], s);
-    launch_settle(c, h->ws, h->v, s);
-    if (tm) cudaEventRecord(h->ev[2], s);
     launch_bpe_engine(c, h->ws, h->v, h->n_sms, s);
-    if (tm) cudaEventRecord(h->ev[3], s);
+    if (tm) cudaEventRecord(h->ev[2], s);
     launch_emit(c, h->ws, h->v, s);
-    if (tm) cudaEventRecord(h->ev[4], s);
+    if (tm) cudaEventRecord(h->ev[3], s);
     h->launches += N_STAGES;
     h->have_times = tm;
   }
@@ -426,12 +452,15 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   std::vector<uint32_t> off32(n_vocab + 1);
   for (uint32_t t = 0; t <= n_vocab; ++t) off32[t] = (uint32_t)(vocab_off[t] - vocab_off[0]);
   for (uint32_t t : whole_tokens) {
-    // entries carry offset and length so a probe needs one more load to compare bytes
+    // entries carry the first 8 bytes, the offset and the length: a probe
+    // of a longer token needs one more load to compare the rest
     if (tok_len[t] > 255 || off32[t] >= (1u << 24)) continue;
-    const unsigned long long hv = bytes_hash(vocab_bytes + vocab_off[t], tok_len[t]);
+    const uint8_t* tb = vocab_bytes + vocab_off[t];
+    const unsigned long long head = bytes_head(tb, tok_len[t]);
+    const unsigned long long hv = bytes_hash(head, tb, tok_len[t]);
     uint32_t slot = (uint32_t)(hv >> (64 - wbits));
     while (whole[slot].offlen != 0) slot = (slot + 1) & ((1u << wbits) - 1u);
-    whole[slot] = WholeEntry{hv, t, (off32[t] << 8) | tok_len[t]};
+    whole[slot] = WholeEntry{head, t, (off32[t] << 8) | tok_len[t]};
   }
 
   tok_handle* h = new tok_handle();
@@ -446,6 +475,7 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   if (e == cudaSuccess) e = dalloc(&h->d_max_right, n_vocab);
   if (e == cudaSuccess) e = dalloc(&h->d_whole, whole.size());
   if (e == cudaSuccess) e = dalloc(&h->d_vocab_bytes, off32[n_vocab] + 16);
+  h->vocab_bytes_len = off32[n_vocab];
   if (e == cudaSuccess) e = dalloc(&h->d_vocab_off, n_vocab + 1);
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_whole, whole.data(), whole.size() * sizeof(WholeEntry), cudaMemcpyHostToDevice);
@@ -770,7 +800,8 @@ static int pretokenize_impl(tok_handle* h, uint64_t len, uint32_t n_items, bool 
   }
   c.pattern = h->pattern;
   c.epoch = next_epoch(h, s);
-  launch_boundaries(c, h->ws, s);
+  clear_counters(h, 0, s);
+  launch_boundaries(c, h->ws, DevVocab{}, s);
   h->launches += 1;
   h->have_times = false;
   cudaError_t e = cudaGetLastError();

@@ -456,187 +456,6 @@ __device__ __forceinline__ int warp_sweeps(WarpBuf& B, const DevVocab& V, DevSta
   return m;
 }
 
-// ---------------------------------------------------------------------------
-// K3: settle the fragments that start in one 512-byte chunk
-//
-// Most fragments need no merge loop: a single byte is its byte token, and a
-// fragment whose bytes equal a token t with BPE(bytes(t)) == [t] (checked for
-// every token at load time) encodes to [t].  Each thread settles at most four
-// fragments with one hash probe each, all its probes issued before it waits
-// on any.  The others are queued for K3b / K4: fragments of at most 32 bytes
-// packed in text order into warp batches of at most 32 bytes, fragments of
-// 33..B_CAP bytes one by one, longer ones (and a last fragment whose end lies
-// beyond the staged bytes) for K4.
-
-constexpr int S_MAX = BCHUNK / 2 + 1;  // fragments of >= 2 bytes that start in a chunk
-
-__global__ void __launch_bounds__(B_THREADS, 10) k_settle(Call c, Workspace ws, DevVocab V) {
-  __shared__ __align__(16) uint8_t text[S_RANGE];
-  __shared__ uint32_t bits[S_RANGE / 32];
-  __shared__ uint16_t fstart[BCHUNK + 1];
-  __shared__ uint16_t slist[S_MAX];     // queued short fragments, in order
-  __shared__ uint16_t soff[S_MAX + 1];  // their byte offsets among themselves, then the total
-  __shared__ uint16_t sbat[S_MAX + 1];  // first slist entry of each warp batch, then ns
-  __shared__ int scan[B_THREADS / 32];
-  __shared__ unsigned long long scan64[B_THREADS / 32];
-  __shared__ long long s_last_end;
-  __shared__ unsigned long long s_sbase;
-  __shared__ uint32_t s_bbase, s_wbase, s_lbase;
-  __shared__ int s_ns, s_nb;
-  const int tid = threadIdx.x, T = B_THREADS;
-  const long long r0 = (long long)blockIdx.x * BCHUNK;
-  const long long r1 = min(r0 + BCHUNK, c.n);
-  const long long lim = min(r0 + S_RANGE, c.n);
-  const int nb = (int)(lim - r0);
-  {  // warm L2 with the merge table for K3b (DRAM is idle in this kernel)
-    const long long lines = (long long)((c.pf.bytes + 127) >> 7);
-    const char* base = static_cast<const char*>(c.pf.p);
-    for (long long g = (long long)blockIdx.x * T + tid; g < lines; g += (long long)gridDim.x * T)
-      asm volatile("prefetch.L2 [%0];" ::"l"(base + (g << 7)));
-  }
-  if (((reinterpret_cast<uintptr_t>(c.text) & 15u) == 0) && nb == S_RANGE) {
-    for (int k = tid; k < S_RANGE / 16; k += T)
-      reinterpret_cast<uint4*>(text)[k] = reinterpret_cast<const uint4*>(c.text + r0)[k];
-  } else {
-    for (int k = tid; k < nb; k += T) text[k] = c.text[r0 + k];
-  }
-  if (tid < S_RANGE / 32) {
-    const long long p = r0 + 32ll * tid;
-    uint32_t v = 0;
-    if (p < lim) {
-      v = ws.pstart[(r0 >> 5) + tid];
-      if (lim - p < 32) v &= (1u << (lim - p)) - 1u;
-    }
-    bits[tid] = v;
-  }
-  __syncthreads();
-  if (tid == 0) {  // end of the last fragment: the first start at or after r1
-    long long e = -1;
-    if (r1 >= c.n) {
-      e = c.n;
-    } else {
-      for (int w = BCHUNK / 32; w < S_RANGE / 32 && e < 0; ++w)
-        if (bits[w]) e = r0 + 32ll * w + (__ffs(bits[w]) - 1);
-      if (e < 0 && lim >= c.n) e = c.n;
-    }
-    s_last_end = e;
-  }
-  // fragment starts in [r0, r1): thread t looks at 4 bit positions
-  const int q0 = tid * 4;
-  const uint32_t mine = (bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
-  int nf = 0;
-  int idx = block_excl_sum(__popc(mine), &nf, scan);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if ((mine >> q) & 1u) fstart[idx++] = (uint16_t)(q0 + q);
-  __syncthreads();
-  // contiguous blocks of at most 4 fragments per thread (nf <= BCHUNK = 4 * T)
-  const int FB = (nf + T - 1) / T;
-  const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
-  int fa[4], fl[4], cls[4];  // start in the chunk, length (-1: unknown), queue (0 settled, 1 short, 2 wide, 3 long)
-  unsigned long long h[4];
-  uint32_t slot[4];
-  uint4 e[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int f = flo + q;
-    fa[q] = 0; fl[q] = 0; cls[q] = 0; h[q] = 0; slot[q] = 0;
-    e[q] = make_uint4(0u, 0u, 0u, 0u);
-    if (f < fhi) {
-      fa[q] = fstart[f];
-      const long long end = (f + 1 < nf) ? r0 + fstart[f + 1] : s_last_end;
-      fl[q] = end < 0 ? -1 : (int)(end - (r0 + fa[q]));
-      if (whole_eligible(V, fl[q])) {
-        h[q] = bytes_hash(text + fa[q], fl[q]);
-        slot[q] = whole_first_slot(V, h[q]);
-        e[q] = __ldg(reinterpret_cast<const uint4*>(V.whole + slot[q]));
-      }
-    }
-  }
-  int scount = 0, sbytes = 0, wcount = 0, lcount = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (flo + q < fhi) {
-      const int L = fl[q];
-      int t = -1;
-      if (L == 1) t = __ldg(V.byte_id + text[fa[q]]);
-      else if (whole_eligible(V, L)) t = whole_lookup_at(V, text + fa[q], L, h[q], slot[q], e[q]);
-      if (t >= 0) {
-        ws.tok[r0 + fa[q]] = t;
-        ws.fcnt[r0 + fa[q]] = 1;
-        cls[q] = 0;
-      } else if (L >= 1 && L <= SB_MAX) {
-        cls[q] = 1;
-        ++scount;
-        sbytes += L;
-      } else if (L > SB_MAX && L <= B_CAP) {
-        cls[q] = 2;
-        ++wcount;
-      } else {
-        cls[q] = 3;
-        ++lcount;
-      }
-    }
-  }
-  // one scan for the four counts, 16 bits each (every count of a chunk is < 2^16)
-  unsigned long long tot4 = 0;
-  const unsigned long long pre4 = block_excl_sum64(
-      (unsigned long long)scount | ((unsigned long long)sbytes << 16) | ((unsigned long long)wcount << 32) |
-          ((unsigned long long)lcount << 48),
-      &tot4, scan64);
-  int si = (int)(pre4 & 0xFFFFu), so = (int)((pre4 >> 16) & 0xFFFFu);
-  int wi = (int)((pre4 >> 32) & 0xFFFFu), li = (int)(pre4 >> 48);
-  const int ns = (int)(tot4 & 0xFFFFu), sb_all = (int)((tot4 >> 16) & 0xFFFFu);
-  const int nw = (int)((tot4 >> 32) & 0xFFFFu), nl = (int)(tot4 >> 48);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (flo + q < fhi && cls[q] == 1) {
-      slist[si] = (uint16_t)(flo + q);
-      soff[si] = (uint16_t)so;
-      ++si;
-      so += fl[q];
-    }
-  }
-  __syncthreads();
-  // queue reservations, one per warp so that they overlap
-  if (tid == 0) {
-    // short fragments: greedy batches of at most SB_MAX bytes, in order
-    soff[ns] = (uint16_t)sb_all;
-    int nbat = 0, k = 0;
-    while (k < ns) {
-      sbat[nbat++] = (uint16_t)k;
-      const int b0 = soff[k];
-      ++k;
-      while (k < ns && soff[k + 1] - b0 <= SB_MAX) ++k;
-    }
-    sbat[nbat] = (uint16_t)ns;
-    s_ns = ns;
-    s_nb = nbat;
-    s_bbase = nbat ? atomicAdd(&ws.st->sbatch_count, (uint32_t)nbat) : 0u;
-    // ids of the settled fragments start the chunk's total; the engines add theirs
-    ws.ctot[blockIdx.x] = (uint32_t)(nf - ns - nw - nl);
-    if (nf - ns - nw - nl) atomicAdd(&ws.gtot[blockIdx.x / CTOT_GROUP], (uint32_t)(nf - ns - nw - nl));
-  } else if (tid == 32) {
-    s_sbase = ns ? atomicAdd(&ws.st->sfrag_count, (unsigned long long)ns) : 0ull;
-  } else if (tid == 64) {
-    s_wbase = nw ? atomicAdd(&ws.st->wide_count, (uint32_t)nw) : 0u;
-  } else if (tid == 96) {
-    s_lbase = nl ? atomicAdd(&ws.st->long_count, (uint32_t)nl) : 0u;
-  }
-  __syncthreads();
-  for (int k = tid; k < s_ns; k += T) {
-    const int f = slist[k];
-    ws.sfrag[s_sbase + k] = ((unsigned long long)(r0 + fstart[f]) << 8) | (unsigned)(soff[k + 1] - soff[k]);
-  }
-  for (int b = tid; b < s_nb; b += T)
-    ws.sbatch[s_bbase + b] = ((s_sbase + sbat[b]) << 5) | (unsigned)(sbat[b + 1] - sbat[b] - 1);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (flo + q >= fhi) continue;
-    if (cls[q] == 2) ws.wq[s_wbase + wi++] = Frag{r0 + fa[q], fl[q]};
-    else if (cls[q] == 3) ws.longq[s_lbase + li++] = Frag{r0 + fa[q], fl[q] > 0 ? fl[q] : -1};
-  }
-}
 
 // ---------------------------------------------------------------------------
 // K3b: queued fragments of at most B_CAP bytes
@@ -854,7 +673,7 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
   __shared__ EngineSmem S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = B_THREADS;
   DevStatus* st = ws.st;
-  if (tid == 0) {  // the queue sizes, loaded together (settle wrote them)
+  if (tid == 0) {  // the queue sizes, loaded together (K2 wrote them)
     S.nq[0] = st->long_count;
     S.nq[1] = st->wide_count;
     S.nq[2] = st->sbatch_count;
@@ -912,9 +731,6 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
   for (uint32_t b = gw; b < nbat; b += nwarps) short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
 }
 
-void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
-  k_settle<<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
-}
 
 void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
   k_bpe_engine<<<n_sms * 16, B_THREADS, 0, s>>>(c, w, v);  // 16 CTAs of 32 registers per SM

@@ -5,12 +5,13 @@
 //   K2 boundaries    per 1 KiB chunk: UTF-8 validation + per-code-point class +
 //                    run decomposition rules -> fragment-start bitmask
 //                    (Section 4.1); the run states at the chunk's edges come
-//                    from the text just beyond them
-//   K3 settle        per 512-byte chunk: every fragment that is one byte, or
-//                    whose bytes are a token that encodes to itself, is
-//                    settled with one probe; the others are queued: those of
-//                    at most 32 bytes packed into warp batches, 33..B_CAP
-//                    bytes one by one, longer ones for K4 (Section 4.2)
+//                    from the text just beyond them.  In encode calls K2 then
+//                    settles every fragment that is one byte, or whose bytes
+//                    are a token that encodes to itself, with one probe, and
+//                    queues the others: those of at most 32 bytes packed into
+//                    warp batches, 33..B_CAP bytes one by one, longer ones
+//                    (Section 4.2).  A fragment across a chunk edge is handled
+//                    by the second of the edge's two CTAs to get there.
 //   K3b bpe_engine   persistent: CTAs take fragments longer than B_CAP bytes
 //                    (arrays in global memory), then 33..B_CAP-byte fragments
 //                    (shared memory), then warps take short batches (one
@@ -29,13 +30,12 @@
 namespace tokgb {
 
 constexpr int CHUNK = 1024;        // bytes per chunk (every per-chunk kernel)
-constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K1 / K2
+constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K2
 constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
-constexpr int BCHUNK = 512;        // bytes per settle / emit CTA (K3, K5)
-constexpr int B_THREADS = 128;     // K3, K3b, K5
-constexpr int B_CAP = 256;         // longest fragment of the K3b shared-memory engine; longer ones go to K4
-constexpr int S_RANGE = BCHUNK + B_CAP;  // bytes K3 stages: its chunk + the tail of its last fragment
+constexpr int BCHUNK = 512;        // bytes per chunk total and per emit CTA (K5)
+constexpr int B_THREADS = 128;     // K3b, K5
+constexpr int B_CAP = 256;         // longest fragment of the K3b shared-memory engine; longer ones use global memory
 constexpr int B_EPT = B_CAP / B_THREADS; // engine symbols per thread at most
 constexpr int SB_MAX = 32;         // bytes (symbols) of a warp batch
 constexpr int CTOT_GROUP = 64;     // chunks per group total (K5 sums group totals, then chunk totals)
@@ -58,10 +58,12 @@ struct __align__(16) MergeEntry {
 // whole-token table entry: a token whose own bytes encode to itself, keyed by
 // a hash of those bytes; offlen = byte offset of the token << 8 | length
 // (length 2..255), offlen == 0 marks an empty slot
+// a token that encodes to itself: its first bytes in the entry, so that a
+// probe of a fragment of at most 8 bytes needs no second load
 struct __align__(16) WholeEntry {
-  unsigned long long hash;
+  unsigned long long head;  // first min(len, 8) bytes, little-endian, zero above
   uint32_t token;
-  uint32_t offlen;
+  uint32_t offlen;          // byte offset in the token bytes << 8 | len; 0: empty slot
 };
 
 struct DevVocab {
@@ -89,17 +91,20 @@ struct Frag {
 
 // device-side per-call status and work counters
 struct DevStatus {
-  int32_t code;
-  uint32_t epoch;
+  // kept across calls
   unsigned long long err_off;   // first malformed UTF-8 byte of the latest call that had one: err_key
+  // cleared before every call, together with the group totals that follow
+  // the status in its allocation (one memset)
+  int32_t code;
+  uint32_t emit_done;              // K5 CTAs finished
   unsigned long long n_ids;
   unsigned long long sfrag_count;  // short fragments queued
   uint32_t sbatch_count, sbatch_taken;  // warp batches of short fragments
   uint32_t wide_count, wide_taken;      // fragments of 33..B_CAP bytes
   uint32_t long_count, long_taken;      // longer fragments
-  uint32_t emit_done;
-  uint32_t pad[4];
+  uint32_t pad[2];
 };
+static_assert(sizeof(DevStatus) % 16 == 0, "the group totals follow the status");
 
 struct Workspace {
   uint8_t* text;            // device copy of host input (host entry points)
@@ -107,13 +112,16 @@ struct Workspace {
   int32_t* tok;             // a fragment's ids, at the fragment's byte offset
   int32_t* fcnt;            // a fragment's number of ids, at its byte offset
   unsigned long long* sfrag;   // short fragments: start << 8 | length, in batch order
-  unsigned long long* sbatch;  // warp batches: first sfrag index << 4 | (fragments - 1)
+  unsigned long long* sbatch;  // warp batches: first sfrag index << 5 | (fragments - 1)
   Frag* wq;                 // fragments of 33..B_CAP bytes
-  Frag* longq;              // longer fragments (K4)
+  Frag* longq;              // longer fragments (K3b, global-memory engine)
+  long long* elast;         // per 1 KiB chunk: its last fragment start, or -1 (the chunk's edge to the next)
+  long long* efirst;        // per 1 KiB chunk edge: the first fragment start of the next chunk, or -1
+  unsigned long long* eflag;  // per edge: the call's epoch << 2 | arrivals (1, 2), see k_boundaries
   uint32_t* ctot;           // ids of the fragments that start in each 512-byte chunk (added up as they finish)
   uint32_t* gtot;           // the same for each group of CTOT_GROUP chunks
   DevStatus* st;
-  // K4 engine storage, indexed by byte position of the fragment
+  // global-memory engine storage, indexed by byte position of the fragment
   uint32_t* e_sym[2];
   uint16_t* e_len[2];
   unsigned long long* e_kr[2];
@@ -123,7 +131,8 @@ struct Workspace {
   uint64_t cap_chunks;
 };
 
-// device range K3 prefetches into L2 for K3b (the merge table)
+// a device range K2 prefetches into L2 (the vocabulary tables the probes
+// and the BPE engine read)
 struct Prefetch {
   const void* p;
   unsigned long long bytes;
@@ -140,7 +149,8 @@ struct Call {
   long long* out_off;         // device: byte offset of every id's token (nullptr: not wanted)
   long long* item_off;        // device, n_items + 1 (batch) or nullptr
   long long* user_status;     // device int64[4] or nullptr
-  Prefetch pf;
+  int settle;                 // K2 also settles fragments and fills the queues (encode calls)
+  Prefetch pf[3];             // whole-token table, token bytes, merge table
 };
 
 // The first malformed UTF-8 byte of a call, as one word that atomicMax keeps
@@ -162,10 +172,18 @@ __host__ __device__ inline uint32_t merge_slot(unsigned long long key, uint32_t 
   return (uint32_t)((key * 0x9E3779B97F4A7C15ull) >> (64 - bits));
 }
 
-// 64-bit hash of a byte string (FNV-1a, then the splitmix64 finaliser)
-__host__ __device__ inline unsigned long long bytes_hash(const uint8_t* s, int len) {
-  unsigned long long h = 1469598103934665603ull;
-  for (int i = 0; i < len; ++i) {
+// first min(len, 8) bytes of s, little-endian, zero above
+__host__ __device__ inline unsigned long long bytes_head(const uint8_t* s, int len) {
+  unsigned long long v = 0;
+  for (int i = 0; i < len && i < 8; ++i) v |= (unsigned long long)s[i] << (8 * i);
+  return v;
+}
+
+// 64-bit hash of a byte string from its head (bytes_head), its length and
+// the bytes after the first 8 (FNV-1a steps, then the splitmix64 finaliser)
+__host__ __device__ inline unsigned long long bytes_hash(unsigned long long head, const uint8_t* s, int len) {
+  unsigned long long h = head ^ (0x9E3779B97F4A7C15ull * (unsigned long long)len);
+  for (int i = 8; i < len; ++i) {
     h ^= s[i];
     h *= 1099511628211ull;
   }
@@ -196,9 +214,10 @@ __device__ __forceinline__ unsigned long long merge_lookup(const DevVocab& v, ui
 }
 
 // Token whose bytes equal s[0..len) and whose own bytes encode to itself,
-// or -1.  The hash only selects candidates; the bytes are compared.  Split in
-// parts so that a thread can issue the first probes of several strings before
-// it waits for any: whole_first_slot gives the first slot of a hash,
+// or -1.  The hash only selects the first slot; the length and the first 8
+// bytes are compared in the entry, the rest against the token bytes.  Split
+// in parts so that a thread can issue the first probes of several strings
+// before it waits for any: whole_first_slot gives the first slot of a hash,
 // whole_lookup_at finishes from the loaded first entry.
 __device__ __forceinline__ bool whole_eligible(const DevVocab& v, int len) {
   return len >= 2 && len <= 255 && len <= (int)v.max_tok_len;
@@ -208,16 +227,17 @@ __device__ __forceinline__ uint32_t whole_first_slot(const DevVocab& v, unsigned
   return (uint32_t)(h >> (64 - v.whole_bits));
 }
 
-__device__ __forceinline__ int whole_lookup_at(const DevVocab& v, const uint8_t* s, int len, unsigned long long h,
-                                               uint32_t slot, uint4 e) {
+__device__ __forceinline__ int whole_lookup_at(const DevVocab& v, const uint8_t* s, int len,
+                                               unsigned long long head, uint32_t slot, uint4 e) {
   const uint32_t mask = (1u << v.whole_bits) - 1u;
   for (uint32_t probe = 0; probe <= mask; ++probe) {
     if (probe) e = __ldg(reinterpret_cast<const uint4*>(v.whole + slot));
     if (e.w == 0u) return -1;
-    if ((e.w & 255u) == (uint32_t)len && (((unsigned long long)e.y << 32) | e.x) == h) {
+    if ((e.w & 255u) == (uint32_t)len && (((unsigned long long)e.y << 32) | e.x) == head) {
       const uint8_t* t = v.vocab_bytes + (e.w >> 8);
       bool eq = true;
-      for (int i = 0; i < len && eq; ++i) eq = __ldg(t + i) == s[i];
+#pragma unroll 1
+      for (int i = 8; i < len; ++i) eq &= __ldg(t + i) == s[i];
       if (eq) return (int)e.z;
     }
     slot = (slot + 1u) & mask;
@@ -227,9 +247,9 @@ __device__ __forceinline__ int whole_lookup_at(const DevVocab& v, const uint8_t*
 
 __device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s, int len) {
   if (!whole_eligible(v, len)) return -1;
-  const unsigned long long h = bytes_hash(s, len);
-  const uint32_t slot = whole_first_slot(v, h);
-  return whole_lookup_at(v, s, len, h, slot, __ldg(reinterpret_cast<const uint4*>(v.whole + slot)));
+  const unsigned long long head = bytes_head(s, len);
+  const uint32_t slot = whole_first_slot(v, bytes_hash(head, s, len));
+  return whole_lookup_at(v, s, len, head, slot, __ldg(reinterpret_cast<const uint4*>(v.whole + slot)));
 }
 
 __device__ __forceinline__ uint32_t kr_rank(unsigned long long kr) { return (uint32_t)(kr >> 32); }
@@ -265,8 +285,7 @@ __device__ __forceinline__ int utf8_decode(const uint8_t* s, int avail, uint32_t
 #endif
 
 // host-side launchers (defined in the kernel translation units)
-void launch_boundaries(const Call& c, const Workspace& w, cudaStream_t s);
-void launch_settle(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
+void launch_boundaries(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
 void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s);
 void launch_emit(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s);
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s);

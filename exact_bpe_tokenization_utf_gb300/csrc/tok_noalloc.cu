@@ -74,7 +74,7 @@ extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_t
   c.pattern = pattern_id;
   c.epoch = epoch;
   if (len) {
-    launch_boundaries(c, w, s);
+    launch_boundaries(c, w, DevVocab{}, s);
     k_noalloc_status<<<1, 1, 0, s>>>(scratch, epoch, reinterpret_cast<long long*>(d_status));
   } else {
     const long long ok[2] = {TOK_OK, -1};
