@@ -106,6 +106,9 @@ uint64_t fnv1a(uint64_t h, const void* p, size_t n) {
   return h;
 }
 
+// group totals held for a workspace of nbch 512-byte chunks
+size_t gtot_cap(uint64_t nbch) { return (size_t)(nbch / CTOT_GROUP + 2); }
+
 template <class T>
 cudaError_t dalloc(T** p, size_t count) {
   return cudaMalloc(reinterpret_cast<void**>(p), std::max<size_t>(count, 1) * sizeof(T));
@@ -114,9 +117,9 @@ cudaError_t dalloc(T** p, size_t count) {
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
   // (the group totals live in the status allocation)
-  void* ptrs[] = {w.text,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,    w.sbatch,   w.wq,
-                  w.longq,    w.ctot,     w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0], w.e_len[1],
-                  w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,     w.elast,    w.efirst,   w.eflag,
+  void* ptrs[] = {w.text,     w.pstart,   w.tok,      w.fcnt,     w.sfrag,  w.sbatch,
+                  w.wq,       w.longq,    w.st,       w.e_sym[0], w.e_sym[1], w.e_len[0],
+                  w.e_len[1], w.e_kr[0],  w.e_kr[1],  w.e_fl,     w.e_rs,   w.edge,
                   h->d_out,   h->d_off};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -127,6 +130,7 @@ void free_workspace(tok_handle* h) {
 
 // Grow the workspace to hold n bytes (no-op when it already does).
 int ensure_workspace(tok_handle* h, uint64_t n) {
+  if (n > MAX_TEXT_BYTES) return fail(h, TOK_EINVAL, "text longer than 2^34 - 2 bytes");
   if (h->ws.st && n <= h->ws.cap_bytes) return TOK_OK;
   uint64_t cap = std::max<uint64_t>(n + n / 4, 1 << 16);
   cap = (cap + CHUNK - 1) / CHUNK * CHUNK;
@@ -149,17 +153,17 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&w.sbatch, cap / 2 + nbch + pad));
   chk(dalloc(&w.wq, cap / (SB_MAX + 1) + nbch + pad));
   chk(dalloc(&w.longq, cap / (B_CAP + 1) + nbch + pad));
-  chk(dalloc(&w.ctot, nbch + 2));
-  // the status, then the group totals: the part cleared before a call is one range
+  // the status, the group totals, the chunk totals (the group and chunk
+  // totals live in the status allocation): the part cleared before a call is
+  // one range
   {
     uint8_t* p = nullptr;
-    chk(dalloc(&p, sizeof(DevStatus) + (nbch / CTOT_GROUP + 2) * sizeof(uint32_t)));
+    chk(dalloc(&p, sizeof(DevStatus) + (gtot_cap(nbch) + nbch + 2) * sizeof(uint32_t)));
     w.st = reinterpret_cast<DevStatus*>(p);
     w.gtot = p ? reinterpret_cast<uint32_t*>(p + sizeof(DevStatus)) : nullptr;
+    w.ctot = p ? w.gtot + gtot_cap(nbch) : nullptr;
   }
-  chk(dalloc(&w.elast, nch + 2));
-  chk(dalloc(&w.efirst, nch + 2));
-  chk(dalloc(&w.eflag, nch + 2));
+  chk(dalloc(&w.edge, nch + 2));
   for (int b = 0; b < 2; ++b) {
     chk(dalloc(&w.e_sym[b], cap + pad));
     chk(dalloc(&w.e_len[b], cap + pad));
@@ -170,7 +174,7 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   chk(dalloc(&h->d_out, cap + pad));
   if (e == cudaSuccess) e = cudaMemset(w.pstart, 0, (cap / 32 + pad) * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(w.st, 0, sizeof(DevStatus));
-  if (e == cudaSuccess) e = cudaMemset(w.eflag, 0, (nch + 2) * sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(w.edge, 0, (nch + 2) * sizeof(unsigned long long));
   if (e != cudaSuccess) {
     free_workspace(h);
     cudaGetLastError();
@@ -208,18 +212,18 @@ uint32_t next_epoch(tok_handle* h, cudaStream_t s) {
   if (e >= 0x3FFFFFFFu) h->epoch = e = 1;
   if ((e & 0xFFFFFFu) <= 1u) {
     cudaMemsetAsync(&h->ws.st->err_off, 0, sizeof(unsigned long long), s);
-    cudaMemsetAsync(h->ws.eflag, 0, (h->ws.cap_chunks + 2) * sizeof(unsigned long long), s);
+    cudaMemsetAsync(h->ws.edge, 0, (h->ws.cap_chunks + 2) * sizeof(unsigned long long), s);
   }
   h->last_epoch = e;
   return e;
 }
 
-// Clear the status counters and the group totals of a call over n bytes
-// (they follow err_off in one allocation).
+// Clear the status counters, the group totals and the chunk totals of a
+// call over n bytes (they follow err_off in one allocation).
 void clear_counters(tok_handle* h, uint64_t n, cudaStream_t s) {
   constexpr size_t lo = offsetof(DevStatus, code);
-  const size_t ng = (size_t)(n_bchunks((long long)n) / CTOT_GROUP + 1);
-  cudaMemsetAsync(reinterpret_cast<uint8_t*>(h->ws.st) + lo, 0, sizeof(DevStatus) - lo + ng * sizeof(uint32_t), s);
+  const size_t nt = gtot_cap(h->ws.cap_bytes / BCHUNK) + (size_t)n_bchunks((long long)n);
+  cudaMemsetAsync(reinterpret_cast<uint8_t*>(h->ws.st) + lo, 0, sizeof(DevStatus) - lo + nt * sizeof(uint32_t), s);
 }
 
 // Enqueue the whole chain for one call.

@@ -38,6 +38,7 @@ constexpr int B_THREADS = 128;     // K3b, K5
 constexpr int B_CAP = 256;         // longest fragment of the K3b shared-memory engine; longer ones use global memory
 constexpr int B_EPT = B_CAP / B_THREADS; // engine symbols per thread at most
 constexpr int SB_MAX = 32;         // bytes (symbols) of a warp batch
+constexpr unsigned long long MAX_TEXT_BYTES = (1ull << 34) - 2;  // chunk-edge words hold positions + 1 in 34 bits
 constexpr int CTOT_GROUP = 64;     // chunks per group total (K5 sums group totals, then chunk totals)
 constexpr uint32_t NO_RANK = 0xFFFFFFFFu;
 constexpr unsigned long long EMPTY_KEY = ~0ull;
@@ -115,9 +116,7 @@ struct Workspace {
   unsigned long long* sbatch;  // warp batches: first sfrag index << 5 | (fragments - 1)
   Frag* wq;                 // fragments of 33..B_CAP bytes
   Frag* longq;              // longer fragments (K3b, global-memory engine)
-  long long* elast;         // per 1 KiB chunk: its last fragment start, or -1 (the chunk's edge to the next)
-  long long* efirst;        // per 1 KiB chunk edge: the first fragment start of the next chunk, or -1
-  unsigned long long* eflag;  // per edge: the call's epoch << 2 | arrivals (1, 2), see k_boundaries
+  unsigned long long* edge; // per 1 KiB chunk edge: edge_word of the first CTA there (k_boundaries)
   uint32_t* ctot;           // ids of the fragments that start in each 512-byte chunk (added up as they finish)
   uint32_t* gtot;           // the same for each group of CTOT_GROUP chunks
   DevStatus* st;

@@ -23,6 +23,8 @@
  *   - The library copies everything tok_load is given; all other buffers are
  *     borrowed for the duration of the call only.
  *   - Outputs are undefined when a call fails; tok_last_error() says why.
+ *   - A text (or a packed batch) is at most 2^34 - 2 bytes; longer ones are
+ *     refused with TOK_EINVAL.
  */
 #ifndef TOK_H
 #define TOK_H

@@ -87,6 +87,42 @@ def test_pretokenize_runs_across_chunks(pkg, pattern):
         assert g == oracle_starts(p, pattern)
 
 
+def _runs_at_chunk_edges(kinds, lengths, offsets, chunk=1024):
+    """One text in which each run (kind * length) is placed so that a chunk
+    edge falls at each offset from the run's start (before it, inside it,
+    just after it); filler of letters and punctuation between runs."""
+    out = bytearray()
+    filler = b"ab.c,"
+    for kind in kinds:
+        for k in lengths:
+            run = kind * k
+            for d in offsets:
+                # pad so that the run starts d bytes before an edge
+                target = (-d) % chunk
+                pad = (target - len(out)) % chunk
+                if pad < 2:
+                    pad += chunk
+                out += (filler * (pad // len(filler) + 1))[:pad - 1] + b"."
+                out += run
+    out += b"Z"
+    return bytes(out)
+
+
+@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+def test_runs_at_every_offset_of_a_chunk_edge(pkg, pattern):
+    # the run states at a chunk's edges come from the window when a run ends
+    # within it and from the text beyond it otherwise: runs of CR/LF, digits,
+    # spaces, mixed whitespace and apostrophes around the window's reach
+    tok = pkg.Tokenizer.from_merges([], pattern)
+    kinds = [b"\r\n", b"7", b" ", b"\t\n ", "\u0663".encode(), b"'s"]
+    text = _runs_at_chunk_edges(kinds, [1, 2, 5, 11, 12, 13, 14, 17], range(-3, 20))
+    assert list(tok.pretokenize(text)) == oracle_starts(text, pattern)
+    name = "gpt2_session_100k" if pattern == PATTERN_GPT2 else "cl100k_session_100k"
+    v, tk = pair(pkg, name, pattern)
+    small = _runs_at_chunk_edges(kinds, [1, 6, 13, 17], range(-2, 18, 3))
+    assert tk.encode(small).tolist() == encode(small, v, pattern)
+
+
 # --- whole encode at full size -------------------------------------------
 
 def test_encode_code_16k_1k_merges(pkg):
