@@ -55,12 +55,14 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
 
 // K5: the ids of the fragments that start in one 512-byte chunk
 template <bool OFFS>
-__global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVocab V) {
+__global__ void __launch_bounds__(B_THREADS, 16) k_emit(Call c, Workspace ws, DevVocab V) {
   __shared__ uint32_t bits[BCHUNK / 32];
   __shared__ uint16_t fstart[BCHUNK];
   __shared__ int fcount[BCHUNK];
   __shared__ int foff[BCHUNK];
   __shared__ uint16_t big[BCHUNK];
+  __shared__ __align__(16) int cnt[BCHUNK];  // fcnt of every byte of the chunk (meaningful at fragment starts)
+  __shared__ __align__(16) int tk[BCHUNK];   // tok of every byte of the chunk
   __shared__ int scan[B_THREADS / 32];
   __shared__ unsigned long long scan64[B_THREADS / 32];
   __shared__ int s_item, s_nbig, s_last;
@@ -71,6 +73,19 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
   const long long r0 = chunk * BCHUNK;
   const long long r1 = min(r0 + BCHUNK, c.n);
   if (tid == 0) s_nbig = 0;
+  // every load this CTA needs, issued together: the bitmask, the counts and
+  // ids of all the chunk's bytes (positions past the text end, or that start
+  // no fragment, are read but not used; the workspace holds whole chunks),
+  // and the totals before the chunk (group totals before its group, chunk
+  // totals before it in its group)
+  static_assert(BCHUNK == 4 * B_THREADS, "one int4 of counts and ids per thread");
+  const int4 cnt4 = reinterpret_cast<const int4*>(ws.fcnt + r0)[tid];
+  const int4 tk4 = reinterpret_cast<const int4*>(ws.tok + r0)[tid];
+  unsigned long long part = 0;
+  const long long grp = chunk / CTOT_GROUP;
+  for (long long i = tid; i < grp; i += T) part += ws.gtot[i];
+  for (long long i = grp * CTOT_GROUP + tid; i < chunk; i += T) part += ws.ctot[i];
+  const uint32_t my_total = ws.ctot[chunk];
   if (tid < BCHUNK / 32) {
     const long long p = r0 + 32ll * tid;
     uint32_t v = 0;
@@ -80,6 +95,8 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
     }
     bits[tid] = v;
   }
+  reinterpret_cast<int4*>(cnt)[tid] = cnt4;
+  reinterpret_cast<int4*>(tk)[tid] = tk4;
   __syncthreads();
   // the fragments that start in this chunk, and their id counts
   const int q0 = tid * 4;
@@ -96,7 +113,7 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
   for (int f = flo; f < fhi; ++f) {
     // a fragment has between 1 and (bytes to the text end) ids; anything else
     // would be a bug upstream, reported instead of written out of bounds
-    int k = ws.fcnt[r0 + fstart[f]];
+    int k = cnt[fstart[f]];
     if (k < 1 || k > c.n - (r0 + fstart[f])) {
       atomicExch(&st->code, ST_EINTERNAL);
       k = 0;
@@ -110,14 +127,10 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
     foff[f] = o;
     o += fcount[f];
   }
-  // ids before this chunk: group totals before its group, chunk totals before it in its group
-  unsigned long long part = 0;
-  const long long grp = chunk / CTOT_GROUP;
-  for (long long i = tid; i < grp; i += T) part += ws.gtot[i];
-  for (long long i = grp * CTOT_GROUP + tid; i < chunk; i += T) part += ws.ctot[i];
+  // ids before this chunk
   unsigned long long base = 0;
   block_excl_sum_t(part, &base, scan64);
-  if ((unsigned long long)total != ws.ctot[chunk]) {  // the counts disagree with the chunk total: a bug upstream
+  if ((uint32_t)total != my_total) {  // the counts disagree with the chunk total: a bug upstream
     if (tid == 0) atomicExch(&st->code, ST_EINTERNAL);
     total = 0;
   }
@@ -128,12 +141,14 @@ __global__ void __launch_bounds__(B_THREADS) k_emit(Call c, Workspace ws, DevVoc
       const int k = fcount[f];
       const long long a = r0 + fstart[f];
       if (k <= 8) {
-        for (int j = 0; j < k; ++j) c.out[base + foff[f] + j] = ws.tok[a + j];
+        // ids from the staged copy while they lie in the chunk
+        const int a0 = fstart[f];
+        for (int j = 0; j < k; ++j) c.out[base + foff[f] + j] = a0 + j < BCHUNK ? tk[a0 + j] : ws.tok[a + j];
         if (OFFS) {
           long long off = a;
           for (int j = 0; j < k; ++j) {
             c.out_off[base + foff[f] + j] = off;
-            off += __ldg(V.tok_len + ws.tok[a + j]);
+            off += __ldg(V.tok_len + (a0 + j < BCHUNK ? tk[a0 + j] : ws.tok[a + j]));
           }
         }
       } else {
