@@ -284,6 +284,7 @@ int read_status(tok_handle* h, cudaStream_t s) {
 Call base_call(tok_handle* h, const uint8_t* d_text, uint64_t n) {
   Call c{};
   c.text = d_text;
+  c.src = d_text;
   c.n = (long long)n;
   c.item = nullptr;
   c.n_items = 1;
@@ -607,11 +608,15 @@ int encode_host(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, 
     }
   }
   cudaStream_t s = h->stream;
-  if (len) {
+  // a pinned input is read by K2 in place (it also fills the device copy the
+  // later stages read); any other is copied first
+  const uint8_t* src = len ? static_cast<const uint8_t*>(mapped_device_ptr(text)) : nullptr;
+  if (len && !src) {
     const cudaError_t e = cudaMemcpyAsync(h->ws.text, text, len, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "input copy");
   }
   Call c = base_call(h, h->ws.text, len);
+  if (src) c.src = src;
   // pinned output buffers large enough for any result: the emit kernel writes
   // the ids (and offsets) and the status straight into host memory, and one
   // synchronisation ends the call

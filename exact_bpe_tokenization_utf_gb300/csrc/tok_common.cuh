@@ -138,7 +138,9 @@ struct Prefetch {
 };
 
 struct Call {
-  const uint8_t* text;        // device
+  const uint8_t* text;        // device: the text the BPE stages and the emit read
+  const uint8_t* src;         // where K2 reads the text: `text` itself, or a pinned host buffer's
+                              // device address, from which K2 also fills `text` (its own chunk)
   long long n;                // bytes
   const long long* item;      // device item starts, n_items + 1 entries
   int n_items;

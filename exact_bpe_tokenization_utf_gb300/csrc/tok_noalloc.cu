@@ -68,6 +68,7 @@ extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_t
   w.pstart = d_start_bits;
   Call c{};
   c.text = d_text;
+  c.src = d_text;
   c.n = (long long)len;
   c.item = nullptr;
   c.n_items = 1;

@@ -182,13 +182,18 @@ def test_token_offsets_device_entry(pkg):
 
 
 def test_pinned_host_buffers(pkg):
-    # pinned output buffers take the direct path (the device writes ids,
-    # offsets and status into host memory); same results as the oracle
+    # pinned buffers take the direct path (the boundary kernel reads the text
+    # in place; the device writes ids, offsets and status into host memory);
+    # same results as the oracle
     import ctypes
     import torch
     v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
     L = pkg.lib()
-    for data in (textgen.agentic_session(100_000, 1021).encode(), b"x", b"  \r\n\t 12345 abc"):
+    # a pinned input is read in place by the boundary kernel: also runs that
+    # reach past a chunk's halo (their edge states read the host buffer) and a
+    # length that ends inside a chunk
+    runs = _runs_at_chunk_edges([b"\r\n", b"7", b" "], [13, 17, 40], range(-2, 19, 4))[:150_001]
+    for data in (textgen.agentic_session(100_000, 1021).encode(), b"x", b"  \r\n\t 12345 abc", runs):
         n = len(data)
         h_text = torch.frombuffer(bytearray(data), dtype=torch.uint8).pin_memory()
         h_ids = torch.empty(n, dtype=torch.int32).pin_memory()
