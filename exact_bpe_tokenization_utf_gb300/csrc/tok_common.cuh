@@ -30,7 +30,7 @@
 namespace tokgb {
 
 constexpr int CHUNK = 1024;        // bytes per chunk (every per-chunk kernel)
-constexpr int CHUNK_THREADS = 256; // 4 bytes per thread in K2
+constexpr int CHUNK_THREADS = 128; // 8 bytes per thread in K2
 constexpr int BYTES_PER_THREAD = CHUNK / CHUNK_THREADS;
 constexpr int HALO = 16;           // look-behind / look-ahead bytes around a chunk
 constexpr int BCHUNK = 512;        // bytes per chunk total and per emit CTA (K5)
