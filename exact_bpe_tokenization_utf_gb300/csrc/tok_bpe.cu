@@ -283,6 +283,137 @@ struct CtaBatch {           // one batch of the CTA engine
   uint8_t fl[B_CAP];        // pair merges this sweep
 };
 
+// ---------------------------------------------------------------------------
+// K3b: queued fragments of at most B_CAP bytes
+//
+// A persistent grid.  First every CTA takes fragments of 33..B_CAP bytes one
+// at a time through the shared-memory engine; then every warp takes batches
+// of short fragments through the warp engine.  Both write a fragment's ids at
+// its byte offset in `tok` and their number at the same offset in `fcnt`.
+
+// One fragment of M (33..B_CAP) bytes at byte offset a, all threads of the CTA.
+__device__ void cta_fragment(const Call& c, const Workspace& ws, const DevVocab& V, long long a, int M, CtaBatch& C,
+                             int* scan, unsigned long long* scan64, int* sflags) {
+  const int tid = threadIdx.x, T = B_THREADS, lane = tid & 31;
+  for (int i = tid; i < M; i += T) {
+    const int32_t id = __ldg(V.byte_id + c.text[a + i]);
+    C.sym[i] = (uint32_t)id;
+    C.len[i] = (uint16_t)(1u | (i == 0 ? FRAG_START : 0u));
+    C.ml[i] = __ldg(V.max_left + id);
+    C.mr[i] = __ldg(V.max_right + id);
+  }
+  if (tid == 0) *sflags = 0;
+  __syncthreads();
+  for (int i = tid; i < M; i += T) C.kr[i] = (i + 1 >= M) ? KR_WALL : merge_lookup(V, C.sym[i], C.sym[i + 1]);
+  __syncthreads();
+  int m = M;
+  for (int sweep = 0; sweep <= M; ++sweep) {
+    const int B = (m + T - 1) / T;
+    const int lo = min(tid * B, m), hi = min(lo + B, m);
+    // A: any mergeable pair left?  any overlapping equal-rank pairs?
+    int fl2 = 0;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t k = kr_rank(C.kr[i]);
+      if (mergeable(k)) {
+        fl2 |= 1;
+        if (i > 0 && kr_rank(C.kr[i - 1]) == k) fl2 |= 2;
+      }
+    }
+    fl2 = __reduce_or_sync(0xffffffffu, fl2);
+    if (lane == 0 && fl2) atomicOr(sflags, fl2);
+    __syncthreads();
+    const int flags = *sflags;
+    if (!(flags & 1)) break;
+    if (flags & 2) {
+      int lastrun = -1;
+      for (int i = lo; i < hi; ++i)
+        if (i == 0 || kr_rank(C.kr[i - 1]) != kr_rank(C.kr[i])) lastrun = i;
+      int run = block_excl_max(lastrun, scan);
+      for (int i = lo; i < hi; ++i) {
+        if (i == 0 || kr_rank(C.kr[i - 1]) != kr_rank(C.kr[i])) run = i;
+        C.rs[i] = (uint16_t)run;
+      }
+      __syncthreads();
+    }
+    // B: safe pairs
+    if (V.monotone) {
+      auto mlf = [&](int x) { return (int)C.ml[x]; };
+      auto mrf = [&](int x) { return (int)C.mr[x]; };
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t k = kr_rank(C.kr[i]);
+        const int u = (flags & 2) ? (int)C.rs[i] : i;
+        C.fl[i] = (mergeable(k) && pair_safe(C.len, C.kr, m, i, u, k, mlf, mrf)) ? 1 : 0;
+      }
+    } else {
+      unsigned long long best = ~0ull;
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t k = kr_rank(C.kr[i]);
+        if (mergeable(k)) {
+          const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
+          best = key < best ? key : best;
+        }
+      }
+      best = block_min_u64(best, scan64);
+      for (int i = lo; i < hi; ++i) C.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
+    }
+    __syncthreads();
+    // C: merge, look up the new pairs, compact
+    uint32_t nsym[B_EPT];
+    uint16_t nlen[B_EPT], nml[B_EPT], nmr[B_EPT];
+    unsigned long long nkr[B_EPT];
+    uint32_t keep = 0;
+#pragma unroll
+    for (int j = 0; j < B_EPT; ++j) {
+      const int i = lo + j;
+      nsym[j] = 0; nlen[j] = 0; nml[j] = 0; nmr[j] = 0; nkr[j] = KR_WALL;
+      if (i < hi && !(i > 0 && C.fl[i - 1])) {
+        keep |= 1u << j;
+        const bool mg = C.fl[i] != 0;
+        if (mg) {
+          const uint32_t r = kr_result(C.kr[i]);
+          nsym[j] = r;
+          nlen[j] = (uint16_t)(((C.len[i] & LEN_MASK) + (C.len[i + 1] & LEN_MASK)) | (C.len[i] & FRAG_START));
+          nml[j] = __ldg(V.max_left + r);
+          nmr[j] = __ldg(V.max_right + r);
+        } else {
+          nsym[j] = C.sym[i];
+          nlen[j] = C.len[i];
+          nml[j] = C.ml[i];
+          nmr[j] = C.mr[i];
+        }
+        const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
+        if (jn >= m) nkr[j] = KR_WALL;
+        else if (!mg && !C.fl[jn]) nkr[j] = C.kr[i];  // unchanged pair keeps its key
+        else nkr[j] = merge_lookup(V, nsym[j], C.fl[jn] ? kr_result(C.kr[jn]) : C.sym[jn]);
+      }
+    }
+    int newm = 0;
+    const int bpos = block_excl_sum(__popc(keep), &newm, scan);
+#pragma unroll
+    for (int j = 0; j < B_EPT; ++j) {
+      if ((keep >> j) & 1u) {
+        const int p = bpos + __popc(keep & ((1u << j) - 1u));
+        C.sym[p] = nsym[j];
+        C.len[p] = nlen[j];
+        C.kr[p] = nkr[j];
+        C.ml[p] = nml[j];
+        C.mr[p] = nmr[j];
+      }
+    }
+    if (tid == 0) *sflags = 0;
+    m = newm;
+    __syncthreads();
+    if (sweep == M && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
+  }
+  for (int i = tid; i < m; i += T) ws.tok[a + i] = (int32_t)C.sym[i];
+  if (tid == 0) {
+    ws.fcnt[a] = m;
+    atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
+    atomicAdd(&ws.gtot[a / BCHUNK / CTOT_GROUP], (uint32_t)m);
+  }
+  __syncthreads();
+}
+
 // Sweep engine of one warp over a batch of M <= 32 symbols (lane i holds
 // symbol i; lanes >= M are empty).  sym / lenb / fst / fid / mlv / mrv / kr
 // are the lane's symbol, byte length, fragment-start flag, fragment, operand
@@ -457,135 +588,98 @@ __device__ __forceinline__ int warp_sweeps(WarpBuf& B, const DevVocab& V, DevSta
 }
 
 
-// ---------------------------------------------------------------------------
-// K3b: queued fragments of at most B_CAP bytes
-//
-// A persistent grid.  First every CTA takes fragments of 33..B_CAP bytes one
-// at a time through the shared-memory engine; then every warp takes batches
-// of short fragments through the warp engine.  Both write a fragment's ids at
-// its byte offset in `tok` and their number at the same offset in `fcnt`.
+// Step engine of one warp over a batch of m <= 32 symbols (lane i holds
+// symbol i; lanes >= m are empty): every step, each fragment of the batch
+// merges its leftmost lowest-rank pair -- the rule itself, one merge at a
+// time per fragment, for any vocabulary.  A step is a segmented minimum
+// (prefix and suffix minima of rank << 5 | lane within the fragment, the
+// segment flag in bit 31), the merge, one lookup per lane at most (the new
+// symbol with its right neighbour, its left neighbour with it) and a
+// compaction.  sym / lenb / fst / fid / kr are the lane's symbol, byte
+// length, fragment-start flag, fragment and the key of pair (i, i+1)
+// (KR_WALL across fragments and past the last symbol).  Ranks are below
+// 2^20 (fewer merges than tokens), so rank << 5 | lane fits in 31 bits.
+constexpr int STEP_MAX_LEN = 16;  // longest fragment of a batch for the step engine
+constexpr uint32_t SEG_FLAG = 0x80000000u;
+constexpr uint32_t SEG_VAL = 0x7FFFFFFFu;
 
-// One fragment of M (33..B_CAP) bytes at byte offset a, all threads of the CTA.
-__device__ void cta_fragment(const Call& c, const Workspace& ws, const DevVocab& V, long long a, int M, CtaBatch& C,
-                             int* scan, unsigned long long* scan64, int* sflags) {
-  const int tid = threadIdx.x, T = B_THREADS, lane = tid & 31;
-  for (int i = tid; i < M; i += T) {
-    const int32_t id = __ldg(V.byte_id + c.text[a + i]);
-    C.sym[i] = (uint32_t)id;
-    C.len[i] = (uint16_t)(1u | (i == 0 ? FRAG_START : 0u));
-    C.ml[i] = __ldg(V.max_left + id);
-    C.mr[i] = __ldg(V.max_right + id);
-  }
-  if (tid == 0) *sflags = 0;
-  __syncthreads();
-  for (int i = tid; i < M; i += T) C.kr[i] = (i + 1 >= M) ? KR_WALL : merge_lookup(V, C.sym[i], C.sym[i + 1]);
-  __syncthreads();
-  int m = M;
-  for (int sweep = 0; sweep <= M; ++sweep) {
-    const int B = (m + T - 1) / T;
-    const int lo = min(tid * B, m), hi = min(lo + B, m);
-    // A: any mergeable pair left?  any overlapping equal-rank pairs?
-    int fl2 = 0;
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t k = kr_rank(C.kr[i]);
-      if (mergeable(k)) {
-        fl2 |= 1;
-        if (i > 0 && kr_rank(C.kr[i - 1]) == k) fl2 |= 2;
-      }
+__device__ __forceinline__ int warp_steps(WarpBuf& B, const DevVocab& V, DevStatus* st, int m, uint32_t& sym,
+                                          uint32_t& lenb, bool& fst, int& fid, unsigned long long& kr) {
+  const int lane = threadIdx.x & 31;
+  const unsigned FULL = 0xffffffffu;
+  for (int step = 0; step <= 32; ++step) {
+    const uint32_t k = kr_rank(kr);
+    const bool mrg = mergeable(k);
+    if (!__any_sync(FULL, mrg)) break;
+    if (step == 32) {  // cannot happen: every step merges a pair of some fragment
+      if (lane == 0) atomicExch(&st->code, ST_EINTERNAL);
+      break;
     }
-    fl2 = __reduce_or_sync(0xffffffffu, fl2);
-    if (lane == 0 && fl2) atomicOr(sflags, fl2);
-    __syncthreads();
-    const int flags = *sflags;
-    if (!(flags & 1)) break;
-    if (flags & 2) {
-      int lastrun = -1;
-      for (int i = lo; i < hi; ++i)
-        if (i == 0 || kr_rank(C.kr[i - 1]) != kr_rank(C.kr[i])) lastrun = i;
-      int run = block_excl_max(lastrun, scan);
-      for (int i = lo; i < hi; ++i) {
-        if (i == 0 || kr_rank(C.kr[i - 1]) != kr_rank(C.kr[i])) run = i;
-        C.rs[i] = (uint16_t)run;
-      }
-      __syncthreads();
+    const uint32_t v = mrg ? ((k << 5) | (uint32_t)lane) : SEG_VAL;
+    const bool nfs = __shfl_down_sync(FULL, fst, 1);  // the next lane starts a fragment
+    uint32_t P = v | ((fst || lane == 0) ? SEG_FLAG : 0u);
+    uint32_t Q = v | ((nfs || lane == 31) ? SEG_FLAG : 0u);
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t o1 = __shfl_up_sync(FULL, P, off);
+      const uint32_t o2 = __shfl_down_sync(FULL, Q, off);
+      if (lane >= off && !(P & SEG_FLAG)) P = (o1 & SEG_FLAG) | min(P, o1 & SEG_VAL);
+      if (lane + off < 32 && !(Q & SEG_FLAG)) Q = (o2 & SEG_FLAG) | min(Q, o2 & SEG_VAL);
     }
-    // B: safe pairs
-    if (V.monotone) {
-      auto mlf = [&](int x) { return (int)C.ml[x]; };
-      auto mrf = [&](int x) { return (int)C.mr[x]; };
-      for (int i = lo; i < hi; ++i) {
-        const uint32_t k = kr_rank(C.kr[i]);
-        const int u = (flags & 2) ? (int)C.rs[i] : i;
-        C.fl[i] = (mergeable(k) && pair_safe(C.len, C.kr, m, i, u, k, mlf, mrf)) ? 1 : 0;
+    const bool sel = mrg && v == min(P & SEG_VAL, Q & SEG_VAL);
+    // merge: the selected pair's left symbol takes the result, its right one goes
+    const bool absorbed = __shfl_up_sync(FULL, sel, 1) && lane > 0;
+    const uint32_t res = kr_result(kr);
+    const uint32_t lnext = __shfl_down_sync(FULL, lenb, 1);
+    const bool nsel = __shfl_down_sync(FULL, sel, 1);
+    const uint32_t nres = __shfl_down_sync(FULL, res, 1);
+    const uint32_t sym2 = __shfl_down_sync(FULL, sym, 2);
+    const bool fst2 = __shfl_down_sync(FULL, fst, 2);
+    uint32_t nsym = sym, nlen = lenb;
+    unsigned long long nkr = kr;
+    bool look = false;
+    uint32_t la = 0, lb = 0;
+    if (sel) {
+      nsym = res;
+      nlen = lenb + lnext;
+      if (lane + 2 < m && !fst2) {
+        look = true;
+        la = res;
+        lb = sym2;
+      } else {
+        nkr = KR_WALL;
       }
+    } else if (nsel && !nfs && lane < m) {
+      look = true;  // the pair with the merged symbol on the right
+      la = sym;
+      lb = nres;
+    }
+    if (look) nkr = merge_lookup(V, la, lb);
+    // compaction through the warp's buffer
+    const bool keep = lane < m && !absorbed;
+    const uint32_t kmask = __ballot_sync(FULL, keep);
+    if (keep) {
+      const int p = __popc(kmask & ((1u << lane) - 1u));
+      B.sym[p] = nsym;
+      B.len[p] = (uint16_t)(nlen | (fst ? FRAG_START : 0u));
+      B.kr[p] = nkr;
+      B.fidx[p] = (uint16_t)fid;
+    }
+    __syncwarp();
+    m = __popc(kmask);
+    if (lane < m) {
+      sym = B.sym[lane];
+      const uint32_t l = B.len[lane];
+      lenb = l & LEN_MASK;
+      fst = (l & FRAG_START) != 0;
+      kr = B.kr[lane];
+      fid = B.fidx[lane];
     } else {
-      unsigned long long best = ~0ull;
-      for (int i = lo; i < hi; ++i) {
-        const uint32_t k = kr_rank(C.kr[i]);
-        if (mergeable(k)) {
-          const unsigned long long key = ((unsigned long long)k << 32) | (uint32_t)i;
-          best = key < best ? key : best;
-        }
-      }
-      best = block_min_u64(best, scan64);
-      for (int i = lo; i < hi; ++i) C.fl[i] = ((uint32_t)best == (uint32_t)i) ? 1 : 0;
+      sym = 0; lenb = 0; fst = false; kr = KR_WALL; fid = 0;
     }
-    __syncthreads();
-    // C: merge, look up the new pairs, compact
-    uint32_t nsym[B_EPT];
-    uint16_t nlen[B_EPT], nml[B_EPT], nmr[B_EPT];
-    unsigned long long nkr[B_EPT];
-    uint32_t keep = 0;
-#pragma unroll
-    for (int j = 0; j < B_EPT; ++j) {
-      const int i = lo + j;
-      nsym[j] = 0; nlen[j] = 0; nml[j] = 0; nmr[j] = 0; nkr[j] = KR_WALL;
-      if (i < hi && !(i > 0 && C.fl[i - 1])) {
-        keep |= 1u << j;
-        const bool mg = C.fl[i] != 0;
-        if (mg) {
-          const uint32_t r = kr_result(C.kr[i]);
-          nsym[j] = r;
-          nlen[j] = (uint16_t)(((C.len[i] & LEN_MASK) + (C.len[i + 1] & LEN_MASK)) | (C.len[i] & FRAG_START));
-          nml[j] = __ldg(V.max_left + r);
-          nmr[j] = __ldg(V.max_right + r);
-        } else {
-          nsym[j] = C.sym[i];
-          nlen[j] = C.len[i];
-          nml[j] = C.ml[i];
-          nmr[j] = C.mr[i];
-        }
-        const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
-        if (jn >= m) nkr[j] = KR_WALL;
-        else if (!mg && !C.fl[jn]) nkr[j] = C.kr[i];  // unchanged pair keeps its key
-        else nkr[j] = merge_lookup(V, nsym[j], C.fl[jn] ? kr_result(C.kr[jn]) : C.sym[jn]);
-      }
-    }
-    int newm = 0;
-    const int bpos = block_excl_sum(__popc(keep), &newm, scan);
-#pragma unroll
-    for (int j = 0; j < B_EPT; ++j) {
-      if ((keep >> j) & 1u) {
-        const int p = bpos + __popc(keep & ((1u << j) - 1u));
-        C.sym[p] = nsym[j];
-        C.len[p] = nlen[j];
-        C.kr[p] = nkr[j];
-        C.ml[p] = nml[j];
-        C.mr[p] = nmr[j];
-      }
-    }
-    if (tid == 0) *sflags = 0;
-    m = newm;
-    __syncthreads();
-    if (sweep == M && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
+    __syncwarp();
   }
-  for (int i = tid; i < m; i += T) ws.tok[a + i] = (int32_t)C.sym[i];
-  if (tid == 0) {
-    ws.fcnt[a] = m;
-    atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
-    atomicAdd(&ws.gtot[a / BCHUNK / CTOT_GROUP], (uint32_t)m);
-  }
-  __syncthreads();
+  return m;
 }
 
 // One warp encodes a batch of short fragments (at most SB_MAX bytes in all).
@@ -612,22 +706,28 @@ __device__ void short_batch(const Call& c, const Workspace& ws, const DevVocab& 
   __syncwarp();
   const long long fpos = __shfl_sync(FULL, start, fid);
   const int foff = __shfl_sync(FULL, off, fid);
+  // batches of short fragments only take the step engine (few merges
+  // each, so few steps); a batch with a longer one the sweep engine, which
+  // merges all certified-safe pairs at once (monotone vocabularies)
+  const bool stepwise = !V.monotone || __reduce_max_sync(FULL, (unsigned)len) <= STEP_MAX_LEN;
   uint32_t sym = 0, lenb = 0, mlv = 0, mrv = 0;
   bool fst = false;
   if (lane < M) {
     const int j = lane - foff;
-    const int32_t id = __ldg(V.byte_id + c.text[fpos + j]);
-    sym = (uint32_t)id;
+    sym = (uint32_t)__ldg(V.byte_id + c.text[fpos + j]);
     lenb = 1;
     fst = j == 0;
-    mlv = __ldg(V.max_left + id);
-    mrv = __ldg(V.max_right + id);
+    if (!stepwise) {
+      mlv = __ldg(V.max_left + sym);
+      mrv = __ldg(V.max_right + sym);
+    }
   }
   const uint32_t nxt = __shfl_down_sync(FULL, sym, 1);
   const bool nfs = __shfl_down_sync(FULL, fst, 1);
   unsigned long long kr = KR_WALL;
   if (lane + 1 < M && !nfs) kr = merge_lookup(V, sym, nxt);
-  const int m = warp_sweeps(B, V, ws.st, M, sym, lenb, fst, fid, mlv, mrv, kr);
+  const int m = stepwise ? warp_steps(B, V, ws.st, M, sym, lenb, fst, fid, kr)
+                         : warp_sweeps(B, V, ws.st, M, sym, lenb, fst, fid, mlv, mrv, kr);
   // ids at the fragment's byte offset, and their number
   const uint32_t fsm = __ballot_sync(FULL, lane < m && fst);
   const long long pos = __shfl_sync(FULL, start, fid);
