@@ -591,17 +591,16 @@ __device__ __forceinline__ int warp_sweeps(WarpBuf& B, const DevVocab& V, DevSta
 // Step engine of one warp over a batch of m <= 32 symbols (lane i holds
 // symbol i; lanes >= m are empty): every step, each fragment of the batch
 // merges its leftmost lowest-rank pair -- the rule itself, one merge at a
-// time per fragment, for any vocabulary.  A step is a segmented minimum
-// (prefix and suffix minima of rank << 5 | lane within the fragment, the
-// segment flag in bit 31), the merge, one lookup per lane at most (the new
-// symbol with its right neighbour, its left neighbour with it) and a
-// compaction.  sym / lenb / fst / fid / kr are the lane's symbol, byte
+// time per fragment, for any vocabulary.  A step is a minimum of
+// rank << 5 | lane over each fragment's lanes (one warp reduction with the
+// fragment's lanes as the member mask, every fragment at once), the merge,
+// one lookup per lane at most (the new symbol with its right neighbour, its
+// left neighbour with it) and a compaction.  sym / lenb / fst / fid / kr are the lane's symbol, byte
 // length, fragment-start flag, fragment and the key of pair (i, i+1)
 // (KR_WALL across fragments and past the last symbol).  Ranks are below
 // 2^20 (fewer merges than tokens), so rank << 5 | lane fits in 31 bits.
 constexpr int STEP_MAX_LEN = 16;  // longest fragment of a batch for the step engine
-constexpr uint32_t SEG_FLAG = 0x80000000u;
-constexpr uint32_t SEG_VAL = 0x7FFFFFFFu;
+constexpr uint32_t SEG_VAL = 0x7FFFFFFFu;  // no mergeable pair
 
 __device__ __forceinline__ int warp_steps(WarpBuf& B, const DevVocab& V, DevStatus* st, int m, uint32_t& sym,
                                           uint32_t& lenb, bool& fst, int& fid, unsigned long long& kr) {
@@ -617,16 +616,17 @@ __device__ __forceinline__ int warp_steps(WarpBuf& B, const DevVocab& V, DevStat
     }
     const uint32_t v = mrg ? ((k << 5) | (uint32_t)lane) : SEG_VAL;
     const bool nfs = __shfl_down_sync(FULL, fst, 1);  // the next lane starts a fragment
-    uint32_t P = v | ((fst || lane == 0) ? SEG_FLAG : 0u);
-    uint32_t Q = v | ((nfs || lane == 31) ? SEG_FLAG : 0u);
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t o1 = __shfl_up_sync(FULL, P, off);
-      const uint32_t o2 = __shfl_down_sync(FULL, Q, off);
-      if (lane >= off && !(P & SEG_FLAG)) P = (o1 & SEG_FLAG) | min(P, o1 & SEG_VAL);
-      if (lane + off < 32 && !(Q & SEG_FLAG)) Q = (o2 & SEG_FLAG) | min(Q, o2 & SEG_VAL);
-    }
-    const bool sel = mrg && v == min(P & SEG_VAL, Q & SEG_VAL);
+    // the lanes of this lane's fragment (the empty lanes past m join the last
+    // one), and their minimum: one reduction per fragment, all at once
+    const unsigned fsm = __ballot_sync(FULL, fst);
+    const unsigned upto = lane == 31 ? 0xffffffffu : ((2u << lane) - 1u);
+    const unsigned before = fsm & upto;
+    const int first = before ? 31 - __clz(before) : 0;
+    const unsigned after = fsm & ~upto;
+    const unsigned fmask = (after ? ((after & (0u - after)) - 1u) : 0xffffffffu) & ~((1u << first) - 1u);
+    // (every lane takes part in the reduction, so it is computed first)
+    const uint32_t fmin = __reduce_min_sync(fmask, v);
+    const bool sel = mrg && v == fmin;
     // merge: the selected pair's left symbol takes the result, its right one goes
     const bool absorbed = __shfl_up_sync(FULL, sel, 1) && lane > 0;
     const uint32_t res = kr_result(kr);
@@ -709,7 +709,8 @@ __device__ void short_batch(const Call& c, const Workspace& ws, const DevVocab& 
   // batches of short fragments only take the step engine (few merges
   // each, so few steps); a batch with a longer one the sweep engine, which
   // merges all certified-safe pairs at once (monotone vocabularies)
-  const bool stepwise = !V.monotone || __reduce_max_sync(FULL, (unsigned)len) <= STEP_MAX_LEN;
+  const unsigned maxlen = __reduce_max_sync(FULL, (unsigned)len);
+  const bool stepwise = !V.monotone || maxlen <= STEP_MAX_LEN;
   uint32_t sym = 0, lenb = 0, mlv = 0, mrv = 0;
   bool fst = false;
   if (lane < M) {
