@@ -451,7 +451,9 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
     }
   }
   uint32_t wbits = 10;
-  while ((1ull << wbits) < 2ull * whole_tokens.size()) ++wbits;
+  // a quarter full at most: a miss (most probes) ends after ~1.4 entries on
+  // average, and a warp's longest chain is short
+  while ((1ull << wbits) < 4ull * whole_tokens.size()) ++wbits;
   std::vector<WholeEntry> whole(1ull << wbits, WholeEntry{0, 0, 0});
   if (vocab_off[n_vocab] - vocab_off[0] >= (1ull << 32)) return fail(nullptr, TOK_EMERGES, "vocabulary too large");
   std::vector<uint32_t> off32(n_vocab + 1);
