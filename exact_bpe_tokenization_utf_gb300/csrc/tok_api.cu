@@ -387,7 +387,9 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   }
   // merges -> hash table
   uint32_t bits = 10;
-  while ((1ull << bits) < 2ull * n_merges) ++bits;
+  // a quarter full at most: short probe chains for the engines' lookups
+  // (a warp waits for its longest)
+  while ((1ull << bits) < 4ull * n_merges) ++bits;
   std::vector<MergeEntry> table(1ull << bits, MergeEntry{EMPTY_KEY, 0, 0});
   std::vector<uint16_t> max_left(n_vocab, 0), max_right(n_vocab, 0);
   std::vector<int64_t> last_made(n_vocab, -1), first_used(n_vocab, INT64_MAX);
