@@ -23,6 +23,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -84,7 +85,10 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+        # the samples go to BENCH_CLOCKS_CSV when set (to keep them), else to
+        # a scratch file; the JSON line carries their summary either way
+        self.path = os.environ.get("BENCH_CLOCKS_CSV") or os.path.join(tempfile.gettempdir(),
+                                                                        "bench_clocks_%d.csv" % os.getpid())
 
     def __enter__(self):
         try:
