@@ -33,7 +33,6 @@
 namespace tokgb {
 
 // pair keys: rank << 32 | result
-constexpr uint32_t RANK_NONE = 0xFFFFFFFFu;  // not a merge (may become one when a symbol changes)
 constexpr uint32_t RANK_WALL = 0xFFFFFFFEu;  // between fragments, or past the last symbol: never merges
 constexpr uint32_t RANK_NEED = 0xFFFFFFFDu;  // to be looked up
 constexpr unsigned long long KR_WALL = (unsigned long long)RANK_WALL << 32;
@@ -767,12 +766,13 @@ struct EngineSmem {
 // K3b: a persistent grid.  Longest work first: fragments of more than B_CAP
 // bytes (global-memory engine, taken one at a time), then those of 33..B_CAP
 // bytes (shared-memory engine, fragment i to CTA i mod grid), then batches of
-// short fragments (warp engine, batch b to warp b mod warps, counted from
-// the last CTA so that the CTAs with a 33..B_CAP-byte fragment get fewer).
+// short fragments (warp step or sweep engine, batch b to warp b mod warps,
+// counted from the last CTA so that the CTAs with a 33..B_CAP-byte fragment
+// get fewer).
 // Static assignment keeps thousands of warps off one contended counter.
 __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
   __shared__ EngineSmem S;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = B_THREADS;
+  const int tid = threadIdx.x, warp = tid >> 5, T = B_THREADS;
   DevStatus* st = ws.st;
   if (tid == 0) {  // the queue sizes, loaded together (K2 wrote them)
     S.nq[0] = st->long_count;

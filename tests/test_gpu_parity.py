@@ -329,6 +329,21 @@ def test_ragged_sizes_and_tier_edges(pkg, pattern):
             assert tok.encode(d).tolist() == encode(d, v, pattern), (n, alpha)
 
 
+@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+def test_warp_engine_tiers(pkg, pattern):
+    # fragments around the warp engines' limits: a batch whose fragments are
+    # all at most 16 bytes merges step by step, one with a longer fragment
+    # (up to 32) in certified sweeps, longer fragments go to the CTA engines;
+    # rare letters keep the fragments from being whole tokens
+    name = "gpt2_session_100k" if pattern == PATTERN_GPT2 else "cl100k_session_100k"
+    v, tok = pair(pkg, name, pattern)
+    rnd = random.Random(11)
+    for lens in ((2, 8, 15, 16), (16, 17), (15, 16, 17, 18), (24, 31, 32), (31, 32, 33, 34), (2, 3, 16, 32, 40)):
+        words = [" " + "".join(rnd.choice("qzxjkvwy") for _ in range(rnd.choice(lens) - 1)) for _ in range(300)]
+        d = "".join(words).encode()
+        assert tok.encode(d).tolist() == encode(d, v, pattern), lens
+
+
 def test_invalid_utf8_offsets(pkg):
     _, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
     cases = [b"abc\xe4\xb8", b"\x80abc", b"ab\xc0\xafcd", b"x\xed\xa0\x80y", b"\xf4\x90\x80\x80", b"ok \xff",
