@@ -4,9 +4,9 @@
 // merge.  The pages tier fragments by length (one thread, one warp, one block
 // per fragment).  Here most fragments are settled by one probe (single bytes,
 // whole self-encoding tokens); of the rest, those of at most 32 bytes share a
-// warp, one symbol per lane, several fragments per warp; fragments of
-// 33..B_CAP bytes get a CTA with shared memory, longer ones a CTA with global
-// memory.
+// warp, one symbol per lane, several fragments per warp (merged step by step
+// when all are at most 16 bytes, else in sweeps); fragments of 33..B_CAP
+// bytes get a CTA with shared memory, longer ones a CTA with global memory.
 //
 // Sweep engine.  The symbols of many fragments sit in one array; the pair
 // between two fragments is a "wall" that never merges.  Let k be the rank of

@@ -5,7 +5,7 @@
 //   K2 boundaries    per 1 KiB chunk: UTF-8 validation + per-code-point class +
 //                    run decomposition rules -> fragment-start bitmask
 //                    (Section 4.1); the run states at the chunk's edges come
-//                    from the text just beyond them.  In encode calls K2 then
+//                    from its halo (or the text beyond).  In encode calls K2 then
 //                    settles every fragment that is one byte, or whose bytes
 //                    are a token that encodes to itself, with one probe, and
 //                    queues the others: those of at most 32 bytes packed into
@@ -14,10 +14,13 @@
 //                    by the second of the edge's two CTAs to get there.
 //   K3b bpe_engine   persistent: CTAs take fragments longer than B_CAP bytes
 //                    (arrays in global memory), then 33..B_CAP-byte fragments
-//                    (shared memory), then warps take short batches (one
-//                    symbol per lane); every sweep merges all certified-safe
-//                    pairs.  Every fragment's id count is added to the total
-//                    of its 512-byte chunk and of that chunk's group.
+//                    (shared memory; sweeps that merge all certified-safe
+//                    pairs), then warps take short batches (one symbol per
+//                    lane): batches of fragments of at most 16 bytes merge
+//                    each fragment's leftmost lowest-rank pair per step, the
+//                    others run certified sweeps.  Every fragment's id count
+//                    is added to the total of its 512-byte chunk and of that
+//                    chunk's group.
 //   K5 emit          per chunk: ids before it (group totals, then chunk
 //                    totals), fragment counts -> offsets, copy of the ids in
 //                    text order
