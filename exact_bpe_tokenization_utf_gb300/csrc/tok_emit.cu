@@ -53,16 +53,48 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
 
 }  // namespace
 
-// K5: the ids of the fragments that start in one 512-byte chunk
+// block-wide exclusive sum of v and the sum of u over the CTA, in one pass
+__device__ __forceinline__ int block_excl_sum_and_total(int v, unsigned long long u, int* total_v,
+                                                        unsigned long long* total_u, int* sh,
+                                                        unsigned long long* sh64) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+  unsigned long long su = u;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+    su += __shfl_xor_sync(0xffffffffu, su, off);
+  }
+  if (lane == 31) sh[warp] = inc;
+  if (lane == 0) sh64[warp] = su;
+  __syncthreads();
+  int pre = 0, tot = 0;
+  unsigned long long tu = 0;
+#pragma unroll
+  for (int k = 0; k < B_THREADS / 32; ++k) {
+    const int x = sh[k];
+    pre += k < warp ? x : 0;
+    tot += x;
+    tu += sh64[k];
+  }
+  *total_v = tot;
+  *total_u = tu;
+  __syncthreads();
+  return pre + inc - v;
+}
+
+// K5: the ids of the fragments that start in one 512-byte chunk.  Thread t
+// owns bytes 4t .. 4t + 3 of the chunk and the fragments that start there:
+// their id counts are in its registers after the up-front loads, so one scan
+// gives every fragment's place.  Fragments of more than 8 ids are copied by
+// the whole CTA.
 template <bool OFFS>
-__global__ void __launch_bounds__(B_THREADS, 16) k_emit(Call c, Workspace ws, DevVocab V) {
-  __shared__ uint32_t bits[BCHUNK / 32];
-  __shared__ uint16_t fstart[BCHUNK];
-  __shared__ int fcount[BCHUNK];
-  __shared__ int foff[BCHUNK];
-  __shared__ uint16_t big[BCHUNK];
-  __shared__ __align__(16) int cnt[BCHUNK];  // fcnt of every byte of the chunk (meaningful at fragment starts)
-  __shared__ __align__(16) int tk[BCHUNK];   // tok of every byte of the chunk
+__global__ void __launch_bounds__(B_THREADS, OFFS ? 12 : 16) k_emit(Call c, Workspace ws, DevVocab V) {
+  constexpr int MAX_BIG = BCHUNK / 8;  // fragments of more than 8 ids have 9 bytes or more
+  __shared__ __align__(16) int tk[BCHUNK];  // tok of every byte of the chunk
+  __shared__ int idb[BCHUNK];               // ids of the chunk before each fragment start (batch item offsets)
+  __shared__ int big_a[MAX_BIG], big_k[MAX_BIG], big_o[MAX_BIG];
   __shared__ int scan[B_THREADS / 32];
   __shared__ unsigned long long scan64[B_THREADS / 32];
   __shared__ int s_item, s_nbig, s_last;
@@ -73,108 +105,102 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_emit(Call c, Workspace ws, De
   const long long r0 = chunk * BCHUNK;
   const long long r1 = min(r0 + BCHUNK, c.n);
   if (tid == 0) s_nbig = 0;
-  // every load this CTA needs, issued together: the bitmask, the counts and
-  // ids of all the chunk's bytes (positions past the text end, or that start
-  // no fragment, are read but not used; the workspace holds whole chunks),
-  // and the totals before the chunk (group totals before its group, chunk
-  // totals before it in its group)
+  // every load this CTA needs, issued together: the counts and ids of the
+  // thread's bytes (positions past the text end, or that start no fragment,
+  // are read but not used; the workspace holds whole chunks), its bits of
+  // the bitmask, and the totals before the chunk (group totals before its
+  // group, chunk totals before it in its group)
   static_assert(BCHUNK == 4 * B_THREADS, "one int4 of counts and ids per thread");
   const int4 cnt4 = reinterpret_cast<const int4*>(ws.fcnt + r0)[tid];
   const int4 tk4 = reinterpret_cast<const int4*>(ws.tok + r0)[tid];
+  const int q0 = 4 * tid;
+  uint32_t mine = 0;
+  if (r0 + q0 < r1) {
+    mine = (ws.pstart[(r0 >> 5) + (q0 >> 5)] >> (q0 & 31)) & 0xFu;
+    if (r1 - (r0 + q0) < 4) mine &= (1u << (r1 - (r0 + q0))) - 1u;
+  }
   unsigned long long part = 0;
   const long long grp = chunk / CTOT_GROUP;
   for (long long i = tid; i < grp; i += T) part += ws.gtot[i];
   for (long long i = grp * CTOT_GROUP + tid; i < chunk; i += T) part += ws.ctot[i];
   const uint32_t my_total = ws.ctot[chunk];
-  if (tid < BCHUNK / 32) {
-    const long long p = r0 + 32ll * tid;
-    uint32_t v = 0;
-    if (p < r1) {
-      v = ws.pstart[(r0 >> 5) + tid];
-      if (r1 - p < 32) v &= (1u << (r1 - p)) - 1u;
-    }
-    bits[tid] = v;
-  }
-  reinterpret_cast<int4*>(cnt)[tid] = cnt4;
   reinterpret_cast<int4*>(tk)[tid] = tk4;
-  __syncthreads();
-  // the fragments that start in this chunk, and their id counts
-  const int q0 = tid * 4;
-  const uint32_t mine = (bits[q0 >> 5] >> (q0 & 31)) & 0xFu;
-  int nf = 0;
-  int idx = block_excl_sum_t(__popc(mine), &nf, scan);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if ((mine >> q) & 1u) fstart[idx++] = (uint16_t)(q0 + q);
-  __syncthreads();
-  const int FB = (nf + T - 1) / T;
-  const int flo = min(tid * FB, nf), fhi = min(flo + FB, nf);
+  // id counts of the thread's fragments: between 1 and (bytes to the text
+  // end); anything else would be a bug upstream, reported instead of
+  // written out of bounds
+  int cn[4] = {cnt4.x, cnt4.y, cnt4.z, cnt4.w};
   int ids = 0;
-  for (int f = flo; f < fhi; ++f) {
-    // a fragment has between 1 and (bytes to the text end) ids; anything else
-    // would be a bug upstream, reported instead of written out of bounds
-    int k = cnt[fstart[f]];
-    if (k < 1 || k > c.n - (r0 + fstart[f])) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (!((mine >> q) & 1u)) { cn[q] = 0; continue; }
+    if (cn[q] < 1 || cn[q] > c.n - (r0 + q0 + q)) {
       atomicExch(&st->code, ST_EINTERNAL);
-      k = 0;
+      cn[q] = 0;
     }
-    fcount[f] = k;
-    ids += k;
+    ids += cn[q];
   }
   int total = 0;
-  int o = block_excl_sum_t(ids, &total, scan);
-  for (int f = flo; f < fhi; ++f) {
-    foff[f] = o;
-    o += fcount[f];
-  }
-  // ids before this chunk
-  unsigned long long base = 0;
-  block_excl_sum_t(part, &base, scan64);
+  unsigned long long base = 0;  // ids before this chunk
+  int o = block_excl_sum_and_total(ids, part, &total, &base, scan, scan64);
   if ((uint32_t)total != my_total) {  // the counts disagree with the chunk total: a bug upstream
     if (tid == 0) atomicExch(&st->code, ST_EINTERNAL);
     total = 0;
   }
-  __syncthreads();
-  // ids in text order: short fragments by their thread, long ones by the CTA
+  // ids in text order: fragments of up to 8 ids by their thread, longer ones
+  // by the CTA
   if (total > 0) {
-    for (int f = flo; f < fhi; ++f) {
-      const int k = fcount[f];
-      const long long a = r0 + fstart[f];
+#pragma unroll(OFFS ? 1 : 4)
+    for (int q = 0; q < 4; ++q) {
+      if (!((mine >> q) & 1u)) continue;
+      const int k = q == 0 ? cn[0] : q == 1 ? cn[1] : q == 2 ? cn[2] : cn[3];
+      const int a0 = q0 + q;
+      const long long a = r0 + a0;
+      if (c.item_off) idb[a0] = o;
       if (k <= 8) {
         // ids from the staged copy while they lie in the chunk
-        const int a0 = fstart[f];
-        for (int j = 0; j < k; ++j) c.out[base + foff[f] + j] = a0 + j < BCHUNK ? tk[a0 + j] : ws.tok[a + j];
+        for (int j = 0; j < k; ++j) c.out[base + o + j] = a0 + j < BCHUNK ? tk[a0 + j] : ws.tok[a + j];
         if (OFFS) {
           long long off = a;
           for (int j = 0; j < k; ++j) {
-            c.out_off[base + foff[f] + j] = off;
+            c.out_off[base + o + j] = off;
             off += __ldg(V.tok_len + (a0 + j < BCHUNK ? tk[a0 + j] : ws.tok[a + j]));
           }
         }
-      } else {
-        big[atomicAdd(&s_nbig, 1)] = (uint16_t)f;
+      } else if (k > 0) {
+        const int bi = atomicAdd(&s_nbig, 1);
+        if (bi < MAX_BIG) {
+          big_a[bi] = a0;
+          big_k[bi] = k;
+          big_o[bi] = o;
+        } else {
+          atomicExch(&st->code, ST_EINTERNAL);
+        }
       }
+      o += k;
     }
   }
   __syncthreads();
-  for (int b = 0; b < s_nbig; ++b) {
-    const int f = big[b];
-    const long long a = r0 + fstart[f];
-    for (int j = tid; j < fcount[f]; j += T) c.out[base + foff[f] + j] = ws.tok[a + j];
+  const int nbig = min(s_nbig, MAX_BIG);
+  for (int b = 0; b < nbig; ++b) {
+    const long long a = r0 + big_a[b];
+    const int k = big_k[b];
+    const unsigned long long ob = base + (unsigned long long)big_o[b];
+    for (int j = tid; j < k; j += T) c.out[ob + j] = ws.tok[a + j];
     if (OFFS) {
       // offsets: exclusive scan of the token lengths, one tile of T ids at a time
       long long carry = a;
-      for (int j0 = 0; j0 < fcount[f]; j0 += T) {
+      for (int j0 = 0; j0 < k; j0 += T) {
         const int j = j0 + tid;
-        const int len = j < fcount[f] ? (int)__ldg(V.tok_len + ws.tok[a + j]) : 0;
+        const int len = j < k ? (int)__ldg(V.tok_len + ws.tok[a + j]) : 0;
         int tile = 0;
         const int ex = block_excl_sum_t(len, &tile, scan);
-        if (j < fcount[f]) c.out_off[base + foff[f] + j] = carry + ex;
+        if (j < k) c.out_off[ob + j] = carry + ex;
         carry += tile;
       }
     }
   }
-  // batch: ids before each item start in this chunk
+  // batch: ids before each item start in this chunk (every item start is a
+  // fragment start)
   if (c.item_off) {
     if (tid == 0) {
       int a = 0, b = c.n_items + 1;
@@ -188,12 +214,7 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_emit(Call c, Workspace ws, De
     for (int k = s_item + tid; k <= c.n_items; k += T) {
       const long long x = c.item[k];
       if (x >= r1) break;
-      int a = 0, b = nf;  // the fragment that starts at x
-      while (a < b) {
-        const int mid = (a + b) >> 1;
-        if (r0 + fstart[mid] < x) a = mid + 1; else b = mid;
-      }
-      c.item_off[k] = (long long)base + (a < nf ? foff[a] : total);
+      c.item_off[k] = (long long)base + (total > 0 ? idb[x - r0] : 0);
     }
   }
   // the last CTA to finish completes the status: the number of ids is the
