@@ -629,6 +629,7 @@ int encode_host(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, 
   if (dir_ids && (!offsets || dir_off)) {
     c.out = dir_ids;
     c.out_off = dir_off;
+    c.out_host = 1;
     c.user_status = h->d_ustatus;
     rc = run_chain(h, c, s);
     if (rc) return rc;

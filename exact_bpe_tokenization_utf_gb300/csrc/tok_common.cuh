@@ -154,6 +154,7 @@ struct Call {
   long long* item_off;        // device, n_items + 1 (batch) or nullptr
   long long* user_status;     // device int64[4] or nullptr
   int settle;                 // K2 also settles fragments and fills the queues (encode calls)
+  int out_host;               // `out` is pinned host memory (mapped): K5 stages a chunk's ids for coalesced stores
   Prefetch pf[3];             // whole-token table, token bytes, merge table
 };
 

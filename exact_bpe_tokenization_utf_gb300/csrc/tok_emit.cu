@@ -89,10 +89,12 @@ __device__ __forceinline__ int block_excl_sum_and_total(int v, unsigned long lon
 // their id counts are in its registers after the up-front loads, so one scan
 // gives every fragment's place.  Fragments of more than 8 ids are copied by
 // the whole CTA.
-template <bool OFFS>
-__global__ void __launch_bounds__(B_THREADS, OFFS ? 12 : 16) k_emit(Call c, Workspace ws, DevVocab V) {
+template <bool OFFS, bool STAGED>
+__global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Workspace ws, DevVocab V) {
   constexpr int MAX_BIG = BCHUNK / 8;  // fragments of more than 8 ids have 9 bytes or more
+  constexpr int STAGE = 2 * BCHUNK;        // ids of a chunk staged for coalesced stores
   __shared__ __align__(16) int tk[BCHUNK];  // tok of every byte of the chunk
+  __shared__ int sid[STAGED ? STAGE : 1];   // the chunk's ids, in order, when they go to host memory and fit
   __shared__ int idb[BCHUNK];               // ids of the chunk before each fragment start (batch item offsets)
   __shared__ int big_a[MAX_BIG], big_k[MAX_BIG], big_o[MAX_BIG];
   __shared__ int scan[B_THREADS / 32];
@@ -147,7 +149,10 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 12 : 16) k_emit(Call c, Work
     total = 0;
   }
   // ids in text order: fragments of up to 8 ids by their thread, longer ones
-  // by the CTA
+  // by the CTA.  When the output is host memory, a chunk's ids that fit in
+  // shared memory are staged there and stored in one coalesced pass (the
+  // scattered stores of the threads cost far more over the host link)
+  const bool staged = STAGED && total <= STAGE;
   if (total > 0) {
 #pragma unroll(OFFS ? 1 : 4)
     for (int q = 0; q < 4; ++q) {
@@ -158,7 +163,11 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 12 : 16) k_emit(Call c, Work
       if (c.item_off) idb[a0] = o;
       if (k <= 8) {
         // ids from the staged copy while they lie in the chunk
-        for (int j = 0; j < k; ++j) c.out[base + o + j] = a0 + j < BCHUNK ? tk[a0 + j] : ws.tok[a + j];
+        for (int j = 0; j < k; ++j) {
+          const int id = a0 + j < BCHUNK ? tk[a0 + j] : ws.tok[a + j];
+          if (staged) sid[o + j] = id;
+          else c.out[base + o + j] = id;
+        }
         if (OFFS) {
           long long off = a;
           for (int j = 0; j < k; ++j) {
@@ -185,7 +194,10 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 12 : 16) k_emit(Call c, Work
     const long long a = r0 + big_a[b];
     const int k = big_k[b];
     const unsigned long long ob = base + (unsigned long long)big_o[b];
-    for (int j = tid; j < k; j += T) c.out[ob + j] = ws.tok[a + j];
+    for (int j = tid; j < k; j += T) {
+      if (staged) sid[big_o[b] + j] = ws.tok[a + j];
+      else c.out[ob + j] = ws.tok[a + j];
+    }
     if (OFFS) {
       // offsets: exclusive scan of the token lengths, one tile of T ids at a time
       long long carry = a;
@@ -198,6 +210,10 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 12 : 16) k_emit(Call c, Work
         carry += tile;
       }
     }
+  }
+  if (staged && total > 0) {
+    __syncthreads();
+    for (int i = tid; i < total; i += T) c.out[base + i] = sid[i];
   }
   // batch: ids before each item start in this chunk (every item start is a
   // fragment start)
@@ -252,8 +268,14 @@ __global__ void k_status_only(Call c, Workspace ws) {
 }
 
 void launch_emit(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
-  if (c.out_off) k_emit<true><<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
-  else k_emit<false><<<(unsigned)n_bchunks(c.n), B_THREADS, 0, s>>>(c, w, v);
+  const unsigned g = (unsigned)n_bchunks(c.n);
+  if (c.out_off) {
+    if (c.out_host) k_emit<true, true><<<g, B_THREADS, 0, s>>>(c, w, v);
+    else k_emit<true, false><<<g, B_THREADS, 0, s>>>(c, w, v);
+  } else {
+    if (c.out_host) k_emit<false, true><<<g, B_THREADS, 0, s>>>(c, w, v);
+    else k_emit<false, false><<<g, B_THREADS, 0, s>>>(c, w, v);
+  }
 }
 
 void launch_status_only(const Call& c, const Workspace& w, cudaStream_t s) {
