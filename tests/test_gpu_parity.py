@@ -193,7 +193,13 @@ def test_pinned_host_buffers(pkg):
     # reach past a chunk's halo (their edge states read the host buffer) and a
     # length that ends inside a chunk
     runs = _runs_at_chunk_edges([b"\r\n", b"7", b" "], [13, 17, 40], range(-2, 19, 4))[:150_001]
-    for data in (textgen.agentic_session(100_000, 1021).encode(), b"x", b"  \r\n\t 12345 abc", runs):
+    # letter runs of many ids: one that the emit kernel stages with the rest
+    # of its 512-byte chunk, and one in the next chunk, which then has more
+    # ids than it stages
+    rng = random.Random(1029)
+    letters = bytes(rng.choice(b"abcdefghijklmnopqrstuvwxyz") for _ in range(4200))
+    long_runs = b"x " + letters[:200] + b" " + b"ab " * 120 + letters[200:] + b" tail"
+    for data in (textgen.agentic_session(100_000, 1021).encode(), b"x", b"  \r\n\t 12345 abc", runs, long_runs):
         n = len(data)
         h_text = torch.frombuffer(bytearray(data), dtype=torch.uint8).pin_memory()
         h_ids = torch.empty(n, dtype=torch.int32).pin_memory()
