@@ -64,3 +64,42 @@ def test_product_path_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".inc")):
                 with open(os.path.join(dp, f)) as fh:
                     assert not re.search(r"\boracle\b", fh.read()), f
+
+
+def test_header_compiles_as_c_and_links(libpath, tmp_path):
+    # the header is plain C (C99, no warnings); a C program links against the
+    # library, reaches every declared entry point, and a load without a usable
+    # device is an error code, not a crash
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    syms = declared_symbols()
+    src = tmp_path / "abi.c"
+    src.write_text("\n".join([
+        "#include <stdio.h>",
+        '#include "tok.h"',
+        "typedef void (*fn)(void);",
+        "static const fn entry[] = {" + ", ".join("(fn)%s" % s for s in syms) + "};",
+        "int main(void) {",
+        "  uint8_t bytes[256]; uint64_t off[257]; tok_handle* h = 0;",
+        "  for (int i = 0; i < 256; ++i) { bytes[i] = (uint8_t)i; off[i] = (uint64_t)i; }",
+        "  off[256] = 256;",
+        "  int rc = tok_load(bytes, off, 256, 0, 0, TOK_PAT_GPT2, &h);",
+        "  printf(\"%d %d\\n\", rc, (int)(sizeof entry / sizeof entry[0]));",
+        "  if (rc == TOK_OK) tok_free(h);",
+        "  return 0;",
+        "}",
+        ""]))
+    exe = tmp_path / "abi"
+    libdir = os.path.dirname(libpath)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-o", str(exe), "-L", libdir, "-ltokgb", "-Wl,-rpath," + libdir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    rc, n = (int(x) for x in r.stdout.split())
+    assert n == len(syms)
+    assert rc in (0, -4)  # TOK_OK with a device, TOK_ECUDA without one
