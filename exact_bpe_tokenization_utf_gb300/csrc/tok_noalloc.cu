@@ -36,12 +36,21 @@ __global__ void k_noalloc_status(const NoAllocScratch* s, uint32_t epoch, long l
   d_status[1] = eo;
 }
 
+// empty text: nothing to split, nothing malformed
+__global__ void k_noalloc_empty(long long* d_status) {
+  d_status[0] = TOK_OK;
+  d_status[1] = -1;
+}
+
 }  // namespace
 
 extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_text, uint64_t len,
                                               uint32_t* d_start_bits, int64_t* d_status, void* stream) {
   if (pattern_id != TOK_PAT_GPT2 && pattern_id != TOK_PAT_CL100K_STYLE) return TOK_EINVAL;
   if (!d_status || (len && (!d_text || !d_start_bits))) return TOK_EINVAL;
+  // the same bound as every other entry point: the chunk grid and the UTF-8
+  // error word hold positions below 2^34; checked before any device call
+  if (len > MAX_TEXT_BYTES) return TOK_EINVAL;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TOK_ECUDA;
   if (!g_scratch_addr[dev]) {
@@ -78,12 +87,7 @@ extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_t
     launch_boundaries(c, w, DevVocab{}, s);
     k_noalloc_status<<<1, 1, 0, s>>>(scratch, epoch, reinterpret_cast<long long*>(d_status));
   } else {
-    const long long ok[2] = {TOK_OK, -1};
-    if (cudaMemcpyAsync(d_status, ok, sizeof ok, cudaMemcpyHostToDevice, s) != cudaSuccess) {
-      cudaGetLastError();
-      return TOK_ECUDA;
-    }
-    if (cudaStreamSynchronize(s) != cudaSuccess) return TOK_ECUDA;
+    k_noalloc_empty<<<1, 1, 0, s>>>(reinterpret_cast<long long*>(d_status));
   }
   return cudaGetLastError() == cudaSuccess ? TOK_OK : TOK_ECUDA;
 }

@@ -11,9 +11,13 @@
  * encodes every fragment on its own with BPE merges in rank order (Section
  * 4.2).  No normaliser, special tokens, truncation or dropout (the
  * assumptions of Appendix A.1).  Output is an id array only, no byte offsets
- * (Section 4.4).  Section 4.3 packages the whole bytes -> ids chain with
- * pre-bucketed buffers so a request needs two host synchronisations; the
- * host entry points below follow that shape.
+ * (Section 4.4).  Section 4.3 packages the whole bytes -> ids chain so that
+ * a request needs two host synchronisations.  Here the chain is one memset
+ * and three kernel launches with no synchronisation between them, on a
+ * workspace that grows to the largest input seen and is then reused; a host
+ * request synchronises once when its output buffers are pinned (the device
+ * writes ids and status straight into them) and twice otherwise (status,
+ * then the id copy).
  *
  * Conventions for every function:
  *   - Return 0 (TOK_OK) or a negative TOK_E* code.  Nothing traps or aborts.
@@ -75,8 +79,10 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
              const uint32_t* merges, uint32_t n_merges, int pattern_id, tok_handle** out);
 
 /* tok_encode -- encode one text (host in, host out), Section 4.3's request:
- * copies text[0..len) to the device, runs the whole bytes -> ids chain on the
- * handle's stream and copies the ids back.
+ * runs the whole bytes -> ids chain on the handle's stream.  A pinned
+ * (page-locked) text is read by the first kernel in place, any other is
+ * copied to the device first; when ids is pinned and cap >= len the last
+ * kernel writes the ids straight into it, otherwise they are copied back.
  * ids: host array of capacity cap.  cap >= len always suffices (a token has
  *   at least one byte).  *n_ids receives the number of ids.
  * Errors: TOK_EUTF8 (tok_error_offset() = offset of the first malformed
@@ -199,8 +205,12 @@ int tok_pretokenize_batch(tok_handle* h, const uint8_t* const* texts, const uint
  * Enqueued on `stream` (NULL = the CUDA default stream) with no host sync.
  * Every call shares the one scratch array: calls that overlap on the GPU (on
  * different streams or devices' shared contexts) race and must be serialised
- * by the caller.
- * Errors: TOK_EINVAL, TOK_EBUF (len > 64 MiB), TOK_ECUDA.
+ * by the caller.  An empty text (len == 0) only writes d_status, also
+ * without a host sync.
+ * Errors (checked on the host before anything is enqueued): TOK_EINVAL
+ *   (NULL pointers, an unknown pattern, or len > 2^34 - 2, the bound of
+ *   every entry point), TOK_ECUDA (no device, the symbol lookup or a launch
+ *   failed).
  */
 int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_text, uint64_t len,
                                    uint32_t* d_start_bits, int64_t* d_status, void* stream);

@@ -13,14 +13,21 @@ def pretoken_byte_spans(data, pattern_id):
     return [(offs[a], offs[b]) for a, b in pretokenize(cps, pattern_id)]
 
 
-def encode(data, vocab, pattern_id, bpe=bpe_heap):
+def encode_with_spans(data, vocab, pattern_id, bpe=bpe_heap):
+    """(ids, fragment byte spans): the encoding and the pre-tokenizer's
+    fragments it was made from, from one pass of the pre-tokenizer."""
     data = bytes(data)
     ids = []
     mm = vocab.merge_map
     bid = vocab.byte_id
-    for a, b in pretoken_byte_spans(data, pattern_id):
+    spans = pretoken_byte_spans(data, pattern_id)
+    for a, b in spans:
         ids.extend(bpe([bid[x] for x in data[a:b]], mm))
-    return ids
+    return ids, spans
+
+
+def encode(data, vocab, pattern_id, bpe=bpe_heap):
+    return encode_with_spans(data, vocab, pattern_id, bpe)[0]
 
 
 def decode(ids, vocab):

@@ -25,3 +25,21 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def oracle_pool():
+    """The oracle on all host cores (worker processes started with spawn, so
+    it is safe to create after the GPU is in use)."""
+    from oracle_par import OraclePool
+    pool = OraclePool()
+    yield pool
+    pool.close()
+
+
+# every string of up to five code points over this alphabet goes through the
+# pre-tokenizer in the brute-force tests: letters (ASCII, contraction letters
+# in both cases, a 3-byte one), the apostrophe, numbers (ASCII and not), the
+# whitespace the patterns treat apart (space, tab, LF, CR, a 2-byte one) and
+# an ASCII symbol
+BRUTE_ALPHABET = ["a", "s", "S", "l", "'", "1", "²", " ", "\t", "\n", "\r", ".", "中", " "]

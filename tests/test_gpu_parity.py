@@ -1,11 +1,10 @@
 """GPU parity: the CUDA library through its C ABI against the oracle.
 
 Integer work, so the bar is bit-exact: every fragment start and every token
-id must equal the oracle's.  Full-size comparisons where the oracle finishes
-in seconds (the 16 KiB, 1 MiB and 1M-character workloads); at the batch and
-adversarial sizes, every fragment start of a scaled copy plus the full-size
-text's round trip, fixpoint property and a sample of fragments re-encoded by
-the oracle."""
+id must equal the oracle's, on every workload at its full size (the 16 KiB,
+1 MiB and 1M-character texts, all 64 items of the batch, the whole 8 MiB
+adversarial text under both patterns).  The large ones run the oracle on all
+host cores (tests/oracle_par.py)."""
 import itertools
 import os
 import random
@@ -14,8 +13,8 @@ import numpy as np
 import pytest
 
 import textgen
-from oracle.bpe import bpe_heap
-from oracle.encode import decode, encode, encode_with_offsets, pretoken_byte_spans
+from conftest import BRUTE_ALPHABET
+from oracle.encode import encode, encode_with_offsets, pretoken_byte_spans
 from oracle.repair import repair_append as oracle_repair_append
 from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2
 from oracle.utf8 import Utf8Error
@@ -70,8 +69,21 @@ def test_pretokenize_brute_force(pkg, pattern):
 
 
 @pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+def test_pretokenize_brute_force_five_code_points(pkg, oracle_pool, pattern):
+    # every string of 1..5 code points over the adversarial alphabet, in one
+    # batch call, against the oracle's fragment starts
+    tok = pkg.Tokenizer.from_merges([], pattern)
+    enc = ["".join(t).encode() for n in range(1, 6) for t in itertools.product(BRUTE_ALPHABET, repeat=n)]
+    want = oracle_pool.starts_many(enc, pattern)
+    got = tok.pretokenize_batch(enc)
+    assert len(got) == len(want)
+    bad = [(b, g, w) for b, g, w in zip(enc, got, want) if g != w]
+    assert not bad, bad[:5]
+
+
+@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
 def test_pretokenize_runs_across_chunks(pkg, pattern):
-    # runs far longer than a 4 KiB chunk: whitespace, digits, letters, CR/LF
+    # runs far longer than a 1 KiB chunk: whitespace, digits, letters, CR/LF
     tok = pkg.Tokenizer.from_merges([], pattern)
     text = textgen.adversarial(600_000, 1005, scale=0.05).encode()
     assert list(tok.pretokenize(text)) == oracle_starts(text, pattern)
@@ -144,11 +156,6 @@ def test_encode_session_1m_chars_100k_merges(pkg):
 
 
 # --- batch ---------------------------------------------------------------
-
-def _token_starts(ids, v):
-    lens = np.array([len(v.token_bytes[i]) for i in ids], dtype=np.int64)
-    return np.concatenate([[0], np.cumsum(lens)])
-
 
 def test_token_offsets_match_oracle(pkg):
     # the device's token byte offsets against the oracle's definition
@@ -251,21 +258,18 @@ def test_repair_append_matches_full_encoding(pkg):
             assert re == o_re
 
 
-def test_encode_batch_64_sessions(pkg):
+def test_encode_batch_64_sessions(pkg, oracle_pool):
+    # the 64-session batch in one tok_encode_batch call: every item's ids
+    # against the oracle's
     v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
     items = [s.encode() for s in textgen.session_batch(64, 1004)]
     ids, off = tok.encode_batch(items)
     assert off[0] == 0 and off[-1] == len(ids) and np.all(np.diff(off) >= 0)
-    rnd = random.Random(4)
-    order = sorted(range(64), key=lambda k: len(items[k]))
-    check = set(order[:8]) | set(rnd.sample(range(64), 3))
+    want = oracle_pool.encode_many(items, os.path.join(VOC, "cl100k_session_100k.merges"), PATTERN_CL100K)
     for k, it in enumerate(items):
-        got = ids[off[k]:off[k + 1]].tolist()
-        assert decode(got, v) == it
-        if k in check:
-            assert got == encode(it, v, PATTERN_CL100K), k
+        assert ids[off[k]:off[k + 1]].tolist() == want[k][0], k
     # batch == singles
-    for k in list(check)[:4]:
+    for k in (0, 17, 63):
         assert tok.encode(items[k]).tolist() == ids[off[k]:off[k + 1]].tolist()
 
 
@@ -285,25 +289,18 @@ def test_adversarial_scaled_exact(pkg, name, pattern):
 
 @pytest.mark.parametrize("name,pattern", [("gpt2_session_100k", PATTERN_GPT2),
                                           ("cl100k_session_100k", PATTERN_CL100K)])
-def test_adversarial_8mib_sampled(pkg, name, pattern):
+def test_adversarial_8mib_exact(pkg, oracle_pool, name, pattern):
+    # the whole 8 MiB adversarial text: every fragment start of the
+    # pre-tokenizer and every id, against the oracle
     v, tok = pair(pkg, name, pattern)
     data = textgen.adversarial(8 << 20, 1005).encode()
+    want_ids, want_starts = oracle_pool.encode_long(data, os.path.join(VOC, name + ".merges"), pattern)
+    starts = tok.pretokenize(data).tolist()
+    assert len(starts) == len(want_starts)
+    assert starts == want_starts
     ids = tok.encode(data).tolist()
-    assert decode(ids, v) == data
-    starts = tok.pretokenize(data)
-    ends = np.append(starts[1:], len(data))
-    tstart = _token_starts(ids, v)
-    pos = {int(p): k for k, p in enumerate(tstart)}
-    # every fragment start is a token start; a fragment's tokens are BPE(fragment)
-    lens = ends - starts
-    rnd = random.Random(pattern)
-    idx = set(np.argsort(lens)[-6:].tolist()) | set(rnd.sample(range(len(starts)), 300))
-    for k in idx:
-        a, b = int(starts[k]), int(ends[k])
-        assert a in pos and b in pos
-        got = ids[pos[a]:pos[b]]
-        want = bpe_heap([v.byte_id[x] for x in data[a:b]], v.merge_map)
-        assert got == want, (k, a, b)
+    assert len(ids) == len(want_ids)
+    assert ids == want_ids
 
 
 # --- edge cases ------------------------------------------------------------

@@ -124,3 +124,28 @@ def test_committed_small_vocab_reproduces():
     ids = encode(data, v, PATTERN_GPT2)
     assert decode(ids, v) == data and len(ids) < len(data) // 2
     assert ids == encode(data, v, PATTERN_GPT2, bpe=bpe_heap)
+
+
+def test_windowed_oracle_equals_whole_text(small_vocab):
+    # the full-size parity tests run the oracle window by window, cut at
+    # certified cuts (tests/oracle_par.py); on texts the oracle finishes in
+    # seconds the windows' ids and shifted fragment starts equal the whole
+    # text's, for both patterns, including a window that is one long run
+    from oracle.encode import encode_with_spans
+    from oracle_par import is_cut, windows
+    v = small_vocab
+    texts = [textgen.adversarial(300_000, 1005, scale=0.02).encode(), textgen.agentic_session(60_000, 8).encode(),
+             b"abc" * 5000 + b".x" + b"9" * 7000 + b"-" + "é".encode() * 900 + b"a's'" + b"q" * 3000]
+    for data in texts:
+        cuts = windows(data, 4096)
+        assert len(cuts) > 3 and cuts[0] == 0 and cuts[-1] == len(data)
+        assert all(is_cut(data, c) for c in cuts[1:-1])
+        for pat in (PATTERN_GPT2, PATTERN_CL100K):
+            ids, spans = encode_with_spans(data, v, pat)
+            got_ids, got_starts = [], []
+            for a, b in zip(cuts, cuts[1:]):
+                i, s = encode_with_spans(data[a:b], v, pat)
+                got_ids += i
+                got_starts += [a + x for x, _ in s]
+            assert got_ids == ids
+            assert got_starts == [x for x, _ in spans]

@@ -66,6 +66,23 @@ def test_brute_force_against_regex_module():
         assert split(s, PATTERN_CL100K) == rc.findall(s), repr(s)
 
 
+def test_brute_force_five_code_points_against_regex_module(oracle_pool):
+    # every string of 1..5 code points over the adversarial alphabet (about
+    # 580,000 strings), the oracle on all host cores
+    regex = pytest.importorskip("regex")
+    from conftest import BRUTE_ALPHABET
+    strs = ["".join(t) for n in range(1, 6) for t in itertools.product(BRUTE_ALPHABET, repeat=n)]
+    enc = [s.encode() for s in strs]
+    for pat, rx in ((PATTERN_GPT2, regex.compile(GPT2_RE)), (PATTERN_CL100K, regex.compile(CL100K_RE))):
+        got = oracle_pool.starts_many(enc, pat)
+        for s, g in zip(strs, got):
+            want, pos = [], 0
+            for m in rx.findall(s):
+                want.append(pos)
+                pos += len(m.encode())
+            assert g == want, repr(s)
+
+
 def test_generated_text_against_regex_module():
     regex = pytest.importorskip("regex")
     rg, rc = regex.compile(GPT2_RE), regex.compile(CL100K_RE)
