@@ -72,6 +72,9 @@ struct tok_handle {
   cudaEvent_t ev[N_STAGES + 1] = {};
   float stage_ms[N_STAGES] = {};
   bool have_times = false;
+  // test hook (tok_debug_fail_alloc): the allocation that fails, counted
+  // from 1 = the next one; 0 = none
+  uint32_t fail_alloc_in = 0;
 };
 
 namespace {
@@ -114,6 +117,32 @@ cudaError_t dalloc(T** p, size_t count) {
   return cudaMalloc(reinterpret_cast<void**>(p), std::max<size_t>(count, 1) * sizeof(T));
 }
 
+// true when the handle's failure hook says this allocation is the one that
+// fails (it then stands in for a cudaMalloc that found the device full)
+bool injected_failure(tok_handle* h) {
+  return h->fail_alloc_in > 0 && --h->fail_alloc_in == 0;
+}
+
+// device allocation of a handle's buffers (workspace, items, offsets)
+template <class T>
+cudaError_t halloc(tok_handle* h, T** p, size_t count) {
+  if (injected_failure(h)) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return dalloc(p, count);
+}
+
+// pinned host allocation of a handle's buffers
+template <class T>
+cudaError_t halloc_pinned(tok_handle* h, T** p, size_t count) {
+  if (injected_failure(h)) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMallocHost(reinterpret_cast<void**>(p), std::max<size_t>(count, 1) * sizeof(T));
+}
+
 void free_workspace(tok_handle* h) {
   Workspace& w = h->ws;
   // (the group totals live in the status allocation)
@@ -141,37 +170,37 @@ int ensure_workspace(tok_handle* h, uint64_t n) {
   const uint64_t pad = 256;
   cudaError_t e = cudaSuccess;
   auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
-  chk(dalloc(&w.text, cap + pad));
-  chk(dalloc(&w.pstart, cap / 32 + pad));
-  chk(dalloc(&w.tok, cap + pad));
+  chk(halloc(h, &w.text, cap + pad));
+  chk(halloc(h, &w.pstart, cap / 32 + pad));
+  chk(halloc(h, &w.tok, cap + pad));
   // queue sizes: a queued short fragment has >= 2 bytes (a single byte always
   // settles), a warp batch >= 1 short fragment, a wide fragment > SB_MAX
   // bytes, a long one > B_CAP bytes (plus at most one of unknown length per
   // chunk)
-  chk(dalloc(&w.fcnt, cap + pad));
-  chk(dalloc(&w.sfrag, cap / 2 + nbch + pad));
-  chk(dalloc(&w.sbatch, cap / 2 + nbch + pad));
-  chk(dalloc(&w.wq, cap / (SB_MAX + 1) + nbch + pad));
-  chk(dalloc(&w.longq, cap / (B_CAP + 1) + nbch + pad));
+  chk(halloc(h, &w.fcnt, cap + pad));
+  chk(halloc(h, &w.sfrag, cap / 2 + nbch + pad));
+  chk(halloc(h, &w.sbatch, cap / 2 + nbch + pad));
+  chk(halloc(h, &w.wq, cap / (SB_MAX + 1) + nbch + pad));
+  chk(halloc(h, &w.longq, cap / (B_CAP + 1) + nbch + pad));
   // the status, the group totals, the chunk totals (the group and chunk
   // totals live in the status allocation): the part cleared before a call is
   // one range
   {
     uint8_t* p = nullptr;
-    chk(dalloc(&p, sizeof(DevStatus) + (gtot_cap(nbch) + nbch + 2) * sizeof(uint32_t)));
+    chk(halloc(h, &p, sizeof(DevStatus) + (gtot_cap(nbch) + nbch + 2) * sizeof(uint32_t)));
     w.st = reinterpret_cast<DevStatus*>(p);
     w.gtot = p ? reinterpret_cast<uint32_t*>(p + sizeof(DevStatus)) : nullptr;
     w.ctot = p ? w.gtot + gtot_cap(nbch) : nullptr;
   }
-  chk(dalloc(&w.edge, nch + 2));
+  chk(halloc(h, &w.edge, nch + 2));
   for (int b = 0; b < 2; ++b) {
-    chk(dalloc(&w.e_sym[b], cap + pad));
-    chk(dalloc(&w.e_len[b], cap + pad));
-    chk(dalloc(&w.e_kr[b], cap + pad));
+    chk(halloc(h, &w.e_sym[b], cap + pad));
+    chk(halloc(h, &w.e_len[b], cap + pad));
+    chk(halloc(h, &w.e_kr[b], cap + pad));
   }
-  chk(dalloc(&w.e_fl, cap + pad));
-  chk(dalloc(&w.e_rs, cap + pad));
-  chk(dalloc(&h->d_out, cap + pad));
+  chk(halloc(h, &w.e_fl, cap + pad));
+  chk(halloc(h, &w.e_rs, cap + pad));
+  chk(halloc(h, &h->d_out, cap + pad));
   if (e == cudaSuccess) e = cudaMemset(w.pstart, 0, (cap / 32 + pad) * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(w.st, 0, sizeof(DevStatus));
   if (e == cudaSuccess) e = cudaMemset(w.edge, 0, (nch + 2) * sizeof(unsigned long long));
@@ -192,11 +221,15 @@ int ensure_items(tok_handle* h, uint64_t n_items) {
   if (h->d_item_off) cudaFree(h->d_item_off);
   if (h->h_items) cudaFreeHost(h->h_items);
   h->d_items = nullptr; h->d_item_off = nullptr; h->h_items = nullptr;
-  cudaError_t e = dalloc(&h->d_items, cap);
-  if (e == cudaSuccess) e = dalloc(&h->d_item_off, cap);
-  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&h->h_items), cap * sizeof(long long));
+  cudaError_t e = halloc(h, &h->d_items, cap);
+  if (e == cudaSuccess) e = halloc(h, &h->d_item_off, cap);
+  if (e == cudaSuccess) e = halloc_pinned(h, &h->h_items, cap);
   if (e != cudaSuccess) {
     cudaGetLastError();
+    if (h->d_items) cudaFree(h->d_items);
+    if (h->d_item_off) cudaFree(h->d_item_off);
+    if (h->h_items) cudaFreeHost(h->h_items);
+    h->d_items = nullptr; h->d_item_off = nullptr; h->h_items = nullptr;
     h->cap_items = h->cap_h_items = 0;
     return fail(h, TOK_ENOMEM, "item buffer allocation failed");
   }
@@ -562,6 +595,12 @@ uint64_t tok_content_hash(tok_handle* h) { return h ? h->hash : 0; }
 
 uint64_t tok_launch_count(tok_handle* h) { return h ? h->launches : 0; }
 
+int tok_debug_fail_alloc(tok_handle* h, uint32_t k) {
+  if (!h) return TOK_EINVAL;
+  h->fail_alloc_in = k;
+  return TOK_OK;
+}
+
 int tok_set_timing(tok_handle* h, int enable) {
   if (!h) return TOK_EINVAL;
   h->timing = enable != 0;
@@ -605,7 +644,7 @@ int encode_host(tok_handle* h, const uint8_t* text, uint64_t len, int32_t* ids, 
   int rc = ensure_workspace(h, len);
   if (rc) return rc;
   if (offsets && !h->d_off) {
-    const cudaError_t e = dalloc(&h->d_off, h->ws.cap_bytes + 256);
+    const cudaError_t e = halloc(h, &h->d_off, h->ws.cap_bytes + 256);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return fail(h, TOK_ENOMEM, "offset buffer allocation failed");
@@ -695,7 +734,12 @@ int tok_repair_append(tok_handle* h, const uint8_t* text, uint64_t old_len, uint
   if (p && (k >= old_n || (uint64_t)old_offsets[k] != p))
     return fail(h, TOK_EINVAL, "the old token offsets do not belong to this text");
   if (k > cap) {
-    *n_ids = k;
+    // the kept tokens alone overflow: the required size still counts the
+    // tail's tokens (encoded with no room, which reports their number)
+    uint64_t m = 0;
+    const int rc = encode_host(h, text + p, len - p, nullptr, nullptr, 0, &m);
+    if (rc != TOK_OK && rc != TOK_EBUF) return rc;
+    *n_ids = k + m;
     return fail(h, TOK_EBUF, "output buffer too small");
   }
   if (ids != old_ids) std::copy(old_ids, old_ids + k, ids);

@@ -134,7 +134,8 @@ int tok_repair_append(tok_handle* h, const uint8_t* text, uint64_t old_len, uint
  *   the items' ids back to back; item_off: host array of n+1 entries, item k's
  *   ids are ids[item_off[k] .. item_off[k+1]).
  * Errors: as tok_encode; TOK_EUTF8 reports the offset within the
- *   concatenation of all items.
+ *   concatenation of all items; on TOK_EBUF item_off[n] = the required
+ *   capacity.
  */
 int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t* lens, uint32_t n,
                      int32_t* ids, uint64_t cap, uint64_t* item_off);
@@ -237,6 +238,15 @@ int tok_stage_times(tok_handle* h, float* ms, const char** names, int cap);
 
 /* tok_launch_count -- number of kernels this handle has launched so far. */
 uint64_t tok_launch_count(tok_handle* h);
+
+/* tok_debug_fail_alloc -- test hook for the out-of-memory paths: the k-th
+ * device or pinned host allocation that h makes from now on (k >= 1: the
+ * workspace, item and offset buffers that calls grow on demand) fails the way
+ * cudaMalloc does when the device is full, without being attempted; k = 0
+ * disarms the hook.  The call that meets it returns TOK_ENOMEM, frees what it
+ * had allocated, and leaves h usable.  Host-side bookkeeping only.
+ * Errors: TOK_EINVAL (h is NULL). */
+int tok_debug_fail_alloc(tok_handle* h, uint32_t k);
 
 /* tok_free -- release the handle and its device memory.  NULL is ignored. */
 void tok_free(tok_handle* h);
