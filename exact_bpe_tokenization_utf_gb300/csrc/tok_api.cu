@@ -49,6 +49,7 @@ struct tok_handle {
   uint8_t* d_vocab_bytes = nullptr;
   uint64_t vocab_bytes_len = 0;
   uint32_t* d_vocab_off = nullptr;
+  uint32_t* d_pair_bits = nullptr;
   uint32_t n_whole = 0;
   uint64_t hash = 0;
   // workspace
@@ -448,6 +449,21 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
     first_used[a] = std::min<int64_t>(first_used[a], r);
     first_used[b] = std::min<int64_t>(first_used[b], r);
   }
+  // byte pairs held by some merge result: no merge crosses any other pair
+  std::vector<uint32_t> pair_bits(2048, 0u);
+  {
+    std::vector<uint8_t> is_result(n_vocab, 0);
+    for (uint32_t i = 0; i <= mask; ++i)
+      if (table[i].key != EMPTY_KEY) is_result[table[i].result] = 1;
+    for (uint32_t t = 0; t < n_vocab; ++t) {
+      if (!is_result[t]) continue;
+      const uint8_t* tb = vocab_bytes + vocab_off[t];
+      for (uint32_t j = 0; j + 1 < tok_len[t]; ++j) {
+        const uint32_t pi = ((uint32_t)tb[j] << 8) | tb[j + 1];
+        pair_bits[pi >> 5] |= 1u << (pi & 31);
+      }
+    }
+  }
   bool monotone = true;
   for (uint32_t t = 0; t < n_vocab && monotone; ++t)
     if (last_made[t] >= 0 && first_used[t] != INT64_MAX && first_used[t] <= last_made[t]) monotone = false;
@@ -519,6 +535,9 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   if (e == cudaSuccess) e = dalloc(&h->d_vocab_bytes, off32[n_vocab] + 16);
   h->vocab_bytes_len = off32[n_vocab];
   if (e == cudaSuccess) e = dalloc(&h->d_vocab_off, n_vocab + 1);
+  if (e == cudaSuccess) e = dalloc(&h->d_pair_bits, pair_bits.size());
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->d_pair_bits, pair_bits.data(), pair_bits.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_whole, whole.data(), whole.size() * sizeof(WholeEntry), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
@@ -555,6 +574,7 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   h->v.max_tok_len = max_tok_len;
   h->v.vocab_bytes = h->d_vocab_bytes;
   h->v.vocab_off = h->d_vocab_off;
+  h->v.pair_bits = h->d_pair_bits;
   h->n_whole = (uint32_t)whole_tokens.size();
   uint64_t hh = 1469598103934665603ull;
   hh = fnv1a(hh, &pattern_id, sizeof pattern_id);
@@ -574,8 +594,8 @@ void tok_free(tok_handle* h) {
   DeviceGuard g(h->dev);
   if (h->stream) cudaStreamSynchronize(h->stream);
   free_workspace(h);
-  void* ptrs[] = {h->d_table,  h->d_byte_id,     h->d_tok_len,     h->d_max_left, h->d_max_right,
-                  h->d_whole,  h->d_vocab_bytes, h->d_vocab_off,   h->d_items,    h->d_item_off};
+  void* ptrs[] = {h->d_table,  h->d_byte_id,     h->d_tok_len,   h->d_max_left, h->d_max_right, h->d_whole,
+                  h->d_vocab_bytes, h->d_vocab_off, h->d_pair_bits, h->d_items, h->d_item_off};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_status) cudaFreeHost(h->h_status);

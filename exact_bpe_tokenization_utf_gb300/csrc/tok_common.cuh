@@ -84,6 +84,11 @@ struct DevVocab {
   const uint16_t* max_left;   // longest left operand of any merge whose right operand is t
   const uint16_t* max_right;  // longest right operand of any merge whose left operand is t
   int monotone;               // every merge that uses a token comes after every merge making it
+  // 65,536 bits: bit (x << 8 | y) is set when some merge result's bytes hold
+  // the byte pair x y; no merge joins two symbols across a pair whose bit is
+  // clear (the result would hold it), so a fragment splits there into
+  // pieces that encode independently
+  const uint32_t* pair_bits;
 };
 
 // a queued fragment: its first byte and its length (-1: ends at the next

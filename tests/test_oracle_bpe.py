@@ -129,3 +129,56 @@ def test_decode_roundtrip_and_vocab_checks():
         Vocab([bytes([b]) for b in range(256)], [(97, 97), (97, 97)])
     with pytest.raises(VocabError):
         Vocab([bytes([b]) for b in range(256)], [(97, 98)])  # result bytes missing
+
+
+def _pair_barriers(word_bytes, vocab):
+    """Positions i (0 < i < len) such that no merge result's bytes contain the
+    byte pair (word[i-1], word[i])."""
+    held = set()
+    for _, res in vocab.merge_map.values():
+        t = vocab.token_bytes[res]
+        held.update(zip(t, t[1:]))
+    return [i for i in range(1, len(word_bytes)) if (word_bytes[i - 1], word_bytes[i]) not in held]
+
+
+def test_words_split_exactly_where_no_merge_result_holds_the_byte_pair():
+    # A merge that joins symbols across the boundary between bytes i-1 and i
+    # makes a token whose bytes contain that pair; where no merge result
+    # contains it, no merge ever crosses i, the two sides evolve apart, and
+    # BPE of the word is the concatenation of BPE of its pieces (any vocabulary,
+    # monotone or not).  The library splits long fragments there.
+    rnd = random.Random(21)
+    n_split = 0
+    for trial in range(300):
+        v = _random_vocab(rnd, "abcd", rnd.randint(1, 30))
+        for _ in range(20):
+            w = bytes(rnd.choice(b"abcd") for _ in range(rnd.randint(0, 30)))
+            cuts = [0] + _pair_barriers(w, v) + [len(w)]
+            n_split += len(cuts) > 2
+            whole = bpe_textbook([v.byte_id[x] for x in w], v.merge_map)
+            parts = []
+            for a, b in zip(cuts, cuts[1:]):
+                parts += bpe_textbook([v.byte_id[x] for x in w[a:b]], v.merge_map)
+            assert parts == whole, (w, cuts)
+    assert n_split > 1000
+    # a cut where the pair does occur in a merge result is not safe: pipe|line
+    v, idx = _vocab_from_strings([("p", "i"), ("p", "e"), ("pi", "pe"), ("l", "i"), ("n", "e"), ("li", "ne"),
+                                  ("pipe", "line")])
+    w = b"pipeline"
+    assert 4 not in _pair_barriers(w, v)
+    assert bpe_textbook(list(w), v.merge_map) == [idx[b"pipeline"]]
+
+
+def test_pair_barriers_on_a_trained_vocabulary_and_a_long_letter_run():
+    import os
+    import textgen
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    v = Vocab.load_merges(os.path.join(root, "data", "vocabs", "cl100k_session_100k.merges"))
+    run = [p for p in textgen.adversarial_pieces(1005, scale=0.004) if p.isalpha() or p[:-1].isalpha()]
+    w = max(run, key=len).strip().encode()
+    cuts = [0] + _pair_barriers(w, v) + [len(w)]
+    assert len(cuts) > 20
+    parts = []
+    for a, b in zip(cuts, cuts[1:]):
+        parts += bpe_heap([v.byte_id[x] for x in w[a:b]], v.merge_map)
+    assert parts == bpe_heap([v.byte_id[x] for x in w], v.merge_map)
