@@ -25,6 +25,8 @@ LIB_PATH = os.path.join(HERE, "_lib", "libtokgb.so")
 
 PATTERN_GPT2 = 0
 PATTERN_CL100K = 1
+PATTERN_O200K = 2
+IGNORE_MERGES = 0x100   # flag ORed into the pattern id (tok.h TOK_IGNORE_MERGES)
 
 TOK_OK, TOK_EINVAL, TOK_EUTF8, TOK_ENOMEM, TOK_ECUDA, TOK_EBUF, TOK_ETIMEOUT, TOK_EMERGES = 0, -1, -2, -3, -4, -5, -6, -7
 _NAMES = {0: "TOK_OK", -1: "TOK_EINVAL", -2: "TOK_EUTF8", -3: "TOK_ENOMEM", -4: "TOK_ECUDA", -5: "TOK_EBUF",
@@ -129,7 +131,7 @@ def _u8(buf):
 class Tokenizer:
     """One tokenizer on the current CUDA device (a tok_handle)."""
 
-    def __init__(self, token_bytes, merges, pattern):
+    def __init__(self, token_bytes, merges, pattern, ignore_merges=False):
         L = lib()
         self._L = L
         offs = np.zeros(len(token_bytes) + 1, dtype=np.uint64)
@@ -139,22 +141,23 @@ class Tokenizer:
         h = ctypes.c_void_p()
         rc = L.tok_load(blob.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
                         offs.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)), len(token_bytes),
-                        m.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), m.shape[0], int(pattern),
-                        ctypes.byref(h))
+                        m.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), m.shape[0],
+                        int(pattern) | (IGNORE_MERGES if ignore_merges else 0), ctypes.byref(h))
         if rc != TOK_OK:
             raise TokError(rc, L.tok_last_error(None).decode())
         self._h = h
         self.pattern = int(pattern)
+        self.ignore_merges = bool(ignore_merges)
         self.n_vocab = len(token_bytes)
         self.token_bytes = token_bytes
 
     @classmethod
-    def from_merges(cls, merges, pattern):
-        return cls(tokens_from_merges(merges), merges, pattern)
+    def from_merges(cls, merges, pattern, ignore_merges=False):
+        return cls(tokens_from_merges(merges), merges, pattern, ignore_merges)
 
     @classmethod
-    def from_merges_file(cls, path, pattern):
-        return cls.from_merges(read_merges_file(path), pattern)
+    def from_merges_file(cls, path, pattern, ignore_merges=False):
+        return cls.from_merges(read_merges_file(path), pattern, ignore_merges)
 
     def _check(self, rc):
         if rc != TOK_OK:

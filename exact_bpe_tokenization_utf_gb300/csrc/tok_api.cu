@@ -329,12 +329,14 @@ Call base_call(tok_handle* h, const uint8_t* d_text, uint64_t n) {
 // ---------------------------------------------------------------------------
 // Session repair after an append (Section 3.3; Appendix A.2's splice theorem).
 // The cut p is the last position inside the old text whose previous code
-// point is a letter or a number and whose own code point has another class.
-// Every alternative of both patterns that consumes letters or numbers matches
-// a maximal run of them, so the match covering p - 1 ends at p whatever
-// follows; the fragments before p depend on the text up to the code point at
-// p, and (no pattern looks behind) the fragments from p on only on the text
-// from p on.  So the old tokens before p stay, and text[p:] is encoded anew.
+// point is a letter or a number and whose own code point has another class
+// and is not an apostrophe.  Every alternative of the patterns that consumes
+// letters or numbers ends at the end of a run of them (or inside it), or
+// after a contraction that begins with an apostrophe, so the match covering
+// p - 1 ends at p whatever follows; the fragments before p depend on the text
+// up to the code point at p, and (no pattern looks behind) the fragments
+// from p on only on the text from p on.  So the old tokens before p stay, and
+// text[p:] is encoded anew.
 
 namespace hostucd {
 #define TOK_UCD_QUAL static const
@@ -381,7 +383,9 @@ uint64_t last_cut(const uint8_t* old, uint64_t n, uint64_t limit) {
     uint64_t j = k - 1;  // start of the code point before k
     while (j > 0 && (old[j] & 0xC0u) == 0x80u && k - j < 4) --j;
     const uint32_t c = host_class_at(old, n, j);
-    if (cur >= 0 && (c == CLS_L || c == CLS_N) && cur_cls != c) return (uint64_t)cur;
+    // (an apostrophe after a word may begin a contraction that the
+    // o200k-style pattern attaches to the word, so it is never a cut)
+    if (cur >= 0 && (c == CLS_L || c == CLS_N) && cur_cls != c && old[cur] != 0x27u) return (uint64_t)cur;
     cur = (long long)j;
     cur_cls = c;
     k = j;
@@ -397,7 +401,9 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
              uint32_t n_merges, int pattern_id, tok_handle** out) {
   if (!out) return fail(nullptr, TOK_EINVAL, "out is NULL");
   *out = nullptr;
-  if (pattern_id != TOK_PAT_GPT2 && pattern_id != TOK_PAT_CL100K_STYLE)
+  const bool ignore_merges = (pattern_id & TOK_IGNORE_MERGES) != 0;
+  const int pattern = pattern_id & ~TOK_IGNORE_MERGES;
+  if (pattern != TOK_PAT_GPT2 && pattern != TOK_PAT_CL100K_STYLE && pattern != TOK_PAT_O200K_STYLE)
     return fail(nullptr, TOK_EINVAL, "unknown pattern id");
   if (!vocab_bytes || !vocab_off || (n_merges && !merges)) return fail(nullptr, TOK_EINVAL, "NULL vocabulary");
   if (n_vocab < 256 || n_vocab >= (1u << 20)) return fail(nullptr, TOK_EMERGES, "n_vocab out of range");
@@ -498,7 +504,7 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
         sy[bi] = br;
         sy.erase(sy.begin() + bi + 1);
       }
-      if (sy.size() == 1 && sy[0] == t) whole_tokens.push_back(t);
+      if (ignore_merges || (sy.size() == 1 && sy[0] == t)) whole_tokens.push_back(t);
     }
   }
   uint32_t wbits = 10;
@@ -512,7 +518,14 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   for (uint32_t t : whole_tokens) {
     // entries carry the first 8 bytes, the offset and the length: a probe
     // of a longer token needs one more load to compare the rest
-    if (tok_len[t] > 255 || off32[t] >= (1u << 24)) continue;
+    if (tok_len[t] > 255 || off32[t] >= (1u << 24)) {
+      // without the flag the table only saves work, so a token it cannot
+      // hold is encoded by the merge loop instead; with the flag every token
+      // must be found
+      if (ignore_merges)
+        return fail(nullptr, TOK_EMERGES, "ignore_merges needs tokens of at most 255 bytes in the first 16 MiB");
+      continue;
+    }
     const uint8_t* tb = vocab_bytes + vocab_off[t];
     const unsigned long long head = bytes_head(tb, tok_len[t]);
     const unsigned long long hv = bytes_hash(head, tb, tok_len[t]);
@@ -522,7 +535,7 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   }
 
   tok_handle* h = new tok_handle();
-  h->pattern = pattern_id;
+  h->pattern = pattern;
   cudaError_t e = cudaGetDevice(&h->dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sms, cudaDevAttrMultiProcessorCount, h->dev);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking);
@@ -574,7 +587,9 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   h->v.max_tok_len = max_tok_len;
   h->v.vocab_bytes = h->d_vocab_bytes;
   h->v.vocab_off = h->d_vocab_off;
-  h->v.pair_bits = h->d_pair_bits;
+  // with ignore_merges a whole fragment that is any token is that token, so
+  // fragments are never split into pieces (a piece may not take that rule)
+  h->v.pair_bits = ignore_merges ? nullptr : h->d_pair_bits;
   h->n_whole = (uint32_t)whole_tokens.size();
   uint64_t hh = 1469598103934665603ull;
   hh = fnv1a(hh, &pattern_id, sizeof pattern_id);

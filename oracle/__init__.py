@@ -13,9 +13,10 @@ E encodes every fragment with BPE on its own, with no state shared across
 fragments.  Sections 3.2 and 4.1 of the same page name the GPT-style
 regex pre-tokenizer and its character classes; Section 4.2 names the
 per-fragment BPE.  The pages print neither pattern nor a BPE listing, so
-the two patterns below are the GPT-2 and cl100k-style patterns written out
-as the configurations name them, and BPE is the textbook rule: repeatedly
-merge the lowest-rank adjacent pair, leftmost first.
+the patterns are the GPT-2 and cl100k-style patterns written out as the
+configurations name them, plus an o200k-style pattern of this project's own
+definition, and BPE is the textbook rule: repeatedly merge the lowest-rank
+adjacent pair, leftmost first.
 
 Modules
   utf8        strict RFC 3629 decoding with the offset of the first bad byte
@@ -31,7 +32,7 @@ Parity pins live in tests/test_oracle_*.py.
 """
 from .utf8 import Utf8Error, decode_utf8  # noqa: F401
 from .ucd import classify, class_array  # noqa: F401
-from .pretokenize import pretokenize, PATTERN_GPT2, PATTERN_CL100K  # noqa: F401
+from .pretokenize import pretokenize, PATTERN_GPT2, PATTERN_CL100K, PATTERN_O200K  # noqa: F401
 from .bpe import bpe_textbook, bpe_rounds, bpe_heap  # noqa: F401
 from .vocab import Vocab  # noqa: F401
 from .encode import encode, decode, pretoken_byte_spans  # noqa: F401

@@ -13,21 +13,30 @@ def pretoken_byte_spans(data, pattern_id):
     return [(offs[a], offs[b]) for a, b in pretokenize(cps, pattern_id)]
 
 
-def encode_with_spans(data, vocab, pattern_id, bpe=bpe_heap):
+def encode_with_spans(data, vocab, pattern_id, bpe=bpe_heap, ignore_merges=False):
     """(ids, fragment byte spans): the encoding and the pre-tokenizer's
-    fragments it was made from, from one pass of the pre-tokenizer."""
+    fragments it was made from, from one pass of the pre-tokenizer.
+
+    ignore_merges: a fragment whose bytes are a token of the vocabulary is
+    that token, without BPE (TokTier, Section 4.2: the whole-word lookup of
+    Llama-style tokenizers, `ignore_merges`); other fragments go through BPE
+    as usual."""
     data = bytes(data)
     ids = []
     mm = vocab.merge_map
     bid = vocab.byte_id
     spans = pretoken_byte_spans(data, pattern_id)
     for a, b in spans:
-        ids.extend(bpe([bid[x] for x in data[a:b]], mm))
+        frag = data[a:b]
+        if ignore_merges and frag in vocab.index:
+            ids.append(vocab.index[frag])
+        else:
+            ids.extend(bpe([bid[x] for x in frag], mm))
     return ids, spans
 
 
-def encode(data, vocab, pattern_id, bpe=bpe_heap):
-    return encode_with_spans(data, vocab, pattern_id, bpe)[0]
+def encode(data, vocab, pattern_id, bpe=bpe_heap, ignore_merges=False):
+    return encode_with_spans(data, vocab, pattern_id, bpe, ignore_merges)[0]
 
 
 def decode(ids, vocab):
@@ -45,7 +54,7 @@ def token_offsets(ids, vocab):
     return out
 
 
-def encode_with_offsets(data, vocab, pattern_id, bpe=bpe_heap):
-    ids = encode(data, vocab, pattern_id, bpe)
+def encode_with_offsets(data, vocab, pattern_id, bpe=bpe_heap, ignore_merges=False):
+    ids = encode(data, vocab, pattern_id, bpe, ignore_merges)
     return ids, token_offsets(ids, vocab)
 

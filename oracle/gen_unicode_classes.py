@@ -38,6 +38,27 @@ def main(out_path):
     print(len(ranges), "ranges ->", out_path)
 
 
+def main_upper(out_path):
+    """Ranges of the upper-case letters \\p{Lu} and title-case letters
+    \\p{Lt} (the o200k-style pattern's upper-case set)."""
+    pu = regex.compile(r"[\p{Lu}\p{Lt}]")
+    ranges = []
+    start = None
+    for cp in range(0x110000 + 1):
+        up = cp < 0x110000 and not (0xD800 <= cp <= 0xDFFF) and bool(pu.match(chr(cp)))
+        if up and start is None:
+            start = cp
+        elif not up and start is not None:
+            ranges.append((start, cp - 1))
+            start = None
+    with open(out_path, "w") as f:
+        f.write("# regex %s; code point ranges of \\p{Lu} and \\p{Lt} (inclusive, hex)\n" % regex.__version__)
+        for a, b in ranges:
+            f.write("%04X %04X\n" % (a, b))
+    print(len(ranges), "ranges ->", out_path)
+
+
 if __name__ == "__main__":
-    main(sys.argv[1] if len(sys.argv) > 1 else
-         os.path.join(os.path.dirname(os.path.abspath(__file__)), "data", "unicode_classes.txt"))
+    data = os.path.join(os.path.dirname(os.path.abspath(__file__)), "data")
+    main(sys.argv[1] if len(sys.argv) > 1 else os.path.join(data, "unicode_classes.txt"))
+    main_upper(sys.argv[2] if len(sys.argv) > 2 else os.path.join(data, "unicode_upper.txt"))

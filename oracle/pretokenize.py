@@ -2,11 +2,11 @@
 left to right (TokTier, Sections 3.2 and 4.1: the serial regex pass whose
 every match start depends on where the previous match ended).
 
-The pages name the tokenizer families but print no pattern.  The two
-patterns here are the GPT-2 pattern and the cl100k-style pattern (case-
-insensitive contractions, digit groups of at most three, newline-aware
-whitespace), written as ASTs for regex_engine in the same order as their
-usual regex text:
+The pages name the tokenizer families but print no pattern.  The patterns
+here are the GPT-2 pattern, the cl100k-style pattern (case-insensitive
+contractions, digit groups of at most three, newline-aware whitespace) and an
+o200k-style pattern, written as ASTs for regex_engine in the same order as
+their regex text:
 
 GPT-2:
   's|'t|'re|'ve|'m|'ll|'d| ?\\p{L}+| ?\\p{N}+| ?[^\\s\\p{L}\\p{N}]+|\\s+(?!\\S)|\\s+
@@ -14,12 +14,20 @@ GPT-2:
 cl100k-style:
   (?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\\r\\n\\p{L}\\p{N}]?\\p{L}+|\\p{N}{1,3}
   | ?[^\\s\\p{L}\\p{N}]+[\\r\\n]*|\\s*[\\r\\n]+|\\s+(?!\\S)|\\s+
+
+o200k-style (this project's own definition in the style of the o200k family
+the pages name: letter runs split by case, contractions as a suffix of the
+word before them, and a symbol run that also takes a tail of CR, LF and '/'):
+  [^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]*[\\p{Ll}\\p{Lm}\\p{Lo}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?
+  |[^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?
+  |\\p{N}{1,3}| ?[^\\s\\p{L}\\p{N}]+[\\r\\n/]*|\\s*[\\r\\n]+|\\s+(?!\\S)|\\s+
 """
 from .regex_engine import Alt, Cls, INF, Lit, NotAhead, Rep, Seq, match_at
-from .ucd import class_array
+from .ucd import class_array, is_upper
 
 PATTERN_GPT2 = 0
 PATTERN_CL100K = 1
+PATTERN_O200K = 2
 
 _L = Cls(lambda cp, c: c == "L", r"\p{L}")
 _N = Cls(lambda cp, c: c == "N", r"\p{N}")
@@ -29,6 +37,9 @@ _NOT_SLN = Cls(lambda cp, c: c == "O", r"[^\s\p{L}\p{N}]")
 _NOT_CRLF_L_N = Cls(lambda cp, c: cp not in (10, 13) and c not in ("L", "N"), r"[^\r\n\p{L}\p{N}]")
 _CRLF = Cls(lambda cp, c: cp in (10, 13), r"[\r\n]")
 _SP = Lit(" ")
+_UPPER = Cls(lambda cp, c: c == "L" and is_upper(cp), r"[\p{Lu}\p{Lt}]")
+_LOWER = Cls(lambda cp, c: c == "L" and not is_upper(cp), r"[\p{Ll}\p{Lm}\p{Lo}]")
+_CRLF_SLASH = Cls(lambda cp, c: cp in (10, 13, 47), r"[\r\n/]")
 
 
 def _contractions(icase):
@@ -54,7 +65,20 @@ CL100K = Alt(
     Rep(_S, 1, INF),
 )
 
-PATTERNS = {PATTERN_GPT2: GPT2, PATTERN_CL100K: CL100K}
+# an optional contraction after a word: the contractions, else nothing
+_SUFFIX = Alt(*_contractions(True), Seq())
+
+O200K = Alt(
+    Seq(Rep(_NOT_CRLF_L_N, 0, 1), Rep(_UPPER, 0, INF), Rep(_LOWER, 1, INF), _SUFFIX),
+    Seq(Rep(_NOT_CRLF_L_N, 0, 1), Rep(_UPPER, 1, INF), _SUFFIX),
+    Rep(_N, 1, 3),
+    Seq(Rep(_SP, 0, 1), Rep(_NOT_SLN, 1, INF), Rep(_CRLF_SLASH, 0, INF)),
+    Seq(Rep(_S, 0, INF), Rep(_CRLF, 1, INF)),
+    Seq(Rep(_S, 1, INF), NotAhead(_NOT_S)),
+    Rep(_S, 1, INF),
+)
+
+PATTERNS = {PATTERN_GPT2: GPT2, PATTERN_CL100K: CL100K, PATTERN_O200K: O200K}
 
 
 def pretokenize(cps, pattern_id, cls=None):

@@ -6,10 +6,12 @@ TEST INFRASTRUCTURE ONLY: the oracle of the library's tok_repair_append.
 
 The cut this oracle uses follows from the patterns themselves.  Let p be a
 position whose previous code point is a letter or a number and whose own code
-point has another class.  Every alternative of both patterns that consumes a
-letter or a number matches a maximal run of them (with at most a one-code-point
-prefix before it), so the match that covers p - 1 ends exactly at p: p starts
-a fragment whatever follows.  The fragments before p depend only on the text up
+point has another class and is not an apostrophe.  Every alternative of the
+patterns that consumes a letter or a number ends at the end of a run of them
+or inside it (after at most a one-code-point prefix), except that the
+o200k-style pattern lets a contraction, which begins with an apostrophe,
+follow a word; so the match that covers p - 1 ends exactly at p: p starts a
+fragment whatever follows.  The fragments before p depend only on the text up
 to and including the code point at p, and, since the patterns have no
 look-behind, the fragments from p on depend only on the text from p on.  So
 when the code point at p lies inside old,
@@ -32,7 +34,7 @@ def last_cut(old):
     cps, offs = decode_utf8(old)
     cls = [classify(c) for c in cps]
     for j in range(len(cps) - 1, 0, -1):
-        if cls[j - 1] in ("L", "N") and cls[j] != cls[j - 1]:
+        if cls[j - 1] in ("L", "N") and cls[j] != cls[j - 1] and cps[j] != 0x27:
             return offs[j]
     return 0
 

@@ -28,6 +28,25 @@ with open(_PATH) as _f:
 
 VERSION_LINE = open(_PATH).readline().strip()
 
+# upper-case and title-case letters (\\p{Lu}, \\p{Lt}): the o200k-style
+# pattern splits letter runs by case; data/unicode_upper.txt comes from the
+# same generator and regex engine
+_UPATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "data", "unicode_upper.txt")
+_ustarts, _uends = [], []
+with open(_UPATH) as _f:
+    for _line in _f:
+        if _line.startswith("#"):
+            continue
+        _a, _b = _line.split()
+        _ustarts.append(int(_a, 16))
+        _uends.append(int(_b, 16))
+
+
+def is_upper(cp):
+    """True for an upper-case or title-case letter (Lu, Lt)."""
+    k = bisect.bisect_right(_ustarts, cp) - 1
+    return k >= 0 and cp <= _uends[k]
+
 
 def classify(cp):
     """Class letter of one code point."""

@@ -38,8 +38,9 @@ def oracle_pool():
 
 
 # every string of up to five code points over this alphabet goes through the
-# pre-tokenizer in the brute-force tests: letters (ASCII, contraction letters
-# in both cases, a 3-byte one), the apostrophe, numbers (ASCII and not), the
-# whitespace the patterns treat apart (space, tab, LF, CR, a 2-byte one) and
-# an ASCII symbol
-BRUTE_ALPHABET = ["a", "s", "S", "l", "'", "1", "²", " ", "\t", "\n", "\r", ".", "中", " "]
+# pre-tokenizer in the brute-force tests: letters (ASCII lower and upper case,
+# contraction letters in both cases, a 3-byte caseless one), the apostrophe,
+# numbers (ASCII and not), the whitespace the patterns treat apart (space,
+# tab, LF, CR, a 2-byte one) and '/' (an ASCII symbol that the o200k-style
+# pattern also takes into a symbol run's tail)
+BRUTE_ALPHABET = ["a", "s", "S", "l", "'", "1", "\u00b2", " ", "\t", "\n", "\r", "/", "\u4e2d", "\u00a0"]

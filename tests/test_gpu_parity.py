@@ -16,7 +16,7 @@ import textgen
 from conftest import BRUTE_ALPHABET
 from oracle.encode import encode, encode_with_offsets, pretoken_byte_spans
 from oracle.repair import repair_append as oracle_repair_append
-from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2
+from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2, PATTERN_O200K
 from oracle.utf8 import Utf8Error
 from oracle.vocab import Vocab
 
@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 VOC = os.path.join(ROOT, "data", "vocabs")
 
-ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ"
+ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ/"
 
 
 @pytest.fixture(scope="session")
@@ -56,7 +56,10 @@ def oracle_starts(data, pattern):
 
 # --- pre-tokenizer ----------------------------------------------------------
 
-@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+ALL_PATTERNS = [PATTERN_GPT2, PATTERN_CL100K, PATTERN_O200K]
+
+
+@pytest.mark.parametrize("pattern", ALL_PATTERNS)
 def test_pretokenize_brute_force(pkg, pattern):
     tok = pkg.Tokenizer.from_merges([], pattern)
     items = ["".join(t) for n in range(1, 4) for t in itertools.product(ALPHABET, repeat=n)]
@@ -68,7 +71,7 @@ def test_pretokenize_brute_force(pkg, pattern):
         assert g == oracle_starts(b, pattern), repr(s)
 
 
-@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+@pytest.mark.parametrize("pattern", ALL_PATTERNS)
 def test_pretokenize_brute_force_five_code_points(pkg, oracle_pool, pattern):
     # every string of 1..5 code points over the adversarial alphabet, in one
     # batch call, against the oracle's fragment starts
@@ -81,7 +84,7 @@ def test_pretokenize_brute_force_five_code_points(pkg, oracle_pool, pattern):
     assert not bad, bad[:5]
 
 
-@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+@pytest.mark.parametrize("pattern", ALL_PATTERNS)
 def test_pretokenize_runs_across_chunks(pkg, pattern):
     # runs far longer than a 1 KiB chunk: whitespace, digits, letters, CR/LF
     tok = pkg.Tokenizer.from_merges([], pattern)
@@ -91,7 +94,9 @@ def test_pretokenize_runs_across_chunks(pkg, pattern):
              b"a" + b"\r\n" * 5000 + b" " * 3,
              b"1" * 12347 + b"z" + b"2" * 8191,
              b" " * 8192,
-             b"'s" * 3000 + b"'" + b" " * 4095 + b"'ll"]
+             b"'s" * 3000 + b"'" + b" " * 4095 + b"'ll",
+             b"x." + b"\n/" * 4000 + b".abc" + b"\r\n" * 700 + b"/" * 900 + b"\n/x",
+             b"camelCase" * 500 + b"ABC" * 700 + b"x's" * 400]
     for p in parts:
         assert list(tok.pretokenize(p)) == oracle_starts(p, pattern)
     got = tok.pretokenize_batch(parts)
@@ -120,13 +125,14 @@ def _runs_at_chunk_edges(kinds, lengths, offsets, chunk=1024):
     return bytes(out)
 
 
-@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+@pytest.mark.parametrize("pattern", ALL_PATTERNS)
 def test_runs_at_every_offset_of_a_chunk_edge(pkg, pattern):
     # the run states at a chunk's edges come from the window when a run ends
     # within it and from the text beyond it otherwise: runs of CR/LF, digits,
-    # spaces, mixed whitespace and apostrophes around the window's reach
+    # spaces, mixed whitespace and apostrophes around the window's reach, and
+    # (o200k-style) tails of CR/LF and '/' after a symbol, case changes
     tok = pkg.Tokenizer.from_merges([], pattern)
-    kinds = [b"\r\n", b"7", b" ", b"\t\n ", "\u0663".encode(), b"'s"]
+    kinds = [b"\r\n", b"7", b" ", b"\t\n ", "\u0663".encode(), b"'s", b"\n/", b"aB", b"\n\n /"]
     text = _runs_at_chunk_edges(kinds, [1, 2, 5, 11, 12, 13, 14, 17], range(-3, 20))
     assert list(tok.pretokenize(text)) == oracle_starts(text, pattern)
     name = "gpt2_session_100k" if pattern == PATTERN_GPT2 else "cl100k_session_100k"
@@ -405,3 +411,65 @@ def test_device_entry_points(pkg):
     ids_h, off_h = tok.encode_batch(items)
     assert d_off.cpu().tolist() == off_h.tolist()
     assert d_ids[:int(off_h[-1])].cpu().numpy().tolist() == ids_h.tolist()
+
+
+# --- o200k-style pattern --------------------------------------------------------
+
+def test_o200k_style_encode_matches_oracle(pkg, oracle_pool):
+    # the o200k-style pattern (this library's own definition) with the
+    # 100k-merge session vocabulary: the 1M-character session, code with
+    # paths and camelCase, the scaled adversarial text and a batch
+    path = os.path.join(VOC, "cl100k_session_100k.merges")
+    v = Vocab.load_merges(path)
+    tok = pkg.Tokenizer.from_merges_file(path, PATTERN_O200K)
+    session = textgen.agentic_session(1_000_000, 1003).encode()
+    want_ids, want_starts = oracle_pool.encode_long(session, path, PATTERN_O200K)
+    assert tok.pretokenize(session).tolist() == want_starts
+    assert tok.encode(session).tolist() == want_ids
+    code = textgen.code_ascii(300_000, 1051).encode()
+    assert tok.encode(code).tolist() == encode(code, v, PATTERN_O200K)
+    adv = textgen.adversarial(400_000, 1005, scale=0.02).encode()
+    ids, offs = tok.encode_with_offsets(adv)
+    assert (ids.tolist(), offs.tolist()) == encode_with_offsets(adv, v, PATTERN_O200K)
+    items = [x.encode() for x in textgen.session_batch(8, 1052, hi=1 << 16)]
+    ids, off = tok.encode_batch(items)
+    for k, it in enumerate(items):
+        assert ids[off[k]:off[k + 1]].tolist() == encode(it, v, PATTERN_O200K), k
+    # repair after appends
+    old, delta = session[:30_000], session[30_000:31_500]
+    oi, oo = tok.encode_with_offsets(old)
+    got = tok.repair_append(old, oi, oo, delta)
+    assert (got[0].tolist(), got[1].tolist()) == encode_with_offsets(old + delta, v, PATTERN_O200K)
+    tok.close()
+
+
+# --- ignore_merges -------------------------------------------------------------
+
+def test_ignore_merges_matches_oracle(pkg):
+    # a vocabulary with tokens that do not encode to themselves: with the flag
+    # a fragment that is such a token is that token (Section 4.2), every other
+    # fragment is BPE; the session vocabulary on session text and on a long
+    # letter run (no split into pieces under the flag)
+    toks = [bytes([b]) for b in range(256)] + [b"ab", b"bc", b"abc", b" ab", b" abc"]
+    ix = {t: i for i, t in enumerate(toks)}
+    merges = [(ix[b"a"], ix[b"b"]), (ix[b"b"], ix[b"c"]), (ix[b"a"], ix[b"bc"]), (ix[b" "], ix[b"ab"]),
+              (ix[b" "], ix[b"abc"])]
+    v = Vocab(toks, merges)
+    data = b"abc abc abcc xabc  abc bcabc " * 50
+    for pat in (PATTERN_GPT2, PATTERN_CL100K):
+        tok = pkg.Tokenizer(toks, merges, pat, ignore_merges=True)
+        assert tok.encode(data).tolist() == encode(data, v, pat, ignore_merges=True)
+        assert encode(data, v, pat, ignore_merges=True) != encode(data, v, pat)
+        tok.close()
+    path = os.path.join(VOC, "cl100k_session_100k.merges")
+    vs = Vocab.load_merges(path)
+    tok = pkg.Tokenizer.from_merges_file(path, PATTERN_CL100K, ignore_merges=True)
+    for d in (textgen.agentic_session(200_000, 1041).encode(), textgen.adversarial(600_000, 1005, scale=0.03).encode()):
+        ids, offs = tok.encode_with_offsets(d)
+        want = encode_with_offsets(d, vs, PATTERN_CL100K, ignore_merges=True)
+        assert (ids.tolist(), offs.tolist()) == want
+    items = [s.encode() for s in textgen.session_batch(6, 1042, hi=1 << 16)]
+    ids, off = tok.encode_batch(items)
+    for k, it in enumerate(items):
+        assert ids[off[k]:off[k + 1]].tolist() == encode(it, vs, PATTERN_CL100K, ignore_merges=True)
+    tok.close()

@@ -182,3 +182,29 @@ def test_pair_barriers_on_a_trained_vocabulary_and_a_long_letter_run():
     for a, b in zip(cuts, cuts[1:]):
         parts += bpe_heap([v.byte_id[x] for x in w[a:b]], v.merge_map)
     assert parts == bpe_heap([v.byte_id[x] for x in w], v.merge_map)
+
+
+def test_ignore_merges_takes_whole_tokens_only_for_whole_fragments():
+    # "abc" is a token made by (a, bc), but (a, b) ranks first, so BPE of the
+    # bytes gives [ab, c]; with ignore_merges the fragment "abc" is the token
+    # "abc" itself (Section 4.2's whole-word lookup), while a fragment that is
+    # not a token ("abcc") still goes through BPE
+    v, idx = _vocab_from_strings([("a", "b"), ("b", "c"), ("a", "bc")])
+    mm = v.merge_map
+    assert bpe_textbook(list(b"abc"), mm) == [idx[b"ab"], 99]
+    assert encode(b"abc", v, PATTERN_GPT2) == [idx[b"ab"], 99]
+    assert encode(b"abc", v, PATTERN_GPT2, ignore_merges=True) == [idx[b"abc"]]
+    assert encode(b"abcc abc", v, PATTERN_GPT2, ignore_merges=True) == (
+        bpe_textbook(list(b"abcc"), mm) + encode(b" abc", v, PATTERN_GPT2))
+    # the pages' pipe / line example: with every piece a token, both readings agree
+    v2, idx2 = _vocab_from_strings([("p", "i"), ("p", "e"), ("pi", "pe"), ("l", "i"), ("n", "e"), ("li", "ne"),
+                                    ("pipe", "line")])
+    for w in (b"pipe", b"line", b"pipeline"):
+        assert encode(w, v2, PATTERN_GPT2, ignore_merges=True) == encode(w, v2, PATTERN_GPT2) == [idx2[w]]
+    # a fragment with no whole token is unchanged by the flag
+    rnd = random.Random(31)
+    for _ in range(200):
+        vr = _random_vocab(rnd, "abc", rnd.randint(1, 20))
+        w = bytes(rnd.choice(b"abc") for _ in range(rnd.randint(1, 12)))
+        want = [vr.index[w]] if w in vr.index else bpe_heap(list(w), vr.merge_map)
+        assert encode(w, vr, PATTERN_GPT2, ignore_merges=True) == want

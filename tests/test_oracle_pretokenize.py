@@ -9,7 +9,7 @@ import random
 import pytest
 
 import textgen
-from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2, pretokenize
+from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2, PATTERN_O200K, pretokenize
 from oracle.utf8 import decode_utf8
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -18,7 +18,13 @@ GPT2_RE = r"""'s|'t|'re|'ve|'m|'ll|'d| ?\p{L}+| ?\p{N}+| ?[^\s\p{L}\p{N}]+|\s+(?
 CL100K_RE = (r"""(?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\r\n\p{L}\p{N}]?\p{L}+|\p{N}{1,3}"""
              r"""| ?[^\s\p{L}\p{N}]+[\r\n]*|\s*[\r\n]+|\s+(?!\S)|\s+""")
 
-ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ"
+# the o200k-style pattern as include/tok.h states it (this project's own
+# definition)
+O200K_RE = (r"""[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]*[\p{Ll}\p{Lm}\p{Lo}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?"""
+            r"""|[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?"""
+            r"""|\p{N}{1,3}| ?[^\s\p{L}\p{N}]+[\r\n/]*|\s*[\r\n]+|\s+(?!\S)|\s+""")
+
+ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ/"
 
 
 def split(s, pat):
@@ -39,10 +45,25 @@ def test_pinned_examples():
     assert n >= 20
 
 
+def test_pinned_examples_o200k_style():
+    # splits the regex module gave for the o200k-style pattern
+    # (tests/golden/make_o200k_pins.py): camelCase splits, contractions as
+    # suffixes, caseless letters, the [\r\n/]* tail
+    n = 0
+    with open(os.path.join(HERE, "golden", "pretoken_pins_o200k.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            s, want = json.loads(line)
+            assert split(s, PATTERN_O200K) == want, s
+            n += 1
+    assert n >= 40
+
+
 def test_partition_and_empty():
     assert pretokenize([], PATTERN_GPT2) == []
     s = textgen.mixed_c2(4000, 3)
-    for pat in (PATTERN_GPT2, PATTERN_CL100K):
+    for pat in (PATTERN_GPT2, PATTERN_CL100K, PATTERN_O200K):
         parts = split(s, pat)
         assert "".join(parts) == s and all(parts)
 
@@ -53,17 +74,19 @@ def _regex_split(rx, s):
 
 def test_brute_force_against_regex_module():
     regex = pytest.importorskip("regex")
-    rg, rc = regex.compile(GPT2_RE), regex.compile(CL100K_RE)
+    rg, rc, ro = regex.compile(GPT2_RE), regex.compile(CL100K_RE), regex.compile(O200K_RE)
     for n in range(1, 4):
         for t in itertools.product(ALPHABET, repeat=n):
             s = "".join(t)
             assert split(s, PATTERN_GPT2) == rg.findall(s), repr(s)
             assert split(s, PATTERN_CL100K) == rc.findall(s), repr(s)
+            assert split(s, PATTERN_O200K) == ro.findall(s), repr(s)
     rnd = random.Random(11)
     for _ in range(5000):
         s = "".join(rnd.choice(ALPHABET) for _ in range(rnd.randint(4, 16)))
         assert split(s, PATTERN_GPT2) == rg.findall(s), repr(s)
         assert split(s, PATTERN_CL100K) == rc.findall(s), repr(s)
+        assert split(s, PATTERN_O200K) == ro.findall(s), repr(s)
 
 
 def test_brute_force_five_code_points_against_regex_module(oracle_pool):
@@ -73,7 +96,8 @@ def test_brute_force_five_code_points_against_regex_module(oracle_pool):
     from conftest import BRUTE_ALPHABET
     strs = ["".join(t) for n in range(1, 6) for t in itertools.product(BRUTE_ALPHABET, repeat=n)]
     enc = [s.encode() for s in strs]
-    for pat, rx in ((PATTERN_GPT2, regex.compile(GPT2_RE)), (PATTERN_CL100K, regex.compile(CL100K_RE))):
+    for pat, rx in ((PATTERN_GPT2, regex.compile(GPT2_RE)), (PATTERN_CL100K, regex.compile(CL100K_RE)),
+                    (PATTERN_O200K, regex.compile(O200K_RE))):
         got = oracle_pool.starts_many(enc, pat)
         for s, g in zip(strs, got):
             want, pos = [], 0
@@ -85,9 +109,10 @@ def test_brute_force_five_code_points_against_regex_module(oracle_pool):
 
 def test_generated_text_against_regex_module():
     regex = pytest.importorskip("regex")
-    rg, rc = regex.compile(GPT2_RE), regex.compile(CL100K_RE)
+    rg, rc, ro = regex.compile(GPT2_RE), regex.compile(CL100K_RE), regex.compile(O200K_RE)
     texts = [textgen.code_ascii(8000, 1), textgen.mixed_c2(20000, 2), textgen.agentic_session(20000, 3)]
     texts += textgen.adversarial_pieces(5, scale=0.002)
     for s in texts:
         assert split(s, PATTERN_GPT2) == rg.findall(s)
         assert split(s, PATTERN_CL100K) == rc.findall(s)
+        assert split(s, PATTERN_O200K) == ro.findall(s)
