@@ -56,13 +56,13 @@ enum {
  * families (Section 4.1) without printing them; these are the GPT-2 pattern,
  * the cl100k-style pattern and an o200k-style pattern of this library's own
  * definition (letter runs split where a lower-case or caseless letter is
- * followed by an upper-case one, contractions a suffix of the word before,
+ * followed by an upper-case one, contractions suffixes of the word before,
  * a symbol run's tail of CR, LF and '/'):
  *   GPT-2:  's|'t|'re|'ve|'m|'ll|'d| ?\p{L}+| ?\p{N}+| ?[^\s\p{L}\p{N}]+|\s+(?!\S)|\s+
  *   cl100k: (?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\r\n\p{L}\p{N}]?\p{L}+|\p{N}{1,3}
  *           | ?[^\s\p{L}\p{N}]+[\r\n]*|\s*[\r\n]+|\s+(?!\S)|\s+
- *   o200k:  [^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]*[\p{Ll}\p{Lm}\p{Lo}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?
- *           |[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?
+ *   o200k:  [^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]*[\p{Ll}\p{Lm}\p{Lo}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
+ *           |[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
  *           |\p{N}{1,3}| ?[^\s\p{L}\p{N}]+[\r\n/]*|\s*[\r\n]+|\s+(?!\S)|\s+       */
 enum { TOK_PAT_GPT2 = 0, TOK_PAT_CL100K_STYLE = 1, TOK_PAT_O200K_STYLE = 2 };
 

@@ -16,10 +16,10 @@ cl100k-style:
   | ?[^\\s\\p{L}\\p{N}]+[\\r\\n]*|\\s*[\\r\\n]+|\\s+(?!\\S)|\\s+
 
 o200k-style (this project's own definition in the style of the o200k family
-the pages name: letter runs split by case, contractions as a suffix of the
+the pages name: letter runs split by case, contractions as suffixes of the
 word before them, and a symbol run that also takes a tail of CR, LF and '/'):
-  [^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]*[\\p{Ll}\\p{Lm}\\p{Lo}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?
-  |[^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?
+  [^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]*[\\p{Ll}\\p{Lm}\\p{Lo}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
+  |[^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
   |\\p{N}{1,3}| ?[^\\s\\p{L}\\p{N}]+[\\r\\n/]*|\\s*[\\r\\n]+|\\s+(?!\\S)|\\s+
 """
 from .regex_engine import Alt, Cls, INF, Lit, NotAhead, Rep, Seq, match_at
@@ -65,8 +65,10 @@ CL100K = Alt(
     Rep(_S, 1, INF),
 )
 
-# an optional contraction after a word: the contractions, else nothing
-_SUFFIX = Alt(*_contractions(True), Seq())
+# the contractions after a word, any number of them (greedy): a
+# self-referential alternation, (?:contraction)*
+_SUFFIX = Alt()
+_SUFFIX.branches = tuple(Seq(c, _SUFFIX) for c in _contractions(True)) + (Seq(),)
 
 O200K = Alt(
     Seq(Rep(_NOT_CRLF_L_N, 0, 1), Rep(_UPPER, 0, INF), Rep(_LOWER, 1, INF), _SUFFIX),

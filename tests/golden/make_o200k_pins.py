@@ -10,13 +10,14 @@ import os
 
 import regex
 
-O200K_RE = (r"""[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]*[\p{Ll}\p{Lm}\p{Lo}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?"""
-            r"""|[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?"""
+O200K_RE = (r"""[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]*[\p{Ll}\p{Lm}\p{Lo}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*"""
+            r"""|[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*"""
             r"""|\p{N}{1,3}| ?[^\s\p{L}\p{N}]+[\r\n/]*|\s*[\r\n]+|\s+(?!\S)|\s+""")
 
 EXAMPLES = [
     "camelCaseWord", "HTMLParser", "parseHTML", "getXMLHttpRequest", "ABC", "aB", "Ab",
     "don't", "DON'T", "they're here", "we'LL see", "x's", "'s", " 's", "1's", "it'sa", "o'clock", "x'ſ",
+    "x's's's", "é'ſ'S", "he'd've", "x'sam's", "'s's", "a''s",
     "中文abc", "abc中文", "ABC中文", "中A", "A中", "中Ab", "ǅungla", "ǅ",
     "x.\n/usr/bin", "a;\r\n/b", ".\n/.abc", "./\n/x", "path/to/file", " //comment\n", "a/\nb", "x\n/y",
     "12345678", "1²3½45", "  foo", "\t\tfoo", "x;\n\n  \ny", "x\r\n\r\n  y", "\n  ", "a.foo", " .foo",

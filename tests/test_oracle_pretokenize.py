@@ -20,8 +20,8 @@ CL100K_RE = (r"""(?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\r\n\p{L}\p{N}]?\p{L}+|\p{N}{1,3
 
 # the o200k-style pattern as include/tok.h states it (this project's own
 # definition)
-O200K_RE = (r"""[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]*[\p{Ll}\p{Lm}\p{Lo}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?"""
-            r"""|[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]+(?i:'s|'t|'re|'ve|'m|'ll|'d)?"""
+O200K_RE = (r"""[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]*[\p{Ll}\p{Lm}\p{Lo}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*"""
+            r"""|[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*"""
             r"""|\p{N}{1,3}| ?[^\s\p{L}\p{N}]+[\r\n/]*|\s*[\r\n]+|\s+(?!\S)|\s+""")
 
 ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ/"
