@@ -22,7 +22,7 @@ word before them, and a symbol run that also takes a tail of CR, LF and '/'):
   |[^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
   |\\p{N}{1,3}| ?[^\\s\\p{L}\\p{N}]+[\\r\\n/]*|\\s*[\\r\\n]+|\\s+(?!\\S)|\\s+
 """
-from .regex_engine import Alt, Cls, INF, Lit, NotAhead, Rep, Seq, match_at
+from .regex_engine import Alt, Cls, INF, Lit, NotAhead, Rep, Seq, Star, match_at
 from .ucd import class_array, is_upper
 
 PATTERN_GPT2 = 0
@@ -65,10 +65,8 @@ CL100K = Alt(
     Rep(_S, 1, INF),
 )
 
-# the contractions after a word, any number of them (greedy): a
-# self-referential alternation, (?:contraction)*
-_SUFFIX = Alt()
-_SUFFIX.branches = tuple(Seq(c, _SUFFIX) for c in _contractions(True)) + (Seq(),)
+# the contractions after a word, any number of them (greedy)
+_SUFFIX = Star(Alt(*_contractions(True)))
 
 O200K = Alt(
     Seq(Rep(_NOT_CRLF_L_N, 0, 1), Rep(_UPPER, 0, INF), Rep(_LOWER, 1, INF), _SUFFIX),

@@ -1,7 +1,8 @@
 """A small leftmost-first (Perl-style) backtracking regex matcher for the
-constructs the two pre-tokenizer patterns use: literals (optionally
+constructs the pre-tokenizer patterns use: literals (optionally
 case-insensitive), classes of one code point, greedy quantifiers over one
-code point, sequences, ordered alternation and negative lookahead.
+code point, greedy repetition of a sub-pattern, sequences, ordered
+alternation and negative lookahead.
 
 Semantics (the usual backtracking reading): an alternation tries its
 branches in order; a greedy quantifier first takes as many code points as
@@ -70,6 +71,17 @@ class Rep(Node):
         self.item, self.lo, self.hi = item, lo, hi
 
 
+class Star(Node):
+    """Greedy repetition (X)* of a sub-pattern X of any length.  Backtracking
+    order as for the recursive reading (X Star)|(empty): at each position X's
+    matches are tried in X's own order, each followed by more repetitions,
+    and only then the rest of the pattern.  The search keeps its own stack, so
+    a long chain of repetitions needs no deep recursion."""
+
+    def __init__(self, item):
+        self.item = item
+
+
 class NotAhead(Node):
     """(?!item): succeeds, consuming nothing, iff item does not match here."""
 
@@ -108,6 +120,24 @@ def _m(node, cps, cls, i, k):
             if r is not None:
                 return r
             count -= 1
+        return None
+    if isinstance(node, Star):
+        def ends(p):
+            # every end of one match of the item at p, in backtracking order
+            out = []
+            _m(node.item, cps, cls, p, lambda j: out.append(j))
+            return iter([j for j in out if j > p])  # an empty repetition adds nothing
+        stack = [(i, ends(i))]
+        while stack:
+            p, it = stack[-1]
+            q = next(it, None)
+            if q is not None:
+                stack.append((q, ends(q)))
+                continue
+            stack.pop()
+            r = k(p)
+            if r is not None:
+                return r
         return None
     if isinstance(node, NotAhead):
         if _m(node.item, cps, cls, i, lambda j: j) is not None:
