@@ -265,6 +265,7 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
   c.pf[0] = Prefetch{h->d_whole, (unsigned long long)sizeof(WholeEntry) << h->v.whole_bits};
   c.pf[1] = Prefetch{h->d_vocab_bytes, h->vocab_bytes_len};
   c.pf[2] = Prefetch{h->d_table, (unsigned long long)sizeof(MergeEntry) << h->v.bits};
+  c.pf[3] = Prefetch{h->v.pair_bits, h->v.pair_bits ? 8192ull : 0ull};
   c.pattern = h->pattern;
   c.epoch = next_epoch(h, s);
   if (c.n == 0) {

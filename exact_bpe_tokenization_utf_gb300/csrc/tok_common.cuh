@@ -160,7 +160,7 @@ struct Call {
   long long* user_status;     // device int64[4] or nullptr
   int settle;                 // K2 also settles fragments and fills the queues (encode calls)
   int out_host;               // `out` is pinned host memory (mapped): K5 stages a chunk's ids for coalesced stores
-  Prefetch pf[3];             // whole-token table, token bytes, merge table
+  Prefetch pf[4];             // whole-token table, token bytes, merge table, byte-pair bits
 };
 
 // The first malformed UTF-8 byte of a call, as one word that atomicMax keeps

@@ -233,22 +233,19 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
       c.item_off[k] = (long long)base + (total > 0 ? idb[x - r0] : 0);
     }
   }
-  // the last CTA to finish completes the status: the number of ids is the
-  // sum of the group totals
+  // the CTA of the last chunk knows the number of ids (the ids before it and
+  // its own); the last CTA to finish completes the status
   __syncthreads();
   if (tid == 0) {
+    if (chunk == nch - 1) st->n_ids = base + (unsigned long long)total;
     __threadfence();
     s_last = atomicAdd(&st->emit_done, 1u) == (uint32_t)(nch - 1);
   }
   __syncthreads();
   if (s_last) {
     __threadfence();
-    unsigned long long all = 0;
-    for (long long i = tid; i <= (nch - 1) / CTOT_GROUP; i += T) all += ws.gtot[i];
-    unsigned long long n_ids = 0;
-    block_excl_sum_t(all, &n_ids, scan64);
+    const unsigned long long n_ids = *(volatile unsigned long long*)&st->n_ids;
     if (tid == 0) {
-      st->n_ids = n_ids;
       if (c.item_off) {
         for (int k = c.n_items; k >= 0 && c.item[k] >= c.n; --k) c.item_off[k] = (long long)n_ids;
       }
