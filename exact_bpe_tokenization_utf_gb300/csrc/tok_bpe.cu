@@ -605,80 +605,86 @@ __device__ __forceinline__ int warp_steps(WarpBuf& B, const DevVocab& V, DevStat
                                           uint32_t& lenb, bool& fst, int& fid, unsigned long long& kr) {
   const int lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
+  // Symbols stay in their lanes: a merge keeps the left lane and retires the
+  // right one, and the live lanes are a mask.  Fragment starts never move, so
+  // each lane's fragment (its lanes, the empty lanes past m joining the last
+  // fragment) is fixed for the whole batch.
+  const unsigned upto = lane == 31 ? FULL : ((2u << lane) - 1u);  // lanes up to this one
+  unsigned alive = m >= 32 ? FULL : ((1u << m) - 1u);
+  const unsigned fsm = __ballot_sync(FULL, fst);
+  const unsigned before = fsm & upto;
+  const int first = before ? 31 - __clz(before) : 0;
+  const unsigned after = fsm & ~upto;
+  const unsigned fmask = (after ? ((after & (0u - after)) - 1u) : FULL) & ~((1u << first) - 1u);
   for (int step = 0; step <= 32; ++step) {
     const uint32_t k = kr_rank(kr);
-    const bool mrg = mergeable(k);
+    const bool mrg = mergeable(k);  // a retired lane holds KR_WALL
     if (!__any_sync(FULL, mrg)) break;
     if (step == 32) {  // cannot happen: every step merges a pair of some fragment
       if (lane == 0) atomicExch(&st->code, ST_EINTERNAL);
       break;
     }
+    // the fragment's leftmost lowest-rank pair: one reduction over its lanes
+    // (every lane takes part, so it comes first)
     const uint32_t v = mrg ? ((k << 5) | (uint32_t)lane) : SEG_VAL;
-    const bool nfs = __shfl_down_sync(FULL, fst, 1);  // the next lane starts a fragment
-    // the lanes of this lane's fragment (the empty lanes past m join the last
-    // one), and their minimum: one reduction per fragment, all at once
-    const unsigned fsm = __ballot_sync(FULL, fst);
-    const unsigned upto = lane == 31 ? 0xffffffffu : ((2u << lane) - 1u);
-    const unsigned before = fsm & upto;
-    const int first = before ? 31 - __clz(before) : 0;
-    const unsigned after = fsm & ~upto;
-    const unsigned fmask = (after ? ((after & (0u - after)) - 1u) : 0xffffffffu) & ~((1u << first) - 1u);
-    // (every lane takes part in the reduction, so it is computed first)
     const uint32_t fmin = __reduce_min_sync(fmask, v);
     const bool sel = mrg && v == fmin;
-    // merge: the selected pair's left symbol takes the result, its right one goes
-    const bool absorbed = __shfl_up_sync(FULL, sel, 1) && lane > 0;
+    const unsigned selm = __ballot_sync(FULL, sel);
+    // neighbours among the live lanes
+    const bool live = (alive >> lane) & 1u;
+    const unsigned above = alive & ~upto;
+    const int nx = above ? __ffs(above) - 1 : 31;            // next live lane
+    const unsigned above2 = above & (above - 1u);
+    const int nx2 = above2 ? __ffs(above2) - 1 : 31;         // the live lane after it
+    const unsigned lower = alive & ((1u << lane) - 1u);
+    const bool absorbed = live && lower && ((selm >> (31 - __clz(lower))) & 1u);  // previous live lane merges into it
     const uint32_t res = kr_result(kr);
-    const uint32_t lnext = __shfl_down_sync(FULL, lenb, 1);
-    const bool nsel = __shfl_down_sync(FULL, sel, 1);
-    const uint32_t nres = __shfl_down_sync(FULL, res, 1);
-    const uint32_t sym2 = __shfl_down_sync(FULL, sym, 2);
-    const bool fst2 = __shfl_down_sync(FULL, fst, 2);
-    uint32_t nsym = sym, nlen = lenb;
+    const uint32_t sym_nx2 = __shfl_sync(FULL, sym, nx2);
+    const uint32_t res_nx = __shfl_sync(FULL, res, nx);
     unsigned long long nkr = kr;
     bool look = false;
     uint32_t la = 0, lb = 0;
     if (sel) {
-      nsym = res;
-      nlen = lenb + lnext;
-      if (lane + 2 < m && !fst2) {
+      sym = res;
+      // the merged symbol and the live symbol after the absorbed one
+      if (above2 && !((fsm >> nx2) & 1u)) {
         look = true;
         la = res;
-        lb = sym2;
+        lb = sym_nx2;
       } else {
         nkr = KR_WALL;
       }
-    } else if (nsel && !nfs && lane < m) {
+    } else if (live && above && ((selm >> nx) & 1u) && !((fsm >> nx) & 1u)) {
       look = true;  // the pair with the merged symbol on the right
       la = sym;
-      lb = nres;
+      lb = res_nx;
     }
     if (look) nkr = merge_lookup(V, la, lb);
-    // compaction through the warp's buffer
-    const bool keep = lane < m && !absorbed;
-    const uint32_t kmask = __ballot_sync(FULL, keep);
-    if (keep) {
-      const int p = __popc(kmask & ((1u << lane) - 1u));
-      B.sym[p] = nsym;
-      B.len[p] = (uint16_t)(nlen | (fst ? FRAG_START : 0u));
-      B.kr[p] = nkr;
-      B.fidx[p] = (uint16_t)fid;
-    }
-    __syncwarp();
-    m = __popc(kmask);
-    if (lane < m) {
-      sym = B.sym[lane];
-      const uint32_t l = B.len[lane];
-      lenb = l & LEN_MASK;
-      fst = (l & FRAG_START) != 0;
-      kr = B.kr[lane];
-      fid = B.fidx[lane];
-    } else {
-      sym = 0; lenb = 0; fst = false; kr = KR_WALL; fid = 0;
-    }
-    __syncwarp();
+    if (absorbed) nkr = KR_WALL;
+    kr = nkr;
+    alive &= ~__ballot_sync(FULL, absorbed);
   }
-  return m;
+  // the live symbols, in order, to the first lanes
+  const bool live = (alive >> lane) & 1u;
+  if (live) {
+    const int p = __popc(alive & ((1u << lane) - 1u));
+    B.sym[p] = sym;
+    B.len[p] = (uint16_t)(fst ? FRAG_START : 0u);
+    B.fidx[p] = (uint16_t)fid;
+  }
+  __syncwarp();
+  const int mm = __popc(alive);
+  if (lane < mm) {
+    sym = B.sym[lane];
+    fst = (B.len[lane] & FRAG_START) != 0;
+    fid = B.fidx[lane];
+  } else {
+    sym = 0; fst = false; fid = 0;
+  }
+  lenb = 0;
+  kr = KR_WALL;
+  __syncwarp();
+  return mm;
 }
 
 // One warp encodes a batch of short fragments (at most SB_MAX bytes in all).
