@@ -779,6 +779,11 @@ struct EngineSmem {
 __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
   __shared__ EngineSmem S;
   const int tid = threadIdx.x, warp = tid >> 5, T = B_THREADS;
+  // launched as a programmatic dependent of the boundary kernel: wait until
+  // it has completed and its writes are visible; let the emit kernel's CTAs
+  // be scheduled as this grid's retire
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   DevStatus* st = ws.st;
   if (tid == 0) {  // the queue sizes, loaded together (K2 wrote them)
     S.nq[0] = st->long_count;
@@ -840,7 +845,18 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
 
 
 void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
-  k_bpe_engine<<<n_sms * 16, B_THREADS, 0, s>>>(c, w, v);  // 16 CTAs of 32 registers per SM
+  // 16 CTAs of 32 registers per SM; a programmatic dependent of the boundary
+  // kernel (its CTAs are scheduled while that grid's last CTAs finish)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n_sms * 16));
+  cfg.blockDim = dim3(B_THREADS);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, k_bpe_engine, c, w, v);
 }
 
 }  // namespace tokgb

@@ -101,6 +101,8 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
   __shared__ unsigned long long scan64[B_THREADS / 32];
   __shared__ int s_item, s_nbig, s_last;
   const int tid = threadIdx.x, T = B_THREADS;
+  // a programmatic dependent of the engine kernel: wait for its writes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long nch = n_bchunks(c.n);
   DevStatus* st = ws.st;
   const long long chunk = blockIdx.x;
@@ -266,12 +268,21 @@ __global__ void k_status_only(Call c, Workspace ws) {
 
 void launch_emit(const Call& c, const Workspace& w, const DevVocab& v, cudaStream_t s) {
   const unsigned g = (unsigned)n_bchunks(c.n);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g);
+  cfg.blockDim = dim3(B_THREADS);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (c.out_off) {
-    if (c.out_host) k_emit<true, true><<<g, B_THREADS, 0, s>>>(c, w, v);
-    else k_emit<true, false><<<g, B_THREADS, 0, s>>>(c, w, v);
+    if (c.out_host) cudaLaunchKernelEx(&cfg, k_emit<true, true>, c, w, v);
+    else cudaLaunchKernelEx(&cfg, k_emit<true, false>, c, w, v);
   } else {
-    if (c.out_host) k_emit<false, true><<<g, B_THREADS, 0, s>>>(c, w, v);
-    else k_emit<false, false><<<g, B_THREADS, 0, s>>>(c, w, v);
+    if (c.out_host) cudaLaunchKernelEx(&cfg, k_emit<false, true>, c, w, v);
+    else cudaLaunchKernelEx(&cfg, k_emit<false, false>, c, w, v);
   }
 }
 
