@@ -533,6 +533,19 @@ def main():
         if k >= args.warmup:
             e2e_t.append(t1 - t0)
     e2e_s = max_over_ranks(sum(e2e_t) / len(e2e_t))
+    # the same host calls with the ids returned as Python lists of ints (the
+    # list output mode beside the array mode)
+    lst_t = []
+    for k in range(args.warmup + min(args.steps, 50)):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        lists = [r.h_ids.numpy()[:r.host_step()].tolist() for r in runs]
+        t1 = time.perf_counter()
+        assert [len(x) for x in lists] == [r.n_ids for r in runs]
+        if k >= args.warmup:
+            lst_t.append(t1 - t0)
+    lst_s = max_over_ranks(sum(lst_t) / len(lst_t))
     ids_ok = all(bool(np.array_equal(r.h_ids.numpy()[:r.n_ids], r.d_ids[:r.n_ids].cpu().numpy())) for r in runs)
 
     if rank != 0:
@@ -573,6 +586,8 @@ def main():
                     "note": "the same steps without the L2 flush: vocabulary tables and text L2-resident"},
         "e2e": {"value": job_bytes / e2e_s / 1e6, "unit": UNIT, "h2d_bytes_per_step": my_bytes,
                 "d2h_bytes_per_step": 4 * n_ids + 32 * len(runs), "ms_per_step": e2e_s * 1e3},
+        "e2e_python_list": {"value": job_bytes / lst_s / 1e6, "unit": UNIT, "ms_per_step": lst_s * 1e3,
+                            "note": "the e2e call with the ids converted to Python lists of ints"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "ids_match_host_path": ids_ok,

@@ -184,6 +184,12 @@ class Tokenizer:
                                        len(ids), ctypes.byref(n)))
         return ids[:n.value].copy()
 
+    def encode_list(self, data):
+        """The ids as a Python list of ints (the list output mode next to the
+        id array: TokTier, Section 4.3).  The encode is the same C-ABI call
+        as encode(); the list is built from its array in one conversion."""
+        return self.encode(data).tolist()
+
     def encode_with_offsets(self, data):
         """(ids, offsets): offsets[k] is the byte offset where token k starts."""
         data = bytes(data)

@@ -314,6 +314,11 @@ def test_adversarial_8mib_exact(pkg, oracle_pool, name, pattern):
 def test_empty_and_tiny(pkg):
     v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
     assert tok.encode(b"").tolist() == []
+    # the Python-list output mode: the same ids as plain ints
+    d = textgen.agentic_session(20_000, 1061).encode()
+    lst = tok.encode_list(d)
+    assert type(lst) is list and all(type(x) is int for x in lst[:10]) and lst == encode(d, v, PATTERN_CL100K)
+    assert tok.encode_list(b"") == []
     for b in range(128):
         d = bytes([b])
         assert tok.encode(d).tolist() == encode(d, v, PATTERN_CL100K)
