@@ -36,7 +36,8 @@ _NAMES = {0: "TOK_OK", -1: "TOK_EINVAL", -2: "TOK_EUTF8", -3: "TOK_ENOMEM", -4: 
 SYMBOLS = ["tok_load", "tok_encode", "tok_encode_offsets", "tok_repair_append", "tok_encode_batch", "tok_encode_device",
            "tok_encode_offsets_device", "tok_encode_batch_device", "tok_pretokenize", "tok_pretokenize_batch",
            "tok_last_error", "tok_error_offset", "tok_content_hash", "tok_set_timing", "tok_stage_times",
-           "tok_launch_count", "tok_free", "tok_pretokenize_device_noalloc", "tok_debug_fail_alloc"]
+           "tok_launch_count", "tok_free", "tok_pretokenize_device_noalloc", "tok_debug_fail_alloc",
+           "tok_debug_grid_wait"]
 
 
 class TokError(RuntimeError):
@@ -87,6 +88,8 @@ def lib():
     L.tok_launch_count.restype = ctypes.c_uint64
     L.tok_debug_fail_alloc.argtypes = [P, U32]
     L.tok_debug_fail_alloc.restype = ctypes.c_int
+    L.tok_debug_grid_wait.argtypes = [P, U32, U32]
+    L.tok_debug_grid_wait.restype = ctypes.c_int
     L.tok_free.argtypes = [P]
     L.tok_free.restype = None
     for fn in ("tok_load", "tok_encode", "tok_encode_offsets", "tok_repair_append", "tok_encode_batch", "tok_encode_device",

@@ -33,6 +33,8 @@ struct ByteStringHash {
 
 }  // namespace
 
+constexpr unsigned long long kDefaultWaitNs = 4000000000ull;  // 4 s
+
 struct tok_handle {
   int dev = 0;
   int n_sms = 1;
@@ -76,6 +78,11 @@ struct tok_handle {
   // test hook (tok_debug_fail_alloc): the allocation that fails, counted
   // from 1 = the next one; 0 = none
   uint32_t fail_alloc_in = 0;
+  // limit of a device-side wait (the grid barriers of the BPE kernel), and
+  // the test hook tok_debug_grid_wait: arrivals a grid barrier waits for
+  // beyond the CTAs that come
+  unsigned long long wait_ns = kDefaultWaitNs;
+  uint32_t grid_extra = 0;
 };
 
 namespace {
@@ -276,6 +283,8 @@ int run_chain(tok_handle* h, Call c, cudaStream_t s) {
     const bool tm = h->timing;
     clear_counters(h, c.n, s);
     c.settle = 1;
+    c.wait_ns = h->wait_ns;
+    c.grid_extra = h->grid_extra;
     if (tm) cudaEventRecord(h->ev[0], s);
     launch_boundaries(c, h->ws, h->v, s);
     if (tm) cudaEventRecord(h->ev[1], s);
@@ -634,6 +643,13 @@ uint64_t tok_launch_count(tok_handle* h) { return h ? h->launches : 0; }
 int tok_debug_fail_alloc(tok_handle* h, uint32_t k) {
   if (!h) return TOK_EINVAL;
   h->fail_alloc_in = k;
+  return TOK_OK;
+}
+
+int tok_debug_grid_wait(tok_handle* h, uint32_t extra, uint32_t wait_ms) {
+  if (!h) return TOK_EINVAL;
+  h->grid_extra = extra;
+  h->wait_ns = wait_ms ? (unsigned long long)wait_ms * 1000000ull : kDefaultWaitNs;
   return TOK_OK;
 }
 

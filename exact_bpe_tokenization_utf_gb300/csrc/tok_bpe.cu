@@ -249,7 +249,7 @@ __device__ int global_engine(const Call& c, const Workspace& ws, const DevVocab&
     __syncthreads();
     cur ^= 1;
     m = newm;
-    if (sweep == m0 && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);
+    if (sweep == m0 && tid == 0) set_error(ws.st, ST_EINTERNAL);
   }
   const uint32_t* S = cur ? S1 : S0;
   for (int i = tid; i < m; i += T) out[i] = (int32_t)S[i];
@@ -402,7 +402,7 @@ __device__ void cta_fragment(const Call& c, const Workspace& ws, const DevVocab&
     if (tid == 0) *sflags = 0;
     m = newm;
     __syncthreads();
-    if (sweep == M && tid == 0) atomicExch(&ws.st->code, ST_EINTERNAL);  // cannot happen: every sweep merges
+    if (sweep == M && tid == 0) set_error(ws.st, ST_EINTERNAL);  // cannot happen: every sweep merges
   }
   for (int i = tid; i < m; i += T) ws.tok[a + i] = (int32_t)C.sym[i];
   if (tid == 0) {
@@ -428,7 +428,7 @@ __device__ __forceinline__ int warp_sweeps(WarpBuf& B, const DevVocab& V, DevSta
     const bool mrg = mergeable(k);
     if (!__any_sync(FULL, mrg)) break;
     if (sweep == 32) {  // cannot happen: every sweep merges at least one pair
-      if (lane == 0) atomicExch(&st->code, ST_EINTERNAL);
+      if (lane == 0) set_error(st, ST_EINTERNAL);
       break;
     }
     uint32_t kl = __shfl_up_sync(FULL, k, 1);
@@ -621,7 +621,7 @@ __device__ __forceinline__ int warp_steps(WarpBuf& B, const DevVocab& V, DevStat
     const bool mrg = mergeable(k);  // a retired lane holds KR_WALL
     if (!__any_sync(FULL, mrg)) break;
     if (step == 32) {  // cannot happen: every step merges a pair of some fragment
-      if (lane == 0) atomicExch(&st->code, ST_EINTERNAL);
+      if (lane == 0) set_error(st, ST_EINTERNAL);
       break;
     }
     // the fragment's leftmost lowest-rank pair: one reduction over its lanes
@@ -755,10 +755,17 @@ __device__ void short_batch(const Call& c, const Workspace& ws, const DevVocab& 
   __syncwarp();
 }
 
+struct GridParams {         // the grid engine's copy of the kernel parameters
+  Call c;
+  Workspace ws;
+  DevVocab V;
+};
+
 struct EngineSmem {
   union {
     CtaBatch cb;
     WarpBuf wb[B_THREADS / 32];
+    GridParams gp;
   } u;
   uint8_t owner[B_THREADS / 32][SB_MAX];
   int scan[B_THREADS / 32];
@@ -766,8 +773,399 @@ struct EngineSmem {
   int sflags;
   uint32_t idx;
   uint32_t nq[3];           // queue sizes: long, 33..B_CAP bytes, short batches
+  int gmode;                // the long fragments go to the grid engine
+  uint32_t gcnt[B_THREADS / 32];  // grid engine: live symbols of each warp's unit
   unsigned long long end;
 };
+
+// End of a long fragment: from its queue entry, or the next fragment start
+// after it (or the text end).  All threads of the CTA; the same value in each.
+__device__ __forceinline__ long long long_end(const Call& c, const Workspace& ws, const Frag& f,
+                                               unsigned long long* send) {
+  const int tid = threadIdx.x, T = B_THREADS;
+  if (tid == 0) *send = f.len > 0 ? (unsigned long long)(f.start + f.len) : (unsigned long long)c.n;
+  __syncthreads();
+  if (f.len <= 0) {
+    const long long w0 = (f.start + 1) >> 5, wn = (c.n + 31) >> 5;
+    for (long long base = w0; base < wn; base += T) {
+      const long long wi = base + tid;
+      if (wi < wn) {
+        uint32_t wv = ws.pstart[wi];
+        if (wi == w0) wv &= ~0u << ((f.start + 1) & 31);
+        if (wi * 32 + 32 > c.n) wv &= (c.n - wi * 32 >= 32) ? ~0u : ((1u << (c.n - wi * 32)) - 1u);
+        if (wv) atomicMin(send, (unsigned long long)(wi * 32 + __ffs(wv) - 1));
+      }
+      __syncthreads();
+      const bool found = *send < (unsigned long long)c.n;
+      __syncthreads();
+      if (found) break;
+    }
+  }
+  const long long e = (long long)*send;
+  __syncthreads();
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+// Grid engine: every fragment longer than B_CAP bytes at once, on the first
+// c.grid_ctas CTAs of K3b.  The launch is cooperative, so every CTA of the
+// grid is resident and these CTAs can wait for one another at grid barriers.
+//
+// The fragments lie end to end in one coordinate space, fragment j at
+// [o_j, o_j + m_j) in queue order.  A symbol stays at the coordinate of its
+// first byte: L[c] is its byte length (0: c lies inside another symbol), the
+// next symbol starts at c + L[c] and the previous one at c - B[c] (B[c] = 0:
+// c starts its fragment), and K[c] is the key of the pair (c, next), KR_WALL
+// at the last symbol of a fragment.  A merge rewrites the two symbols and
+// the links of their neighbours only, so nothing is compacted between
+// sweeps.  A sweep is the sweep of the global-memory engine (monotone
+// vocabularies) in three steps, a grid barrier after each:
+//   P1  stale keys are looked up; a mergeable pair whose left neighbour pair
+//       is another merge starts a run of equal-rank pairs
+//   P2  each pair's run start (a max-scan over the whole space, carried from
+//       unit to unit through the last run start of each unit) and its safe
+//       flag
+//   P3  the safe pairs merge
+// Warp w of CTA b owns the coordinates of unit u = 4b + w, [u*R, (u+1)*R)
+// with R a multiple of 32, in tiles of 32.  Symbols and links are written by
+// other CTAs between barriers, so they are read past L1 (ld.global.cg).
+
+constexpr unsigned long long GRID_MIN_INNER = 16ull * CHUNK;  // start-free chunk bytes from which the grid engine runs
+constexpr int GRID_PER_SM = 8;                                // CTAs per SM in the grid engine
+constexpr int GRID_UNITS = B_THREADS / 32;                    // units (warps) per CTA
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Barrier of the n CTAs of the grid engine; every thread of each CTA calls
+// it.  Thread 0 arrives on a counter and, unless it is the last arrival,
+// waits for the last one to advance the generation: for at most the call's
+// wait limit, after which it marks the call ST_ETIMEOUT and raises the abort
+// flag, which ends every other CTA's wait too.  False in every CTA once the
+// flag is up.
+__device__ bool grid_barrier(const Call& c, DevStatus* st, uint32_t n, int* sflag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const uint32_t gen = ld_acquire(&st->gb_gen);
+    __threadfence();
+    if (atomicAdd(&st->gb_count, 1u) == n - 1u) {
+      atomicExch(&st->gb_count, 0u);
+      st_release(&st->gb_gen, gen + 1u);
+    } else {
+      const unsigned long long t0 = global_ns();
+      for (uint32_t it = 0; ld_acquire(&st->gb_gen) == gen; ++it) {
+        if (ld_acquire(&st->g_abort) || it >= (1u << 28) || ((it & 31u) == 31u && global_ns() - t0 > c.wait_ns)) {
+          atomicExch(&st->g_abort, 1u);
+          set_error(st, ST_ETIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    __threadfence();
+    if (ld_acquire(&st->g_abort)) ok = 0;
+    *sflag = ok;
+  }
+  __syncthreads();
+  return *sflag != 0;
+}
+
+// Is the pair at coordinate i (rank k, run start u) safe to merge now?  The
+// rule of pair_safe over the linked symbols.
+__device__ __forceinline__ bool pair_safe_linked(const uint32_t* S, const uint16_t* L, const uint16_t* B,
+                                                 const unsigned long long* K, const DevVocab& V, long long i,
+                                                 long long u, uint32_t k) {
+  const int bu = __ldcg(B + u);
+  if (bu) {
+    long long q = u - bu;
+    if (kr_rank(__ldcg(K + q)) < k) return false;
+    const int lim = V.max_left[__ldcg(S + u)];
+    int cum = __ldcg(L + q);
+    for (int bq = __ldcg(B + q); bq; bq = __ldcg(B + q)) {
+      const long long q2 = q - bq;
+      cum += __ldcg(L + q2);
+      if (cum > lim) break;
+      if (kr_rank(__ldcg(K + q2)) < k) return false;
+      q = q2;
+    }
+  }
+  const long long j1 = i + __ldcg(L + i);
+  const uint32_t kr = kr_rank(__ldcg(K + j1));
+  if (kr != RANK_WALL) {
+    if (kr < k) return false;
+    const int lim = V.max_right[__ldcg(S + j1)];
+    long long q = j1 + __ldcg(L + j1);
+    int cum = __ldcg(L + q);
+    for (;;) {
+      const uint32_t kq = kr_rank(__ldcg(K + q));
+      if (kq == RANK_WALL) break;
+      const long long q2 = q + __ldcg(L + q);
+      cum += __ldcg(L + q2);
+      if (cum > lim) break;
+      if (kq < k) return false;
+      q = q2;
+    }
+  }
+  return true;
+}
+
+// The long fragments' ids to their byte offsets in ws.tok (and their counts
+// to fcnt, ctot and gtot), by the first c.grid_ctas CTAs together.  The
+// arrays are the global-memory engine's: symbols e_sym[0], lengths
+// e_len[0], links e_len[1], keys e_kr[0] (after the sweeps: each live
+// symbol's rank among all live symbols, bit 63 set at a fragment's last),
+// flags e_fl, fragment of each coordinate e_rs; e_kr[1] holds the fragment
+// offsets (nlong + 1), the rank of each fragment's first symbol (nlong), the
+// last run start of each unit (4 per CTA) and the live symbols of each CTA.
+__device__ __noinline__ void grid_engine(uint32_t nlong, EngineSmem& S) {
+  const Call& c = S.u.gp.c;
+  const Workspace& ws = S.u.gp.ws;
+  const DevVocab& V = S.u.gp.V;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t P = (uint32_t)c.grid_ctas, nb = P + c.grid_extra, b = blockIdx.x;
+  DevStatus* st = ws.st;
+  uint32_t* Sy = ws.e_sym[0];
+  uint16_t* Ln = ws.e_len[0];
+  uint16_t* Bk = ws.e_len[1];
+  unsigned long long* K = ws.e_kr[0];
+  uint8_t* F = ws.e_fl;
+  int32_t* fid = ws.e_rs;
+  unsigned long long* off = ws.e_kr[1];
+  unsigned long long* fbase = off + nlong + 1;
+  long long* urs = reinterpret_cast<long long*>(fbase + nlong);
+  unsigned long long* ccnt = reinterpret_cast<unsigned long long*>(urs + (size_t)P * GRID_UNITS);
+  const long long ngroups = ((long long)P * GRID_UNITS + 31) / 32;
+  long long* ugrp = reinterpret_cast<long long*>(ccnt + P);  // two buffers of ngroups
+
+  // every fragment's length; its id count stays 0 (nothing to emit) unless
+  // the engine finishes
+  for (uint32_t j = b; j < nlong; j += P) {
+    const Frag f = ws.longq[j];
+    const long long e = long_end(c, ws, f, &S.end);
+    if (tid == 0) {
+      ws.longq[j].len = e - f.start;
+      ws.fcnt[f.start] = 0;
+    }
+  }
+  if (!grid_barrier(c, st, nb, &S.sflags)) return;
+  // their offsets, in queue order: every CTA computes them and stores the
+  // same values (no barrier needed before its own reads)
+  unsigned long long run = 0;
+  for (uint32_t j0 = 0; j0 < nlong; j0 += B_THREADS) {
+    const uint32_t j = j0 + tid;
+    const unsigned long long m = j < nlong ? (unsigned long long)__ldcg(&ws.longq[j].len) : 0ull;
+    unsigned long long tot = 0;
+    const unsigned long long ex = block_excl_sum64(m, &tot, S.scan64);
+    if (j < nlong) __stcg(off + j, run + ex);
+    run += tot;
+  }
+  if (tid == 0) __stcg(off + nlong, run);
+  __syncthreads();
+  const long long M = (long long)run;
+  const long long nunits = (long long)P * GRID_UNITS;
+  const long long R = ((M + nunits - 1) / nunits + 31) & ~31ll;
+  const long long u = (long long)b * GRID_UNITS + warp;
+  const long long ulo = min(u * R, M), uhi = min(ulo + R, M);
+
+  // the bytes' symbols
+  for (long long t = ulo; t < uhi; t += 32) {
+    const long long x = t + lane;
+    if (x < uhi) {
+      uint32_t lo = 0, hi = nlong;  // off[lo] <= x < off[hi]
+      while (hi - lo > 1u) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if ((long long)__ldcg(off + mid) <= x) lo = mid;
+        else hi = mid;
+      }
+      const long long o = (long long)__ldcg(off + lo), e = (long long)__ldcg(off + lo + 1);
+      const long long a = __ldcg(&ws.longq[lo].start);
+      __stcg(Sy + x, (uint32_t)__ldg(V.byte_id + c.text[a + (x - o)]));
+      __stcg(Ln + x, (uint16_t)1);
+      __stcg(Bk + x, (uint16_t)(x == o ? 0 : 1));
+      __stcg(K + x, x + 1 == e ? KR_WALL : KR_NEED);
+      __stcg(fid + x, (int32_t)lo);
+    }
+  }
+  if (lane == 0 && (u & 31) == 0) __stcg(ugrp + (u >> 5), -1ll);
+  if (!grid_barrier(c, st, nb, &S.sflags)) return;
+
+  for (uint32_t sweep = 0;; ++sweep) {
+    // P1: keys, run starts; the live symbols of the unit
+    long long last = -1;
+    bool any = false;
+    uint32_t cnt = 0;
+    long long* grp = ugrp + (sweep & 1) * ngroups;
+    for (long long t = ulo; t < uhi; t += 32) {
+      const long long x = t + lane;
+      bool rs = false;
+      int l = 0;
+      if (x < uhi) {
+        l = __ldcg(Ln + x);
+        if (l) {
+          unsigned long long k = __ldcg(K + x);
+          if (kr_rank(k) == RANK_NEED || mergeable(kr_rank(k))) {
+            const uint32_t sx = __ldcg(Sy + x), sn = __ldcg(Sy + x + l);
+            if (kr_rank(k) == RANK_NEED) {
+              k = merge_lookup(V, sx, sn);
+              __stcg(K + x, k);
+            }
+            if (mergeable(kr_rank(k))) {
+              any = true;
+              const int bx = __ldcg(Bk + x);
+              rs = bx == 0 || sn != sx || __ldcg(Sy + x - bx) != sx;
+            }
+          }
+          __stcg(F + x, (uint8_t)(rs ? 2 : 0));
+        }
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, rs);
+      if (bal) last = t + 31 - __clz(bal);
+      cnt += __popc(__ballot_sync(0xffffffffu, l != 0));
+    }
+    if (lane == 0) {
+      __stcg(urs + u, last);
+      if (last >= 0) atomicMax(grp + (u >> 5), last);
+      // the other buffer, read in the previous sweep, serves the next one
+      if ((u & 31) == 0) __stcg(ugrp + ((sweep + 1) & 1) * ngroups + (u >> 5), -1ll);
+      S.gcnt[warp] = cnt;
+    }
+    if (__syncthreads_or(any) && tid == 0) atomicOr(&st->g_any[sweep % 3], 1u);
+    if (tid == 0) {
+      unsigned long long tot = 0;
+      for (int w = 0; w < GRID_UNITS; ++w) tot += S.gcnt[w];
+      __stcg(ccnt + b, tot);
+    }
+    if (b == 0 && tid == 0) atomicExch(&st->g_any[(sweep + 1) % 3], 0u);
+    if (!grid_barrier(c, st, nb, &S.sflags)) return;
+    if (!ld_acquire(&st->g_any[sweep % 3])) break;
+    if (sweep >= (uint32_t)min(M, 1ll << 30)) {
+      if (tid == 0) set_error(st, ST_EINTERNAL);
+      return;
+    }
+    // P2: run starts, safe flags.  The run start carried into the unit:
+    // the last one of the nearest earlier unit of its group of 32 units
+    // that has one, else the largest of the nearest earlier group that has
+    // one
+    long long carry = -1;
+    if (ulo < uhi) {
+      const long long g = u >> 5, v = u - 1 - lane;
+      long long r = v >= (g << 5) ? __ldcg(urs + v) : -1ll;
+      uint32_t hit = __ballot_sync(0xffffffffu, r >= 0);
+      for (long long g0 = g - 1; !hit && g0 >= 0; g0 -= 32) {
+        const long long gg = g0 - lane;
+        r = gg >= 0 ? __ldcg(grp + gg) : -1ll;
+        hit = __ballot_sync(0xffffffffu, r >= 0);
+      }
+      if (hit) carry = __shfl_sync(0xffffffffu, r, __ffs(hit) - 1);
+    }
+    for (long long t = ulo; t < uhi; t += 32) {
+      const long long x = t + lane;
+      int l = 0, f = 0;
+      unsigned long long k = 0;
+      if (x < uhi) {
+        l = __ldcg(Ln + x);
+        if (l) {
+          f = __ldcg(F + x);
+          k = __ldcg(K + x);
+        }
+      }
+      long long rsx = (f & 2) ? x : -1ll;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, rsx, o);
+        if (lane >= o) rsx = max(rsx, y);
+      }
+      rsx = max(rsx, carry);
+      carry = __shfl_sync(0xffffffffu, rsx, 31);
+      if (l) {
+        bool safe = false;
+        const uint32_t kr = kr_rank(k);
+        if (mergeable(kr)) {
+          // pairs of a run alternate from its start; the run's symbols all
+          // have this symbol's length
+          const unsigned long long d = (unsigned long long)(x - rsx);
+          const unsigned long long q = d < 0x80000000ull ? (unsigned long long)((uint32_t)d / (uint32_t)l)
+                                                         : d / (unsigned long long)l;
+          safe = !(q & 1ull) && pair_safe_linked(Sy, Ln, Bk, K, V, x, rsx, kr);
+        }
+        __stcg(F + x, (uint8_t)(safe ? 1 : 0));
+      }
+    }
+    if (!grid_barrier(c, st, nb, &S.sflags)) return;
+    // P3: merges
+    for (long long t = ulo; t < uhi; t += 32) {
+      const long long x = t + lane;
+      if (x < uhi) {
+        const int l = __ldcg(Ln + x);
+        if (l && (__ldcg(F + x) & 1)) {
+          const long long j = x + l;
+          const int lj = __ldcg(Ln + j);
+          const bool wall = kr_rank(__ldcg(K + j)) == RANK_WALL;
+          const int nl = l + lj;
+          __stcg(Sy + x, kr_result(__ldcg(K + x)));
+          __stcg(Ln + x, (uint16_t)nl);
+          __stcg(Ln + j, (uint16_t)0);
+          __stcg(K + x, wall ? KR_WALL : KR_NEED);
+          if (!wall) __stcg(Bk + j + lj, (uint16_t)nl);
+          const int bx = __ldcg(Bk + x);
+          if (bx) __stcg(K + x - bx, KR_NEED);
+        }
+      }
+    }
+    if (!grid_barrier(c, st, nb, &S.sflags)) return;
+  }
+
+  // each live symbol's rank (the live counts of the last P1 are final);
+  // each fragment's first rank
+  unsigned long long pre = 0;
+  for (uint32_t y = tid; y < b; y += B_THREADS) pre += __ldcg(ccnt + y);
+  unsigned long long cta_pre = 0;
+  block_excl_sum64(pre, &cta_pre, S.scan64);
+  unsigned long long rank = cta_pre;
+  for (int w = 0; w < warp; ++w) rank += S.gcnt[w];
+  for (long long t = ulo; t < uhi; t += 32) {
+    const long long x = t + lane;
+    const bool live = x < uhi && __ldcg(Ln + x) != 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, live);
+    if (live) {
+      const unsigned long long r = rank + __popc(bal & ((1u << lane) - 1u));
+      const bool lastsym = kr_rank(__ldcg(K + x)) == RANK_WALL;
+      __stcg(K + x, r | (lastsym ? (1ull << 63) : 0ull));
+      if (__ldcg(Bk + x) == 0) __stcg(fbase + __ldcg(fid + x), r);
+    }
+    rank += __popc(bal);
+  }
+  if (!grid_barrier(c, st, nb, &S.sflags)) return;
+  // ids
+  for (long long t = ulo; t < uhi; t += 32) {
+    const long long x = t + lane;
+    if (x < uhi && __ldcg(Ln + x) != 0) {
+      const int32_t j = __ldcg(fid + x);
+      const long long a = __ldcg(&ws.longq[j].start);
+      const unsigned long long kx = __ldcg(K + x);
+      const long long k = (long long)((kx & ~(1ull << 63)) - __ldcg(fbase + j));
+      ws.tok[a + k] = (int32_t)__ldcg(Sy + x);
+      if (kx >> 63) {
+        ws.fcnt[a] = (int32_t)(k + 1);
+        atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)(k + 1));
+        atomicAdd(&ws.gtot[a / BCHUNK / CTOT_GROUP], (uint32_t)(k + 1));
+      }
+    }
+  }
+}
 
 // K3b: a persistent grid.  Longest work first: fragments of more than B_CAP
 // bytes (global-memory engine, taken one at a time), then those of 33..B_CAP
@@ -789,73 +1187,102 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
     S.nq[0] = st->long_count;
     S.nq[1] = st->wide_count;
     S.nq[2] = st->sbatch_count;
+    // many long-fragment bytes: the grid engine takes them all
+    S.gmode = S.nq[0] && V.monotone && c.grid_ctas > 0 && st->inner_bytes >= GRID_MIN_INNER;
   }
   __syncthreads();
   const uint32_t nlong = S.nq[0];
-  while (nlong) {
-    // one thread decides for the CTA (the loop has barriers); the plain read
-    // first keeps CTAs without work off the contended counter
-    if (tid == 0)
-      S.idx = *(volatile const uint32_t*)&st->long_taken < nlong ? atomicAdd(&st->long_taken, 1u) : nlong;
-    __syncthreads();
-    const uint32_t idx = S.idx;
-    __syncthreads();
-    if (idx >= nlong) break;
-    const Frag f = ws.longq[idx];
-    // end: known from the queue entry, or the next fragment start after
-    // f.start (or the text end)
-    if (tid == 0) S.end = f.len > 0 ? (unsigned long long)(f.start + f.len) : (unsigned long long)c.n;
-    __syncthreads();
-    if (f.len <= 0) {
-      const long long w0 = (f.start + 1) >> 5, wn = (c.n + 31) >> 5;
-      for (long long base = w0; base < wn; base += T) {
-        const long long wi = base + tid;
-        if (wi < wn) {
-          uint32_t wv = ws.pstart[wi];
-          if (wi == w0) wv &= ~0u << ((f.start + 1) & 31);
-          if (wi * 32 + 32 > c.n) wv &= (c.n - wi * 32 >= 32) ? ~0u : ((1u << (c.n - wi * 32)) - 1u);
-          if (wv) atomicMin(&S.end, (unsigned long long)(wi * 32 + __ffs(wv) - 1));
-        }
-        __syncthreads();
-        const bool found = S.end < (unsigned long long)c.n;
-        __syncthreads();
-        if (found) break;
+  const uint32_t c0 = S.gmode ? (uint32_t)c.grid_ctas : 0u;  // CTAs [c0, grid) take the other queues
+  if (c0) {
+    if (blockIdx.x < c0) {
+      if (tid == 0) {
+        S.u.gp.c = c;
+        S.u.gp.ws = ws;
+        S.u.gp.V = V;
       }
+      __syncthreads();
+      grid_engine(nlong, S);
+      return;
     }
-    const long long a = f.start;
-    const int m = global_engine(c, ws, V, a, (int)((long long)S.end - a), ws.tok + a, S.scan, S.scan64);
-    if (tid == 0) {
-      ws.fcnt[a] = m;
-      atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
-      atomicAdd(&ws.gtot[a / BCHUNK / CTOT_GROUP], (uint32_t)m);
+  } else {
+    while (nlong) {
+      // one thread decides for the CTA (the loop has barriers); the plain
+      // read first keeps CTAs without work off the contended counter
+      if (tid == 0)
+        S.idx = *(volatile const uint32_t*)&st->long_taken < nlong ? atomicAdd(&st->long_taken, 1u) : nlong;
+      __syncthreads();
+      const uint32_t idx = S.idx;
+      __syncthreads();
+      if (idx >= nlong) break;
+      const Frag f = ws.longq[idx];
+      const long long a = f.start;
+      const long long e = long_end(c, ws, f, &S.end);
+      const int m = global_engine(c, ws, V, a, (int)(e - a), ws.tok + a, S.scan, S.scan64);
+      if (tid == 0) {
+        ws.fcnt[a] = m;
+        atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)m);
+        atomicAdd(&ws.gtot[a / BCHUNK / CTOT_GROUP], (uint32_t)m);
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
+  const uint32_t G = gridDim.x - c0, bb = blockIdx.x - c0;
   const uint32_t nwide = S.nq[1];
-  for (uint32_t i = blockIdx.x; i < nwide; i += gridDim.x) {
+  for (uint32_t i = bb; i < nwide; i += G) {
     const Frag f = ws.wq[i];
     cta_fragment(c, ws, V, f.start, (int)f.len, S.u.cb, S.scan, S.scan64, &S.sflags);
   }
   __syncthreads();
   const uint32_t nbat = S.nq[2];
-  const uint32_t nwarps = gridDim.x * (T / 32);
-  const uint32_t gw = (gridDim.x - 1 - blockIdx.x) * (T / 32) + warp;
+  const uint32_t nwarps = G * (T / 32);
+  const uint32_t gw = (G - 1 - bb) * (T / 32) + warp;
   for (uint32_t b = gw; b < nbat; b += nwarps) short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
 }
 
 
-void launch_bpe_engine(const Call& c, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
-  // 16 CTAs of 32 registers per SM; a programmatic dependent of the boundary
-  // kernel (its CTAs are scheduled while that grid's last CTAs finish)
+void launch_bpe_engine(const Call& call, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
+  // a persistent grid of as many CTAs as fit at once (16 of 32 registers per
+  // SM), launched cooperatively (all resident together: the grid engine's
+  // CTAs wait for one another) and as a programmatic dependent of the
+  // boundary kernel (its CTAs are scheduled while that grid's last CTAs
+  // finish)
+  constexpr int kMaxDev = 64;
+  static int per_sm[kMaxDev] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int& ps = per_sm[dev >= 0 && dev < kMaxDev ? dev : 0];
+  if (!ps) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_bpe_engine, B_THREADS, 0) != cudaSuccess) {
+      cudaGetLastError();
+      occ = 1;
+    }
+    ps = occ < 1 ? 1 : (occ > 16 ? 16 : occ);
+  }
+  const unsigned long long grid = (unsigned long long)n_sms * ps;
+  Call c = call;
+  // the grid engine keeps in e_kr[1] two words per long fragment and one
+  // more, then per CTA one word per unit, one for the CTA and two buffers of
+  // one word per 32 units (at most 2 + 1 per CTA with GRID_UNITS <= 16)
+  static_assert(GRID_UNITS <= 16, "two group words per CTA at most");
+  const unsigned long long lq = w.cap_bytes / (B_CAP + 1) + w.cap_bytes / BCHUNK + 256;
+  const unsigned long long words = w.cap_bytes + 256;
+  const unsigned long long room = words > 2 * lq + 3 ? (words - 2 * lq - 3) / (GRID_UNITS + 2) : 0;
+  unsigned long long gc = (unsigned long long)n_sms * (ps < GRID_PER_SM ? ps : GRID_PER_SM);
+  if (gc > room) gc = room;
+  if (gc + 1 > grid) gc = grid - 1;
+  c.grid_ctas = (int)gc;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(n_sms * 16));
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(B_THREADS);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaLaunchKernelEx(&cfg, k_bpe_engine, c, w, v);
 }
 

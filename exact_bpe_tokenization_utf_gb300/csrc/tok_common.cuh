@@ -111,6 +111,10 @@ struct DevStatus {
   uint32_t sbatch_count, sbatch_taken;  // warp batches of short fragments
   uint32_t wide_count, wide_taken;      // fragments of 33..B_CAP bytes
   uint32_t long_count, long_taken;      // longer fragments
+  unsigned long long inner_bytes;       // bytes of the chunks that hold no fragment start (all in long fragments)
+  // the grid engine of K3b: its barrier (arrivals, generation), the flag a
+  // CTA sets when it gave up waiting, and per sweep whether a pair merges
+  uint32_t gb_count, gb_gen, g_abort, g_any[3];
   uint32_t pad[2];
 };
 static_assert(sizeof(DevStatus) % 16 == 0, "the group totals follow the status");
@@ -160,6 +164,9 @@ struct Call {
   long long* user_status;     // device int64[4] or nullptr
   int settle;                 // K2 also settles fragments and fills the queues (encode calls)
   int out_host;               // `out` is pinned host memory (mapped): K5 stages a chunk's ids for coalesced stores
+  int grid_ctas;              // K3b CTAs that run the grid engine (0: none)
+  uint32_t grid_extra;        // arrivals a grid barrier waits for beyond grid_ctas (0; a test sets 1)
+  unsigned long long wait_ns; // limit of a device-side wait, in ns of the global timer
   Prefetch pf[4];             // whole-token table, token bytes, merge table, byte-pair bits
 };
 
@@ -261,6 +268,9 @@ __device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s,
   const uint32_t slot = whole_first_slot(v, bytes_hash(head, s, len));
   return whole_lookup_at(v, s, len, head, slot, __ldg(reinterpret_cast<const uint4*>(v.whole + slot)));
 }
+
+// Record a device-side error of the call; the first error stays.
+__device__ __forceinline__ void set_error(DevStatus* st, int32_t code) { atomicCAS(&st->code, (int32_t)ST_OK, code); }
 
 __device__ __forceinline__ uint32_t kr_rank(unsigned long long kr) { return (uint32_t)(kr >> 32); }
 __device__ __forceinline__ uint32_t kr_result(unsigned long long kr) { return (uint32_t)kr; }

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
   for (int q = 0; q < 4; ++q) {
     if (!((mine >> q) & 1u)) { cn[q] = 0; continue; }
     if (cn[q] < 1 || cn[q] > c.n - (r0 + q0 + q)) {
-      atomicExch(&st->code, ST_EINTERNAL);
+      set_error(st, ST_EINTERNAL);
       cn[q] = 0;
     }
     ids += cn[q];
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
   unsigned long long base = 0;  // ids before this chunk
   int o = block_excl_sum_and_total(ids, part, &total, &base, scan, scan64);
   if ((uint32_t)total != my_total) {  // the counts disagree with the chunk total: a bug upstream
-    if (tid == 0) atomicExch(&st->code, ST_EINTERNAL);
+    if (tid == 0) set_error(st, ST_EINTERNAL);
     total = 0;
   }
   // ids in text order: fragments of up to 8 ids by their thread, longer ones
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
           big_k[bi] = k;
           big_o[bi] = o;
         } else {
-          atomicExch(&st->code, ST_EINTERNAL);
+          set_error(st, ST_EINTERNAL);
         }
       }
       o += k;

@@ -261,6 +261,17 @@ uint64_t tok_launch_count(tok_handle* h);
  * Errors: TOK_EINVAL (h is NULL). */
 int tok_debug_fail_alloc(tok_handle* h, uint32_t k);
 
+/* tok_debug_grid_wait -- test hook for the device-side wait limit.  The BPE
+ * kernel encodes many long fragments (more than 256 bytes) on a group of its
+ * CTAs that wait for one another at grid barriers; each wait gives up after
+ * a time limit (4 s by default) and the call then returns TOK_ETIMEOUT with
+ * the device context intact.  From now on every such barrier of h waits for
+ * `extra` arrivals beyond the CTAs that come (extra = 1: a barrier that never
+ * completes), and the limit is wait_ms milliseconds (0: the default).
+ * extra = 0, wait_ms = 0 restores normal operation.  Host-side bookkeeping
+ * only.  Errors: TOK_EINVAL (h is NULL). */
+int tok_debug_grid_wait(tok_handle* h, uint32_t extra, uint32_t wait_ms);
+
 /* tok_free -- release the handle and its device memory.  NULL is ignored. */
 void tok_free(tok_handle* h);
 
