@@ -761,11 +761,28 @@ struct GridParams {         // the grid engine's copy of the kernel parameters
   DevVocab V;
 };
 
+// One warp's window of the grid engine's coordinate space for the safe-pair
+// walks: GW consecutive coordinates, GW_BEHIND of them before the warp's
+// current tile of 32, held as a ring (coordinate p in slot p mod GW).
+constexpr int GW = 128;
+constexpr int GW_BEHIND = 32;
+struct GridWin {
+  uint32_t rank[GW];        // rank of the pair (p, next)
+  uint32_t sym[GW];
+  uint16_t len[GW];
+  uint16_t back[GW];
+};
+
+struct GridSmem {
+  GridParams gp;
+  GridWin win[B_THREADS / 32];
+};
+
 struct EngineSmem {
   union {
     CtaBatch cb;
     WarpBuf wb[B_THREADS / 32];
-    GridParams gp;
+    GridSmem g;
   } u;
   uint8_t owner[B_THREADS / 32][SB_MAX];
   int scan[B_THREADS / 32];
@@ -830,7 +847,7 @@ __device__ __forceinline__ long long long_end(const Call& c, const Workspace& ws
 // with R a multiple of 32, in tiles of 32.  Symbols and links are written by
 // other CTAs between barriers, so they are read past L1 (ld.global.cg).
 
-constexpr unsigned long long GRID_MIN_INNER = 16ull * CHUNK;  // start-free chunk bytes from which the grid engine runs
+constexpr long long GRID_MIN_LONG = 32 * 1024;  // long-fragment bytes from which the grid engine runs
 constexpr int GRID_PER_SM = 8;                                // CTAs per SM in the grid engine
 constexpr int GRID_UNITS = B_THREADS / 32;                    // units (warps) per CTA
 
@@ -883,47 +900,99 @@ __device__ bool grid_barrier(const Call& c, DevStatus* st, uint32_t n, int* sfla
   return *sflag != 0;
 }
 
-// Is the pair at coordinate i (rank k, run start u) safe to merge now?  The
-// rule of pair_safe over the linked symbols.
-__device__ __forceinline__ bool pair_safe_linked(const uint32_t* S, const uint16_t* L, const uint16_t* B,
-                                                 const unsigned long long* K, const DevVocab& V, long long i,
-                                                 long long u, uint32_t k) {
-  const int bu = __ldcg(B + u);
-  if (bu) {
-    long long q = u - bu;
-    if (kr_rank(__ldcg(K + q)) < k) return false;
-    const int lim = V.max_left[__ldcg(S + u)];
-    int cum = __ldcg(L + q);
-    for (int bq = __ldcg(B + q); bq; bq = __ldcg(B + q)) {
-      const long long q2 = q - bq;
-      cum += __ldcg(L + q2);
+// The grid engine's symbol arrays (coordinate space of the long fragments).
+struct GridSyms {
+  uint32_t* S;
+  uint16_t* L;
+  uint16_t* B;
+  unsigned long long* K;
+};
+
+// What the safe-pair walks read of the symbol at coordinate p: from the
+// warp's window [wlo, wlo + GW) when p lies in it, else from global memory.
+struct WinSym {
+  uint32_t rank, sym;
+  int len, back;
+};
+
+__device__ __forceinline__ WinSym win_get(const GridWin& W, long long wlo, long long p, const GridSyms& G) {
+  WinSym r;
+  const long long d = p - wlo;
+  if (d >= 0 && d < GW) {
+    const int s = (int)(p & (GW - 1));
+    r.rank = W.rank[s];
+    r.sym = W.sym[s];
+    r.len = W.len[s];
+    r.back = W.back[s];
+  } else {
+    r.rank = kr_rank(__ldcg(G.K + p));
+    r.sym = __ldcg(G.S + p);
+    r.len = __ldcg(G.L + p);
+    r.back = __ldcg(G.B + p);
+  }
+  return r;
+}
+
+// The 32 coordinates [base, base + 32) into the window (one per lane; those
+// outside [0, M) are not read).
+__device__ __forceinline__ void win_fill(GridWin& W, long long base, long long M, const GridSyms& G) {
+  const long long p = base + (threadIdx.x & 31);
+  if (p >= 0 && p < M) {
+    const int s = (int)(p & (GW - 1));
+    W.rank[s] = kr_rank(__ldcg(G.K + p));
+    W.sym[s] = __ldcg(G.S + p);
+    W.len[s] = __ldcg(G.L + p);
+    W.back[s] = __ldcg(G.B + p);
+  }
+}
+
+// Is the pair at coordinate i (length li of its left symbol, rank k, run
+// start u) safe to merge now?  The rule of pair_safe over the linked
+// symbols.
+__device__ __forceinline__ bool pair_safe_win(const GridWin& W, long long wlo, const GridSyms& G, const DevVocab& V,
+                                              long long i, int li, long long u, uint32_t k) {
+  const WinSym su = win_get(W, wlo, u, G);
+  if (su.back) {
+    long long q = u - su.back;
+    WinSym sq = win_get(W, wlo, q, G);
+    if (sq.rank < k) return false;
+    const int lim = V.max_left[su.sym];
+    int cum = sq.len;
+    while (sq.back) {
+      const long long q2 = q - sq.back;
+      const WinSym s2 = win_get(W, wlo, q2, G);
+      cum += s2.len;
       if (cum > lim) break;
-      if (kr_rank(__ldcg(K + q2)) < k) return false;
+      if (s2.rank < k) return false;
       q = q2;
+      sq = s2;
     }
   }
-  const long long j1 = i + __ldcg(L + i);
-  const uint32_t kr = kr_rank(__ldcg(K + j1));
-  if (kr != RANK_WALL) {
-    if (kr < k) return false;
-    const int lim = V.max_right[__ldcg(S + j1)];
-    long long q = j1 + __ldcg(L + j1);
-    int cum = __ldcg(L + q);
-    for (;;) {
-      const uint32_t kq = kr_rank(__ldcg(K + q));
-      if (kq == RANK_WALL) break;
-      const long long q2 = q + __ldcg(L + q);
-      cum += __ldcg(L + q2);
+  const long long j1 = i + li;
+  const WinSym s1 = win_get(W, wlo, j1, G);
+  if (s1.rank != RANK_WALL) {
+    if (s1.rank < k) return false;
+    const int lim = V.max_right[s1.sym];
+    long long q = j1 + s1.len;
+    WinSym sq = win_get(W, wlo, q, G);
+    int cum = sq.len;
+    while (sq.rank != RANK_WALL) {
+      const long long q2 = q + sq.len;
+      const WinSym s2 = win_get(W, wlo, q2, G);
+      cum += s2.len;
       if (cum > lim) break;
-      if (kq < k) return false;
+      if (sq.rank < k) return false;
       q = q2;
+      sq = s2;
     }
   }
   return true;
 }
 
 // The long fragments' ids to their byte offsets in ws.tok (and their counts
-// to fcnt, ctot and gtot), by the first c.grid_ctas CTAs together.  The
+// to fcnt, ctot and gtot), by the first c.grid_ctas CTAs: all at once when
+// they hold GRID_MIN_LONG bytes or more, else one fragment per CTA with the
+// global-memory engine.  The
 // arrays are the global-memory engine's: symbols e_sym[0], lengths
 // e_len[0], links e_len[1], keys e_kr[0] (after the sweeps: each live
 // symbol's rank among all live symbols, bit 63 set at a fragment's last),
@@ -931,9 +1000,9 @@ __device__ __forceinline__ bool pair_safe_linked(const uint32_t* S, const uint16
 // offsets (nlong + 1), the rank of each fragment's first symbol (nlong), the
 // last run start of each unit (4 per CTA) and the live symbols of each CTA.
 __device__ __noinline__ void grid_engine(uint32_t nlong, EngineSmem& S) {
-  const Call& c = S.u.gp.c;
-  const Workspace& ws = S.u.gp.ws;
-  const DevVocab& V = S.u.gp.V;
+  const Call& c = S.u.g.gp.c;
+  const Workspace& ws = S.u.g.gp.ws;
+  const DevVocab& V = S.u.g.gp.V;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t P = (uint32_t)c.grid_ctas, nb = P + c.grid_extra, b = blockIdx.x;
   DevStatus* st = ws.st;
@@ -975,6 +1044,20 @@ __device__ __noinline__ void grid_engine(uint32_t nlong, EngineSmem& S) {
   if (tid == 0) __stcg(off + nlong, run);
   __syncthreads();
   const long long M = (long long)run;
+  if (M < GRID_MIN_LONG) {
+    // few long-fragment bytes: one fragment per CTA, fragment j to CTA j mod P
+    for (uint32_t j = b; j < nlong; j += P) {
+      const long long a = __ldcg(&ws.longq[j].start), m = __ldcg(&ws.longq[j].len);
+      const int n = global_engine(c, ws, V, a, (int)m, ws.tok + a, S.scan, S.scan64);
+      if (tid == 0) {
+        ws.fcnt[a] = n;
+        atomicAdd(&ws.ctot[a / BCHUNK], (uint32_t)n);
+        atomicAdd(&ws.gtot[a / BCHUNK / CTOT_GROUP], (uint32_t)n);
+      }
+      __syncthreads();
+    }
+    return;
+  }
   const long long nunits = (long long)P * GRID_UNITS;
   const long long R = ((M + nunits - 1) / nunits + 31) & ~31ll;
   const long long u = (long long)b * GRID_UNITS + warp;
@@ -1071,15 +1154,25 @@ __device__ __noinline__ void grid_engine(uint32_t nlong, EngineSmem& S) {
       }
       if (hit) carry = __shfl_sync(0xffffffffu, r, __ffs(hit) - 1);
     }
+    // the warp's window: [wlo, wlo + GW) around its current tile
+    GridWin& W = S.u.g.win[warp];
+    const GridSyms G{Sy, Ln, Bk, K};
+    long long wlo = ulo - GW_BEHIND;
+    if (ulo < uhi) {
+#pragma unroll
+      for (int q = 0; q < GW / 32; ++q) win_fill(W, wlo + 32 * q, M, G);
+      __syncwarp();
+    }
     for (long long t = ulo; t < uhi; t += 32) {
       const long long x = t + lane;
       int l = 0, f = 0;
-      unsigned long long k = 0;
+      uint32_t kr = RANK_WALL;
       if (x < uhi) {
-        l = __ldcg(Ln + x);
+        const int s = (int)(x & (GW - 1));
+        l = W.len[s];
         if (l) {
           f = __ldcg(F + x);
-          k = __ldcg(K + x);
+          kr = W.rank[s];
         }
       }
       long long rsx = (f & 2) ? x : -1ll;
@@ -1092,17 +1185,21 @@ __device__ __noinline__ void grid_engine(uint32_t nlong, EngineSmem& S) {
       carry = __shfl_sync(0xffffffffu, rsx, 31);
       if (l) {
         bool safe = false;
-        const uint32_t kr = kr_rank(k);
         if (mergeable(kr)) {
           // pairs of a run alternate from its start; the run's symbols all
           // have this symbol's length
           const unsigned long long d = (unsigned long long)(x - rsx);
           const unsigned long long q = d < 0x80000000ull ? (unsigned long long)((uint32_t)d / (uint32_t)l)
                                                          : d / (unsigned long long)l;
-          safe = !(q & 1ull) && pair_safe_linked(Sy, Ln, Bk, K, V, x, rsx, kr);
+          safe = !(q & 1ull) && pair_safe_win(W, wlo, G, V, x, l, rsx, kr);
         }
         __stcg(F + x, (uint8_t)(safe ? 1 : 0));
       }
+      // slide the window by one tile
+      __syncwarp();
+      win_fill(W, wlo + GW, M, G);
+      wlo += 32;
+      __syncwarp();
     }
     if (!grid_barrier(c, st, nb, &S.sflags)) return;
     // P3: merges
@@ -1168,12 +1265,16 @@ __device__ __noinline__ void grid_engine(uint32_t nlong, EngineSmem& S) {
 }
 
 // K3b: a persistent grid.  Longest work first: fragments of more than B_CAP
-// bytes (global-memory engine, taken one at a time), then those of 33..B_CAP
-// bytes (shared-memory engine, fragment i to CTA i mod grid), then batches of
-// short fragments (warp step or sweep engine, batch b to warp b mod warps,
-// counted from the last CTA so that the CTAs with a 33..B_CAP-byte fragment
-// get fewer).
-// Static assignment keeps thousands of warps off one contended counter.
+// bytes (the grid engine's CTAs, or every CTA taking one at a time for the
+// global-memory engine), then those of 33..B_CAP bytes (shared-memory
+// engine, one fragment per CTA), then batches of short fragments (warp step
+// or sweep engine, one batch per warp, counted from the other end of the
+// grid so that the CTAs with a 33..B_CAP-byte fragment get fewer).  Static
+// assignment keeps thousands of warps off one contended counter.
+// GRID: the grid engine is compiled in (the launch is then cooperative);
+// without it the kernel carries no call, whose calling convention costs the
+// other paths registers.
+template <bool GRID>
 __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace ws, DevVocab V) {
   __shared__ EngineSmem S;
   const int tid = threadIdx.x, warp = tid >> 5, T = B_THREADS;
@@ -1187,18 +1288,20 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
     S.nq[0] = st->long_count;
     S.nq[1] = st->wide_count;
     S.nq[2] = st->sbatch_count;
-    // many long-fragment bytes: the grid engine takes them all
-    S.gmode = S.nq[0] && V.monotone && c.grid_ctas > 0 && st->inner_bytes >= GRID_MIN_INNER;
   }
   __syncthreads();
   const uint32_t nlong = S.nq[0];
-  const uint32_t c0 = S.gmode ? (uint32_t)c.grid_ctas : 0u;  // CTAs [c0, grid) take the other queues
-  if (c0) {
+  // Where the grid engine can run, CTAs [0, c0) take the long fragments
+  // (all at once when they hold many bytes, else one each) and nothing else;
+  // CTAs [c0, grid) take the other queues.  Else every CTA takes long
+  // fragments one at a time, then the other queues.
+  const uint32_t c0 = GRID && nlong && V.monotone && c.grid_ctas > 0 ? (uint32_t)c.grid_ctas : 0u;
+  if (GRID && c0) {
     if (blockIdx.x < c0) {
       if (tid == 0) {
-        S.u.gp.c = c;
-        S.u.gp.ws = ws;
-        S.u.gp.V = V;
+        S.u.g.gp.c = c;
+        S.u.g.gp.ws = ws;
+        S.u.g.gp.V = V;
       }
       __syncthreads();
       grid_engine(nlong, S);
@@ -1239,13 +1342,13 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
   for (uint32_t b = gw; b < nbat; b += nwarps) short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
 }
 
-
 void launch_bpe_engine(const Call& call, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {
   // a persistent grid of as many CTAs as fit at once (16 of 32 registers per
-  // SM), launched cooperatively (all resident together: the grid engine's
-  // CTAs wait for one another) and as a programmatic dependent of the
-  // boundary kernel (its CTAs are scheduled while that grid's last CTAs
-  // finish)
+  // SM), launched as a programmatic dependent of the boundary kernel (its
+  // CTAs are scheduled while that grid's last CTAs finish) and, where the
+  // grid engine can run (a monotone vocabulary, a text of GRID_MIN_LONG bytes
+  // or more), cooperatively: all CTAs resident together, as the grid
+  // engine's CTAs wait for one another
   constexpr int kMaxDev = 64;
   static int per_sm[kMaxDev] = {};
   int dev = 0;
@@ -1253,7 +1356,7 @@ void launch_bpe_engine(const Call& call, const Workspace& w, const DevVocab& v, 
   int& ps = per_sm[dev >= 0 && dev < kMaxDev ? dev : 0];
   if (!ps) {
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_bpe_engine, B_THREADS, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_bpe_engine<true>, B_THREADS, 0) != cudaSuccess) {
       cudaGetLastError();
       occ = 1;
     }
@@ -1271,6 +1374,7 @@ void launch_bpe_engine(const Call& call, const Workspace& w, const DevVocab& v, 
   unsigned long long gc = (unsigned long long)n_sms * (ps < GRID_PER_SM ? ps : GRID_PER_SM);
   if (gc > room) gc = room;
   if (gc + 1 > grid) gc = grid - 1;
+  if (c.n < GRID_MIN_LONG || !v.monotone) gc = 0;  // the grid engine cannot run
   c.grid_ctas = (int)gc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
@@ -1282,8 +1386,10 @@ void launch_bpe_engine(const Call& call, const Workspace& w, const DevVocab& v, 
   attr[1].id = cudaLaunchAttributeCooperative;
   attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaLaunchKernelEx(&cfg, k_bpe_engine, c, w, v);
+  // cooperative only where the grid engine may wait at its barriers
+  cfg.numAttrs = gc ? 2 : 1;
+  if (gc) cudaLaunchKernelEx(&cfg, k_bpe_engine<true>, c, w, v);
+  else cudaLaunchKernelEx(&cfg, k_bpe_engine<false>, c, w, v);
 }
 
 }  // namespace tokgb

@@ -111,11 +111,9 @@ struct DevStatus {
   uint32_t sbatch_count, sbatch_taken;  // warp batches of short fragments
   uint32_t wide_count, wide_taken;      // fragments of 33..B_CAP bytes
   uint32_t long_count, long_taken;      // longer fragments
-  unsigned long long inner_bytes;       // bytes of the chunks that hold no fragment start (all in long fragments)
   // the grid engine of K3b: its barrier (arrivals, generation), the flag a
   // CTA sets when it gave up waiting, and per sweep whether a pair merges
   uint32_t gb_count, gb_gen, g_abort, g_any[3];
-  uint32_t pad[2];
 };
 static_assert(sizeof(DevStatus) % 16 == 0, "the group totals follow the status");
 

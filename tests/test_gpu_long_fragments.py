@@ -1,13 +1,14 @@
 """The BPE kernel's grid engine: when the fragments longer than 256 bytes
-cover many whole 1 KiB chunks, a group of the kernel's CTAs encodes all of
-them at once, meeting at grid barriers between the steps of each sweep.
+hold at least 32 KiB, a group of the kernel's CTAs encodes all of them at
+once, meeting at grid barriers between the steps of each sweep; with fewer
+bytes, the same CTAs encode one fragment each.
 
 Parity: ids against the oracle, id for id, on texts made of such fragments
 (whitespace, newline, digit and letter runs of 200 bytes to 100 KB, repeated
 symbols whose merges pair up from the left end of the run, 2-byte letters)
 under both patterns, as one text and as batch items; the same texts with the
-vocabulary's merges ignored; and a non-monotone vocabulary, which keeps the
-one-CTA engine.  The wait limit: a barrier that never completes (made on the
+vocabulary's merges ignored; long fragments of fewer bytes in all; and a
+non-monotone vocabulary, which keeps the one-CTA engine.  The wait limit: a barrier that never completes (made on the
 host with tok_debug_grid_wait) ends the call with TOK_ETIMEOUT after the limit,
 and the handle then encodes normally."""
 import os
@@ -75,7 +76,7 @@ def test_many_long_fragments_match_the_oracle(pkg, pattern):
             assert tok.encode(data).tolist() == encode(data, v, pattern), seed
         # one run of each kind alone, just past the size at which the grid
         # engine takes over and well beyond it
-        for n in (17 * 1024 + 5, 100_003):
+        for n in (32 * 1024 + 5, 100_003):
             for s in (" " * n + "x", "\n" * n, "9" * n + " ", "ab" * (n // 2), "é" * (n // 2)):
                 data = s.encode()
                 assert tok.encode(data).tolist() == encode(data, v, pattern), (n, s[:3])
@@ -110,9 +111,25 @@ def test_long_fragments_with_merges_ignored(pkg):
         tok.close()
 
 
+@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+def test_few_long_fragment_bytes_take_one_cta_each(pkg, pattern):
+    # a 200 KB session with eight runs of 300..3000 bytes: below 32 KiB of
+    # long fragments, in a text long enough for the grid engine
+    v = vocab(pattern)
+    tok = tokenizer(pkg, pattern)
+    try:
+        r = random.Random(5)
+        parts = [textgen.agentic_session(25_000, 60 + j) for j in range(8)]
+        runs = [" " * 3000, "\n" * 2000, "7" * 1500, "ab" * 400, "é" * 300, "x" * 257, "  " * 1000, "9" * 300]
+        data = "".join(p + run + "!" for p, run in zip(parts, runs)).encode()
+        assert tok.encode(data).tolist() == encode(data, v, pattern)
+    finally:
+        tok.close()
+
+
 def test_non_monotone_vocabulary_keeps_the_cta_engine(pkg):
     # "abc" is made by (ab,c) at rank 1 and again by (a,bc) at rank 4, after
-    # (abc,d) used it at rank 2; three 8000-letter words cover 18 whole chunks
+    # (abc,d) used it at rank 2; three 12000-letter words: 36 KB of long fragments
     toks = [bytes([b]) for b in range(256)] + [b"ab", b"abc", b"abcd", b"bc", b"cd", b"dd"]
     ix = {t: i for i, t in enumerate(toks)}
     merges = [(ix[b"a"], ix[b"b"]), (ix[b"ab"], ix[b"c"]), (ix[b"abc"], ix[b"d"]), (ix[b"b"], ix[b"c"]),
@@ -122,7 +139,7 @@ def test_non_monotone_vocabulary_keeps_the_cta_engine(pkg):
     tok = pkg.Tokenizer(toks, merges, PATTERN_GPT2)
     try:
         r = random.Random(8)
-        data = " ".join("".join(r.choice("abcd") for _ in range(8000)) for _ in range(3)).encode()
+        data = " ".join("".join(r.choice("abcd") for _ in range(12000)) for _ in range(3)).encode()
         assert tok.encode(data).tolist() == encode(data, v, PATTERN_GPT2)
     finally:
         tok.close()
