@@ -7,8 +7,10 @@ Parity: ids against the oracle, id for id, on texts made of such fragments
 (whitespace, newline, digit and letter runs of 200 bytes to 100 KB, repeated
 symbols whose merges pair up from the left end of the run, 2-byte letters)
 under both patterns, as one text and as batch items; the same texts with the
-vocabulary's merges ignored; long fragments of fewer bytes in all; and a
-non-monotone vocabulary, which keeps the one-CTA engine.  The wait limit: a barrier that never completes (made on the
+vocabulary's merges ignored; under the o200k-style pattern, with token
+offsets; long-fragment bytes on both sides of the 32 KiB switch; long
+fragments of fewer bytes in all; and a non-monotone vocabulary, which keeps
+the one-CTA engine.  The wait limit: a barrier that never completes (made on the
 host with tok_debug_grid_wait) ends the call with TOK_ETIMEOUT after the limit,
 and the handle then encodes normally."""
 import os
@@ -17,15 +19,16 @@ import random
 import pytest
 
 import textgen
-from oracle.encode import encode
-from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2
+from oracle.encode import encode, encode_with_offsets
+from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2, PATTERN_O200K
 from oracle.vocab import Vocab
 
 pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 VOC = os.path.join(ROOT, "data", "vocabs")
-VOCABS = {PATTERN_GPT2: "gpt2_session_100k", PATTERN_CL100K: "cl100k_session_100k"}
+VOCABS = {PATTERN_GPT2: "gpt2_session_100k", PATTERN_CL100K: "cl100k_session_100k",
+          PATTERN_O200K: "cl100k_session_100k"}
 
 
 @pytest.fixture(scope="module")
@@ -80,6 +83,35 @@ def test_many_long_fragments_match_the_oracle(pkg, pattern):
             for s in (" " * n + "x", "\n" * n, "9" * n + " ", "ab" * (n // 2), "é" * (n // 2)):
                 data = s.encode()
                 assert tok.encode(data).tolist() == encode(data, v, pattern), (n, s[:3])
+    finally:
+        tok.close()
+
+
+def test_o200k_style_long_fragments_with_offsets(pkg):
+    pattern = PATTERN_O200K
+    v = vocab(pattern)
+    tok = tokenizer(pkg, pattern)
+    try:
+        data = long_text(6, n_mid=60)
+        ids, offs = tok.encode_with_offsets(data)
+        assert (ids.tolist(), offs.tolist()) == encode_with_offsets(data, v, pattern)
+    finally:
+        tok.close()
+
+
+@pytest.mark.parametrize("pattern", [PATTERN_GPT2, PATTERN_CL100K])
+def test_both_sides_of_the_grid_engine_switch(pkg, pattern):
+    # one long space run (a single fragment before "x") of 32 KiB - 1, 32 KiB
+    # and 32 KiB + 1 bytes in a text of 40 KB or more; the fragment that ends
+    # the run keeps the space before "x", so the run's piece is one byte
+    # shorter than the run
+    v = vocab(pattern)
+    tok = tokenizer(pkg, pattern)
+    try:
+        filler = textgen.agentic_session(8_000, 77)
+        for m in (32 * 1024 - 1, 32 * 1024, 32 * 1024 + 1, 32 * 1024 + 2):
+            data = (filler + " " * m + "x" + filler).encode()
+            assert tok.encode(data).tolist() == encode(data, v, pattern), m
     finally:
         tok.close()
 
