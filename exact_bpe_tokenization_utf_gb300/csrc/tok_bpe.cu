@@ -838,18 +838,23 @@ __device__ __forceinline__ long long long_end(const Call& c, const Workspace& ws
 // sweeps.  A sweep is the sweep of the global-memory engine (monotone
 // vocabularies) in three steps, a grid barrier after each:
 //   P1  stale keys are looked up; a mergeable pair whose left neighbour pair
-//       is another merge starts a run of equal-rank pairs
-//   P2  each pair's run start (a max-scan over the whole space, carried from
-//       unit to unit through the last run start of each unit) and its safe
-//       flag
+//       is another merge starts a run of equal-rank pairs; live symbols are
+//       counted
+//   P2  each pair's run start (a max-scan over the whole space: shuffles in a
+//       tile, then the last run start of each earlier unit of the group of 32
+//       units, then the largest of each earlier group) and its safe flag, the
+//       walks reading a per-warp window of the space in shared memory
 //   P3  the safe pairs merge
-// Warp w of CTA b owns the coordinates of unit u = 4b + w, [u*R, (u+1)*R)
-// with R a multiple of 32, in tiles of 32.  Symbols and links are written by
-// other CTAs between barriers, so they are read past L1 (ld.global.cg).
+// then each live symbol's rank gives its id's place (grid_ids).  Warp w of
+// CTA b owns the coordinates of unit u = 4b + w, [u*R, (u+1)*R) with R a
+// multiple of 32, in tiles of 32.  Symbols and links are written by other
+// CTAs between barriers, so they are read past L1 (ld.global.cg).  When the
+// long fragments hold fewer than GRID_MIN_LONG bytes, the same CTAs take one
+// fragment each instead.
 
 constexpr long long GRID_MIN_LONG = 32 * 1024;  // long-fragment bytes from which the grid engine runs
-constexpr int GRID_PER_SM = 8;                                // CTAs per SM in the grid engine
-constexpr int GRID_UNITS = B_THREADS / 32;                    // units (warps) per CTA
+constexpr int GRID_PER_SM = 8;                  // CTAs per SM in the grid engine
+constexpr int GRID_UNITS = B_THREADS / 32;      // units (warps) per CTA
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
@@ -1049,13 +1054,14 @@ __device__ __noinline__ void grid_ids(uint32_t nlong, EngineSmem& S, long long u
 // The long fragments' ids to their byte offsets in ws.tok (and their counts
 // to fcnt, ctot and gtot), by the first c.grid_ctas CTAs: all at once when
 // they hold GRID_MIN_LONG bytes or more, else one fragment per CTA with the
-// global-memory engine.  The
-// arrays are the global-memory engine's: symbols e_sym[0], lengths
-// e_len[0], links e_len[1], keys e_kr[0] (after the sweeps: each live
-// symbol's rank among all live symbols, bit 63 set at a fragment's last),
-// flags e_fl, fragment of each coordinate e_rs; e_kr[1] holds the fragment
-// offsets (nlong + 1), the rank of each fragment's first symbol (nlong), the
-// last run start of each unit (4 per CTA) and the live symbols of each CTA.
+// global-memory engine.  The arrays are the global-memory engine's: symbols
+// e_sym[0], lengths e_len[0], links e_len[1], keys e_kr[0] (after the
+// sweeps: each live symbol's rank among all live symbols, bit 63 set at a
+// fragment's last), flags e_fl, fragment of each coordinate e_rs; e_kr[1]
+// holds the fragment offsets (nlong + 1), the rank of each fragment's first
+// symbol (nlong), the last run start of each unit (4 per CTA), the live
+// symbols of each CTA and two buffers of the largest run start of each group
+// of 32 units.
 __device__ __noinline__ void grid_engine(uint32_t nlong, EngineSmem& S) {
   const Call& c = S.u.g.gp.c;
   const Workspace& ws = S.u.g.gp.ws;
