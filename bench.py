@@ -10,7 +10,7 @@ Workloads (all synthetic and seeded; C3 is the default):
   C3  cl100k-style pattern, 100,000 merges; one 1,000,000-character agentic
       session (fresh-session init)
   C4  cl100k-style, 100,000 merges; 64 sessions of log-uniform length
-      (2 KiB .. 1 MiB, 10.7 MB in all) in one tok_encode_batch call
+      (2 KiB .. 1 MiB, 15.0 MB in all) in one tok_encode_batch call
   C5  the 8 MiB adversarial text, encoded with the GPT-2 and the cl100k-style
       pattern (100,000 merges each): one step is both encodes
 
