@@ -303,7 +303,14 @@ __device__ void cta_fragment(const Call& c, const Workspace& ws, const DevVocab&
   }
   if (tid == 0) *sflags = 0;
   __syncthreads();
-  for (int i = tid; i < M; i += T) C.kr[i] = (i + 1 >= M) ? KR_WALL : merge_lookup(V, C.sym[i], C.sym[i + 1]);
+  // a byte pair that no merge result holds is a wall from the start: no
+  // merge ever crosses it, so the pieces between walls encode apart (fewer
+  // sweeps: the safe-pair walks stop at walls)
+  for (int i = tid; i < M; i += T) {
+    bool wall = i + 1 >= M;
+    if (!wall && V.pair_bits) wall = !bit_at(V.pair_bits, ((int)c.text[a + i] << 8) | (int)c.text[a + i + 1]);
+    C.kr[i] = wall ? KR_WALL : merge_lookup(V, C.sym[i], C.sym[i + 1]);
+  }
   __syncthreads();
   int m = M;
   for (int sweep = 0; sweep <= M; ++sweep) {
@@ -381,7 +388,8 @@ __device__ void cta_fragment(const Call& c, const Workspace& ws, const DevVocab&
           nmr[j] = C.mr[i];
         }
         const int jn = mg ? i + 2 : i + 1;  // the next symbol that survives
-        if (jn >= m) nkr[j] = KR_WALL;
+        // a wall before it stays (no merge crosses a wall)
+        if (jn >= m || kr_rank(mg ? C.kr[i + 1] : C.kr[i]) == RANK_WALL) nkr[j] = KR_WALL;
         else if (!mg && !C.fl[jn]) nkr[j] = C.kr[i];  // unchanged pair keeps its key
         else nkr[j] = merge_lookup(V, nsym[j], C.fl[jn] ? kr_result(C.kr[jn]) : C.sym[jn]);
       }
