@@ -8,11 +8,12 @@ Parity: ids against the oracle, id for id, on texts made of such fragments
 symbols whose merges pair up from the left end of the run, 2-byte letters)
 under both patterns, as one text and as batch items; the same texts with the
 vocabulary's merges ignored; under the o200k-style pattern, with token
-offsets; long-fragment bytes on both sides of the 32 KiB switch; long
-fragments of fewer bytes in all; and a non-monotone vocabulary, which keeps
-the one-CTA engine.  The wait limit: a barrier that never completes (made on the
-host with tok_debug_grid_wait) ends the call with TOK_ETIMEOUT after the limit,
-and the handle then encodes normally."""
+offsets; long-fragment bytes on both sides of the 32 KiB switch; about 4,000
+long fragments at once; long fragments of fewer bytes in all; and a
+non-monotone vocabulary, which keeps the one-CTA engine.  The wait limit: a
+barrier that never completes (made on the host with tok_debug_grid_wait) ends
+the call with TOK_ETIMEOUT after the limit, and the handle then encodes
+normally."""
 import os
 import random
 
@@ -112,6 +113,27 @@ def test_both_sides_of_the_grid_engine_switch(pkg, pattern):
         for m in (32 * 1024 - 1, 32 * 1024, 32 * 1024 + 1, 32 * 1024 + 2):
             data = (filler + " " * m + "x" + filler).encode()
             assert tok.encode(data).tolist() == encode(data, v, pattern), m
+    finally:
+        tok.close()
+
+
+def test_thousands_of_long_fragments(pkg):
+    # about 4,000 fragments of 257..600 bytes (runs of spaces, newlines,
+    # digits, letters and dashes, each a single fragment that no byte-pair
+    # boundary cuts): every grid-engine CTA scans all their lengths, the
+    # coordinates are looked up among thousands of offsets
+    pattern = PATTERN_GPT2
+    v = vocab(pattern)
+    tok = tokenizer(pkg, pattern)
+    try:
+        r = random.Random(12)
+        runs = [" ", "\n", "7", "a", "-"]
+        parts = []
+        for _ in range(4000):
+            ch = r.choice(runs)
+            parts.append(ch * r.randint(258, 600) + r.choice(["x", ";", "Q"]))
+        data = "".join(parts).encode()
+        assert tok.encode(data).tolist() == encode(data, v, pattern)
     finally:
         tok.close()
 
