@@ -32,7 +32,7 @@ Parity pins live in tests/test_oracle_*.py.
 """
 from .utf8 import Utf8Error, decode_utf8  # noqa: F401
 from .ucd import classify, class_array  # noqa: F401
-from .pretokenize import pretokenize, PATTERN_GPT2, PATTERN_CL100K, PATTERN_O200K  # noqa: F401
+from .pretokenize import pretokenize, PATTERN_GPT2, PATTERN_CL100K, PATTERN_O200K, PATTERN_DEEPSEEK  # noqa: F401
 from .bpe import bpe_textbook, bpe_rounds, bpe_heap  # noqa: F401
 from .vocab import Vocab  # noqa: F401
 from .encode import encode, decode, pretoken_byte_spans  # noqa: F401

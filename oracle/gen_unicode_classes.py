@@ -58,7 +58,34 @@ def main_upper(out_path):
     print(len(ranges), "ranges ->", out_path)
 
 
+# the letters of the CJK scripts: script extensions Han, Hiragana, Katakana or
+# Hangul (the DeepSeek-style pattern's CJK runs)
+CJK_SET = r"[\p{scx=Han}\p{scx=Hiragana}\p{scx=Katakana}\p{scx=Hangul}]"
+
+
+def main_cjk(out_path):
+    """Ranges of the letters (\\p{L}) whose script extensions include Han,
+    Hiragana, Katakana or Hangul."""
+    pl, pc = regex.compile(r"\p{L}"), regex.compile(CJK_SET)
+    ranges = []
+    start = None
+    for cp in range(0x110000 + 1):
+        ok = cp < 0x110000 and not (0xD800 <= cp <= 0xDFFF) and bool(pl.match(chr(cp))) and bool(pc.match(chr(cp)))
+        if ok and start is None:
+            start = cp
+        elif not ok and start is not None:
+            ranges.append((start, cp - 1))
+            start = None
+    with open(out_path, "w") as f:
+        f.write("# regex %s; code point ranges of the letters of script extensions Han, Hiragana, Katakana, "
+                "Hangul (inclusive, hex)\n" % regex.__version__)
+        for a, b in ranges:
+            f.write("%04X %04X\n" % (a, b))
+    print(len(ranges), "ranges ->", out_path)
+
+
 if __name__ == "__main__":
     data = os.path.join(os.path.dirname(os.path.abspath(__file__)), "data")
     main(sys.argv[1] if len(sys.argv) > 1 else os.path.join(data, "unicode_classes.txt"))
     main_upper(sys.argv[2] if len(sys.argv) > 2 else os.path.join(data, "unicode_upper.txt"))
+    main_cjk(sys.argv[3] if len(sys.argv) > 3 else os.path.join(data, "unicode_cjk.txt"))

@@ -4,9 +4,9 @@ every match start depends on where the previous match ended).
 
 The pages name the tokenizer families but print no pattern.  The patterns
 here are the GPT-2 pattern, the cl100k-style pattern (case-insensitive
-contractions, digit groups of at most three, newline-aware whitespace) and an
-o200k-style pattern, written as ASTs for regex_engine in the same order as
-their regex text:
+contractions, digit groups of at most three, newline-aware whitespace), an
+o200k-style pattern and a DeepSeek-style pattern, written as ASTs for
+regex_engine in the same order as their regex text:
 
 GPT-2:
   's|'t|'re|'ve|'m|'ll|'d| ?\\p{L}+| ?\\p{N}+| ?[^\\s\\p{L}\\p{N}]+|\\s+(?!\\S)|\\s+
@@ -21,13 +21,21 @@ word before them, and a symbol run that also takes a tail of CR, LF and '/'):
   [^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]*[\\p{Ll}\\p{Lm}\\p{Lo}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
   |[^\\r\\n\\p{L}\\p{N}]?[\\p{Lu}\\p{Lt}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
   |\\p{N}{1,3}| ?[^\\s\\p{L}\\p{N}]+[\\r\\n/]*|\\s*[\\r\\n]+|\\s+(?!\\S)|\\s+
+
+DeepSeek-style (this project's own definition in the style of the DeepSeek
+family the pages name: the cl100k-style pattern with the letter runs of the
+CJK scripts, C = letters of script extensions Han, Hiragana, Katakana or
+Hangul, taken apart from other letters and without a prefix):
+  (?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\\r\\n\\p{L}\\p{N}]?(?:(?!C)\\p{L})+|(?:(?=C)\\p{L})+
+  |\\p{N}{1,3}| ?[^\\s\\p{L}\\p{N}]+[\\r\\n]*|\\s*[\\r\\n]+|\\s+(?!\\S)|\\s+
 """
 from .regex_engine import Alt, Cls, INF, Lit, NotAhead, Rep, Seq, Star, match_at
-from .ucd import class_array, is_upper
+from .ucd import class_array, is_cjk, is_upper
 
 PATTERN_GPT2 = 0
 PATTERN_CL100K = 1
 PATTERN_O200K = 2
+PATTERN_DEEPSEEK = 3
 
 _L = Cls(lambda cp, c: c == "L", r"\p{L}")
 _N = Cls(lambda cp, c: c == "N", r"\p{N}")
@@ -40,6 +48,8 @@ _SP = Lit(" ")
 _UPPER = Cls(lambda cp, c: c == "L" and is_upper(cp), r"[\p{Lu}\p{Lt}]")
 _LOWER = Cls(lambda cp, c: c == "L" and not is_upper(cp), r"[\p{Ll}\p{Lm}\p{Lo}]")
 _CRLF_SLASH = Cls(lambda cp, c: cp in (10, 13, 47), r"[\r\n/]")
+_CJK_L = Cls(lambda cp, c: c == "L" and is_cjk(cp), r"(?=C)\p{L}")
+_OTHER_L = Cls(lambda cp, c: c == "L" and not is_cjk(cp), r"(?!C)\p{L}")
 
 
 def _contractions(icase):
@@ -78,7 +88,18 @@ O200K = Alt(
     Rep(_S, 1, INF),
 )
 
-PATTERNS = {PATTERN_GPT2: GPT2, PATTERN_CL100K: CL100K, PATTERN_O200K: O200K}
+DEEPSEEK = Alt(
+    Alt(*_contractions(True)),
+    Seq(Rep(_NOT_CRLF_L_N, 0, 1), Rep(_OTHER_L, 1, INF)),
+    Rep(_CJK_L, 1, INF),
+    Rep(_N, 1, 3),
+    Seq(Rep(_SP, 0, 1), Rep(_NOT_SLN, 1, INF), Rep(_CRLF, 0, INF)),
+    Seq(Rep(_S, 0, INF), Rep(_CRLF, 1, INF)),
+    Seq(Rep(_S, 1, INF), NotAhead(_NOT_S)),
+    Rep(_S, 1, INF),
+)
+
+PATTERNS = {PATTERN_GPT2: GPT2, PATTERN_CL100K: CL100K, PATTERN_O200K: O200K, PATTERN_DEEPSEEK: DEEPSEEK}
 
 
 def pretokenize(cps, pattern_id, cls=None):

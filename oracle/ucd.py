@@ -42,6 +42,26 @@ with open(_UPATH) as _f:
         _uends.append(int(_b, 16))
 
 
+# the letters of the CJK scripts (script extensions Han, Hiragana, Katakana,
+# Hangul): the DeepSeek-style pattern takes their runs apart from other
+# letters; data/unicode_cjk.txt comes from the same generator and regex engine
+_CPATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "data", "unicode_cjk.txt")
+_cstarts, _cends = [], []
+with open(_CPATH) as _f:
+    for _line in _f:
+        if _line.startswith("#"):
+            continue
+        _a, _b = _line.split()
+        _cstarts.append(int(_a, 16))
+        _cends.append(int(_b, 16))
+
+
+def is_cjk(cp):
+    """True for a letter of script extensions Han, Hiragana, Katakana or Hangul."""
+    k = bisect.bisect_right(_cstarts, cp) - 1
+    return k >= 0 and cp <= _cends[k]
+
+
 def is_upper(cp):
     """True for an upper-case or title-case letter (Lu, Lt)."""
     k = bisect.bisect_right(_ustarts, cp) - 1
