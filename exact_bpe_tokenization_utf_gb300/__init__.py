@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(HERE, "_lib", "libtokgb.so")
 PATTERN_GPT2 = 0
 PATTERN_CL100K = 1
 PATTERN_O200K = 2
+PATTERN_DEEPSEEK = 3
 IGNORE_MERGES = 0x100   # flag ORed into the pattern id (tok.h TOK_IGNORE_MERGES)
 
 TOK_OK, TOK_EINVAL, TOK_EUTF8, TOK_ENOMEM, TOK_ECUDA, TOK_EBUF, TOK_ETIMEOUT, TOK_EMERGES = 0, -1, -2, -3, -4, -5, -6, -7

@@ -413,7 +413,8 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   *out = nullptr;
   const bool ignore_merges = (pattern_id & TOK_IGNORE_MERGES) != 0;
   const int pattern = pattern_id & ~TOK_IGNORE_MERGES;
-  if (pattern != TOK_PAT_GPT2 && pattern != TOK_PAT_CL100K_STYLE && pattern != TOK_PAT_O200K_STYLE)
+  if (pattern != TOK_PAT_GPT2 && pattern != TOK_PAT_CL100K_STYLE && pattern != TOK_PAT_O200K_STYLE &&
+      pattern != TOK_PAT_DEEPSEEK_STYLE)
     return fail(nullptr, TOK_EINVAL, "unknown pattern id");
   if (!vocab_bytes || !vocab_off || (n_merges && !merges)) return fail(nullptr, TOK_EINVAL, "NULL vocabulary");
   if (n_vocab < 256 || n_vocab >= (1u << 20)) return fail(nullptr, TOK_EMERGES, "n_vocab out of range");

@@ -46,7 +46,8 @@ __global__ void k_noalloc_empty(long long* d_status) {
 
 extern "C" int tok_pretokenize_device_noalloc(int pattern_id, const uint8_t* d_text, uint64_t len,
                                               uint32_t* d_start_bits, int64_t* d_status, void* stream) {
-  if (pattern_id != TOK_PAT_GPT2 && pattern_id != TOK_PAT_CL100K_STYLE && pattern_id != TOK_PAT_O200K_STYLE)
+  if (pattern_id != TOK_PAT_GPT2 && pattern_id != TOK_PAT_CL100K_STYLE && pattern_id != TOK_PAT_O200K_STYLE &&
+      pattern_id != TOK_PAT_DEEPSEEK_STYLE)
     return TOK_EINVAL;
   if (!d_status || (len && (!d_text || !d_start_bits))) return TOK_EINVAL;
   // the same bound as every other entry point: the chunk grid and the UTF-8

@@ -54,17 +54,22 @@ enum {
 
 /* Pre-tokenizer patterns.  The pages name the cl100k / o200k / DeepSeek
  * families (Section 4.1) without printing them; these are the GPT-2 pattern,
- * the cl100k-style pattern and an o200k-style pattern of this library's own
+ * the cl100k-style pattern, an o200k-style pattern of this library's own
  * definition (letter runs split where a lower-case or caseless letter is
  * followed by an upper-case one, contractions suffixes of the word before,
- * a symbol run's tail of CR, LF and '/'):
+ * a symbol run's tail of CR, LF and '/') and a DeepSeek-style pattern of its
+ * own definition (the cl100k-style pattern with the letter runs of the CJK
+ * scripts, C = letters of script extensions Han, Hiragana, Katakana or
+ * Hangul, apart from other letters and without a prefix):
  *   GPT-2:  's|'t|'re|'ve|'m|'ll|'d| ?\p{L}+| ?\p{N}+| ?[^\s\p{L}\p{N}]+|\s+(?!\S)|\s+
  *   cl100k: (?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\r\n\p{L}\p{N}]?\p{L}+|\p{N}{1,3}
  *           | ?[^\s\p{L}\p{N}]+[\r\n]*|\s*[\r\n]+|\s+(?!\S)|\s+
  *   o200k:  [^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]*[\p{Ll}\p{Lm}\p{Lo}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
  *           |[^\r\n\p{L}\p{N}]?[\p{Lu}\p{Lt}]+(?:(?i:'s|'t|'re|'ve|'m|'ll|'d))*
- *           |\p{N}{1,3}| ?[^\s\p{L}\p{N}]+[\r\n/]*|\s*[\r\n]+|\s+(?!\S)|\s+       */
-enum { TOK_PAT_GPT2 = 0, TOK_PAT_CL100K_STYLE = 1, TOK_PAT_O200K_STYLE = 2 };
+ *           |\p{N}{1,3}| ?[^\s\p{L}\p{N}]+[\r\n/]*|\s*[\r\n]+|\s+(?!\S)|\s+
+ *   DeepSeek: (?i:'s|'t|'re|'ve|'m|'ll|'d)|[^\r\n\p{L}\p{N}]?(?:(?!C)\p{L})+|(?:(?=C)\p{L})+
+ *           |\p{N}{1,3}| ?[^\s\p{L}\p{N}]+[\r\n]*|\s*[\r\n]+|\s+(?!\S)|\s+        */
+enum { TOK_PAT_GPT2 = 0, TOK_PAT_CL100K_STYLE = 1, TOK_PAT_O200K_STYLE = 2, TOK_PAT_DEEPSEEK_STYLE = 3 };
 
 /* Flag ORed into tok_load's pattern_id: Section 4.2's whole-word lookup
  * (Llama-style `ignore_merges`): a fragment whose bytes are a token of the
@@ -82,8 +87,8 @@ enum { TOK_IGNORE_MERGES = 0x100 };
  *   (rank = index).  The result of a merge is the token whose bytes are
  *   bytes(left) || bytes(right); it must exist.  No pair may repeat.
  *   (Section 4.2: BPE merges applied lowest rank first.)
- * pattern_id: TOK_PAT_GPT2, TOK_PAT_CL100K_STYLE or TOK_PAT_O200K_STYLE,
- *   optionally ORed with TOK_IGNORE_MERGES.
+ * pattern_id: TOK_PAT_GPT2, TOK_PAT_CL100K_STYLE, TOK_PAT_O200K_STYLE or
+ *   TOK_PAT_DEEPSEEK_STYLE, optionally ORed with TOK_IGNORE_MERGES.
  * out: receives the handle; free it with tok_free.
  * Errors: TOK_EINVAL, TOK_EMERGES (validation, message in tok_last_error(NULL)),
  *   TOK_ENOMEM, TOK_ECUDA.

@@ -16,7 +16,7 @@ import textgen
 from conftest import BRUTE_ALPHABET
 from oracle.encode import encode, encode_with_offsets, pretoken_byte_spans
 from oracle.repair import repair_append as oracle_repair_append
-from oracle.pretokenize import PATTERN_CL100K, PATTERN_GPT2, PATTERN_O200K
+from oracle.pretokenize import PATTERN_CL100K, PATTERN_DEEPSEEK, PATTERN_GPT2, PATTERN_O200K
 from oracle.utf8 import Utf8Error
 from oracle.vocab import Vocab
 
@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 VOC = os.path.join(ROOT, "data", "vocabs")
 
-ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ/"
+ALPHABET = "asStlLe1² \t\n\r'.éx́中 ſ/カー한"
 
 
 @pytest.fixture(scope="session")
@@ -56,7 +56,7 @@ def oracle_starts(data, pattern):
 
 # --- pre-tokenizer ----------------------------------------------------------
 
-ALL_PATTERNS = [PATTERN_GPT2, PATTERN_CL100K, PATTERN_O200K]
+ALL_PATTERNS = [PATTERN_GPT2, PATTERN_CL100K, PATTERN_O200K, PATTERN_DEEPSEEK]
 
 
 @pytest.mark.parametrize("pattern", ALL_PATTERNS)
@@ -449,6 +449,37 @@ def test_o200k_style_encode_matches_oracle(pkg, oracle_pool):
 
 
 # --- ignore_merges -------------------------------------------------------------
+
+def test_deepseek_style_encode_matches_oracle(pkg, oracle_pool):
+    # the DeepSeek-style pattern (this library's own definition) with the
+    # 100k-merge session vocabulary: the 1M-character session, the mixed text
+    # with 10% CJK, Japanese and Korean runs among Latin words, the scaled
+    # adversarial text with offsets, a batch
+    path = os.path.join(VOC, "cl100k_session_100k.merges")
+    v = Vocab.load_merges(path)
+    tok = pkg.Tokenizer.from_merges_file(path, PATTERN_DEEPSEEK)
+    session = textgen.agentic_session(1_000_000, 1003).encode()
+    want_ids, want_starts = oracle_pool.encode_long(session, path, PATTERN_DEEPSEEK)
+    assert tok.pretokenize(session).tolist() == want_starts
+    assert tok.encode(session).tolist() == want_ids
+    mixed = textgen.mixed_c2(300_000, 1061).encode()
+    assert tok.pretokenize(mixed).tolist() == oracle_starts(mixed, PATTERN_DEEPSEEK)
+    assert tok.encode(mixed).tolist() == encode(mixed, v, PATTERN_DEEPSEEK)
+    rnd = random.Random(1062)
+    words = ["カーテン", "ひらがな", "한국어", "漢字", "々", "〆切", "text", "naïve", " ", "  ", ".", ",", "'s", "1234",
+             "\n", "\r\n", "Ωmega", "ㄅ", "ｱｲｳ", "𠀀"]
+    cjk = "".join(rnd.choice(words) for _ in range(40_000)).encode()
+    assert tok.pretokenize(cjk).tolist() == oracle_starts(cjk, PATTERN_DEEPSEEK)
+    assert tok.encode(cjk).tolist() == encode(cjk, v, PATTERN_DEEPSEEK)
+    adv = textgen.adversarial(400_000, 1005, scale=0.02).encode()
+    ids, offs = tok.encode_with_offsets(adv)
+    assert (ids.tolist(), offs.tolist()) == encode_with_offsets(adv, v, PATTERN_DEEPSEEK)
+    items = [x.encode() for x in textgen.session_batch(8, 1063, hi=1 << 16)]
+    ids, off = tok.encode_batch(items)
+    for k, it in enumerate(items):
+        assert ids[off[k]:off[k + 1]].tolist() == encode(it, v, PATTERN_DEEPSEEK), k
+    tok.close()
+
 
 def test_ignore_merges_matches_oracle(pkg):
     # a vocabulary with tokens that do not encode to themselves: with the flag

@@ -41,7 +41,7 @@ def test_noalloc_pretokenizer_matches_oracle():
     import exact_bpe_tokenization_utf_gb300 as pkg
     L = pkg.lib()
     stream = torch.cuda.current_stream().cuda_stream
-    for pattern in (pkg.PATTERN_GPT2, pkg.PATTERN_CL100K, pkg.PATTERN_O200K):
+    for pattern in (pkg.PATTERN_GPT2, pkg.PATTERN_CL100K, pkg.PATTERN_O200K, pkg.PATTERN_DEEPSEEK):
         tok = pkg.Tokenizer.from_merges([], pattern)
         # lengths that end inside a bitmask word (n % 32 != 0) and inside a chunk
         texts = [textgen.agentic_session(300_000, 50 + pattern).encode(),
