@@ -84,3 +84,22 @@ def test_classes_match_regex_module_everywhere():
         ch = chr(cp)
         want = "L" if pl.match(ch) else "N" if pn.match(ch) else "W" if ps.match(ch) else "O"
         assert classify(cp) == want, hex(cp)
+
+
+def test_cjk_letters_match_regex_module_everywhere():
+    # the DeepSeek-style pattern's CJK letters: letters whose script
+    # extensions include Han, Hiragana, Katakana or Hangul
+    regex = pytest.importorskip("regex")
+    from oracle.ucd import is_cjk
+    pc = regex.compile(r"(?=[\p{scx=Han}\p{scx=Hiragana}\p{scx=Katakana}\p{scx=Hangul}])\p{L}")
+    for cp in range(0x110000):
+        if 0xD800 <= cp <= 0xDFFF:
+            continue
+        assert is_cjk(cp) == bool(pc.match(chr(cp))), hex(cp)
+    # fixed values: Han, kana with the prolonged sound mark, Hangul; not
+    # Bopomofo, Latin, digits or CJK punctuation
+    for cp in (0x4E2D, 0x3005, 0x30AB, 0x30FC, 0x3072, 0xD55C, 0xFF71, 0x20000, 0x3400):
+        assert is_cjk(cp), hex(cp)
+    for cp in (0x3105, ord("a"), 0xE9, ord("1"), 0x3002, 0x3001, 0x4E00 - 1):
+        assert not is_cjk(cp), hex(cp)
+
