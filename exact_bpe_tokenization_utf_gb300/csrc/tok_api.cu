@@ -48,9 +48,8 @@ struct tok_handle {
   uint16_t* d_max_left = nullptr;
   uint16_t* d_max_right = nullptr;
   WholeEntry* d_whole = nullptr;
-  uint8_t* d_vocab_bytes = nullptr;
-  uint64_t vocab_bytes_len = 0;
-  uint32_t* d_vocab_off = nullptr;
+  unsigned long long* d_whole_tail = nullptr;
+  uint64_t whole_tail_bytes = 0;
   uint32_t* d_pair_bits = nullptr;
   uint32_t n_whole = 0;
   uint64_t hash = 0;
@@ -270,7 +269,7 @@ void clear_counters(tok_handle* h, uint64_t n, cudaStream_t s) {
 // Enqueue the whole chain for one call.
 int run_chain(tok_handle* h, Call c, cudaStream_t s) {
   c.pf[0] = Prefetch{h->d_whole, (unsigned long long)sizeof(WholeEntry) << h->v.whole_bits};
-  c.pf[1] = Prefetch{h->d_vocab_bytes, h->vocab_bytes_len};
+  c.pf[1] = Prefetch{h->d_whole_tail, h->whole_tail_bytes};
   c.pf[2] = Prefetch{h->d_table, (unsigned long long)sizeof(MergeEntry) << h->v.bits};
   c.pf[3] = Prefetch{h->v.pair_bits, h->v.pair_bits ? 8192ull : 0ull};
   c.pattern = h->pattern;
@@ -523,26 +522,31 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   // average, and a warp's longest chain is short
   while ((1ull << wbits) < 4ull * whole_tokens.size()) ++wbits;
   std::vector<WholeEntry> whole(1ull << wbits, WholeEntry{0, 0, 0});
-  if (vocab_off[n_vocab] - vocab_off[0] >= (1ull << 32)) return fail(nullptr, TOK_EMERGES, "vocabulary too large");
-  std::vector<uint32_t> off32(n_vocab + 1);
-  for (uint32_t t = 0; t <= n_vocab; ++t) off32[t] = (uint32_t)(vocab_off[t] - vocab_off[0]);
+  // bytes 8.. of the longer tokens, each from a word boundary, zero-padded
+  // to whole 8-byte words (word 0 is never read)
+  std::vector<unsigned long long> tail(1, 0ull);
   for (uint32_t t : whole_tokens) {
-    // entries carry the first 8 bytes, the offset and the length: a probe
-    // of a longer token needs one more load to compare the rest
-    if (tok_len[t] > 255 || off32[t] >= (1u << 24)) {
+    const uint32_t len = tok_len[t];
+    const uint64_t first = len > 8 ? tail.size() : 0;
+    if (len > 255 || first >= (1u << 24)) {
       // without the flag the table only saves work, so a token it cannot
       // hold is encoded by the merge loop instead; with the flag every token
       // must be found
       if (ignore_merges)
-        return fail(nullptr, TOK_EMERGES, "ignore_merges needs tokens of at most 255 bytes in the first 16 MiB");
+        return fail(nullptr, TOK_EMERGES, "ignore_merges needs tokens of at most 255 bytes (and under 128 MiB of them)");
       continue;
     }
     const uint8_t* tb = vocab_bytes + vocab_off[t];
-    const unsigned long long head = bytes_head(tb, tok_len[t]);
-    const unsigned long long hv = bytes_hash(head, tb, tok_len[t]);
+    for (uint32_t i = 8; i < len; i += 8) {
+      unsigned long long w = 0;
+      for (uint32_t k = 0; k < 8 && i + k < len; ++k) w |= (unsigned long long)tb[i + k] << (8 * k);
+      tail.push_back(w);
+    }
+    const unsigned long long head = bytes_head(tb, len);
+    const unsigned long long hv = bytes_hash(head, tb, len);
     uint32_t slot = (uint32_t)(hv >> (64 - wbits));
     while (whole[slot].offlen != 0) slot = (slot + 1) & ((1u << wbits) - 1u);
-    whole[slot] = WholeEntry{head, t, (off32[t] << 8) | tok_len[t]};
+    whole[slot] = WholeEntry{head, t, ((uint32_t)first << 8) | len};
   }
 
   tok_handle* h = new tok_handle();
@@ -556,18 +560,15 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   if (e == cudaSuccess) e = dalloc(&h->d_max_left, n_vocab);
   if (e == cudaSuccess) e = dalloc(&h->d_max_right, n_vocab);
   if (e == cudaSuccess) e = dalloc(&h->d_whole, whole.size());
-  if (e == cudaSuccess) e = dalloc(&h->d_vocab_bytes, off32[n_vocab] + 16);
-  h->vocab_bytes_len = off32[n_vocab];
-  if (e == cudaSuccess) e = dalloc(&h->d_vocab_off, n_vocab + 1);
+  if (e == cudaSuccess) e = dalloc(&h->d_whole_tail, tail.size());
+  h->whole_tail_bytes = tail.size() * sizeof(unsigned long long);
   if (e == cudaSuccess) e = dalloc(&h->d_pair_bits, pair_bits.size());
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_pair_bits, pair_bits.data(), pair_bits.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_whole, whole.data(), whole.size() * sizeof(WholeEntry), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
-    e = cudaMemcpy(h->d_vocab_bytes, vocab_bytes + vocab_off[0], off32[n_vocab], cudaMemcpyHostToDevice);
-  if (e == cudaSuccess)
-    e = cudaMemcpy(h->d_vocab_off, off32.data(), (n_vocab + 1) * sizeof(uint32_t), cudaMemcpyHostToDevice);
+    e = cudaMemcpy(h->d_whole_tail, tail.data(), h->whole_tail_bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_table, table.data(), table.size() * sizeof(MergeEntry), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(h->d_byte_id, byte_id.data(), 256 * sizeof(int32_t), cudaMemcpyHostToDevice);
@@ -596,8 +597,7 @@ int tok_load(const uint8_t* vocab_bytes, const uint64_t* vocab_off, uint32_t n_v
   h->v.whole = h->d_whole;
   h->v.whole_bits = wbits;
   h->v.max_tok_len = max_tok_len;
-  h->v.vocab_bytes = h->d_vocab_bytes;
-  h->v.vocab_off = h->d_vocab_off;
+  h->v.whole_tail = h->d_whole_tail;
   // with ignore_merges a whole fragment that is any token is that token, so
   // fragments are never split into pieces (a piece may not take that rule)
   h->v.pair_bits = ignore_merges ? nullptr : h->d_pair_bits;
@@ -621,7 +621,7 @@ void tok_free(tok_handle* h) {
   if (h->stream) cudaStreamSynchronize(h->stream);
   free_workspace(h);
   void* ptrs[] = {h->d_table,  h->d_byte_id,     h->d_tok_len,   h->d_max_left, h->d_max_right, h->d_whole,
-                  h->d_vocab_bytes, h->d_vocab_off, h->d_pair_bits, h->d_items, h->d_item_off};
+                  h->d_whole_tail, h->d_pair_bits, h->d_items, h->d_item_off};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->h_status) cudaFreeHost(h->h_status);

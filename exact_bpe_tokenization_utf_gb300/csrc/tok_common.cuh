@@ -60,14 +60,15 @@ struct __align__(16) MergeEntry {
 };
 
 // whole-token table entry: a token whose own bytes encode to itself, keyed by
-// a hash of those bytes; offlen = byte offset of the token << 8 | length
-// (length 2..255), offlen == 0 marks an empty slot
-// a token that encodes to itself: its first bytes in the entry, so that a
-// probe of a fragment of at most 8 bytes needs no second load
+// a hash of those bytes.  Its first 8 bytes are in the entry, so that a probe
+// of a fragment of at most 8 bytes needs no second load; the rest of a longer
+// token is in the tail array, as whole 8-byte words (zero above the end), so
+// that its compare takes one load per 8 bytes.  offlen == 0 marks an empty
+// slot (len is 2..255).
 struct __align__(16) WholeEntry {
   unsigned long long head;  // first min(len, 8) bytes, little-endian, zero above
   uint32_t token;
-  uint32_t offlen;          // byte offset in the token bytes << 8 | len; 0: empty slot
+  uint32_t offlen;          // first tail word (tokens of more than 8 bytes) << 8 | len
 };
 
 struct DevVocab {
@@ -77,8 +78,7 @@ struct DevVocab {
   const WholeEntry* whole;    // tokens t with BPE(bytes(t)) == [t], length >= 2
   uint32_t whole_bits;        // log2(capacity)
   uint32_t max_tok_len;
-  const uint8_t* vocab_bytes; // token bytes back to back
-  const uint32_t* vocab_off;  // n_vocab + 1 offsets
+  const unsigned long long* whole_tail;  // bytes 8.. of the whole-table tokens longer than 8 bytes
   const int32_t* byte_id;     // 256 entries: initial symbol of each byte value
   const uint16_t* tok_len;    // byte length of every token
   const uint16_t* max_left;   // longest left operand of any merge whose right operand is t
@@ -242,6 +242,22 @@ __device__ __forceinline__ uint32_t whole_first_slot(const DevVocab& v, unsigned
   return (uint32_t)(h >> (64 - v.whole_bits));
 }
 
+// First min(len, 8) bytes at p, little-endian, zero above: three aligned
+// 32-bit loads and two funnel shifts.  The 12 bytes from p rounded down to a
+// multiple of 4 must be readable (shared-memory buffers with room after the
+// string).
+__device__ __forceinline__ unsigned long long head8(const uint8_t* p, int len) {
+  const uintptr_t u = reinterpret_cast<uintptr_t>(p);
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(u & ~uintptr_t(3));
+  const uint32_t sh = (uint32_t)(u & 3u) * 8u;
+  const uint32_t w0 = q[0], w1 = q[1], w2 = q[2];
+  unsigned long long v = ((unsigned long long)__funnelshift_r(w1, w2, sh) << 32) | __funnelshift_r(w0, w1, sh);
+  if (len < 8) v &= (1ull << (8 * len)) - 1ull;
+  return v;
+}
+
+// `s` is read with head8: len + 11 bytes from s (rounded down to 4) must be
+// readable.
 __device__ __forceinline__ int whole_lookup_at(const DevVocab& v, const uint8_t* s, int len,
                                                unsigned long long head, uint32_t slot, uint4 e) {
   const uint32_t mask = (1u << v.whole_bits) - 1u;
@@ -249,22 +265,16 @@ __device__ __forceinline__ int whole_lookup_at(const DevVocab& v, const uint8_t*
     if (probe) e = __ldg(reinterpret_cast<const uint4*>(v.whole + slot));
     if (e.w == 0u) return -1;
     if ((e.w & 255u) == (uint32_t)len && (((unsigned long long)e.y << 32) | e.x) == head) {
-      const uint8_t* t = v.vocab_bytes + (e.w >> 8);
+      // bytes 8.. against the tail words (most longer tokens have one)
+      const unsigned long long* t = v.whole_tail + (e.w >> 8);
       bool eq = true;
 #pragma unroll 1
-      for (int i = 8; i < len; ++i) eq &= __ldg(t + i) == s[i];
+      for (int i = 8; i < len; i += 8) eq &= __ldg(t++) == head8(s + i, len - i);
       if (eq) return (int)e.z;
     }
     slot = (slot + 1u) & mask;
   }
   return -1;
-}
-
-__device__ __forceinline__ int whole_lookup(const DevVocab& v, const uint8_t* s, int len) {
-  if (!whole_eligible(v, len)) return -1;
-  const unsigned long long head = bytes_head(s, len);
-  const uint32_t slot = whole_first_slot(v, bytes_hash(head, s, len));
-  return whole_lookup_at(v, s, len, head, slot, __ldg(reinterpret_cast<const uint4*>(v.whole + slot)));
 }
 
 // Record a device-side error of the call; the first error stays.
