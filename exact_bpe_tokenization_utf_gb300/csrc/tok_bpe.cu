@@ -1376,7 +1376,18 @@ __global__ void __launch_bounds__(B_THREADS, 16) k_bpe_engine(Call c, Workspace 
   const uint32_t nbat = S.nq[2];
   const uint32_t nwarps = G * (T / 32);
   const uint32_t gw = (G - 1 - bb) * (T / 32) + warp;
-  for (uint32_t b = gw; b < nbat; b += nwarps) short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
+  // one batch per warp first (no counter); with more batches than warps the
+  // rest go to whichever warp is free, each claim issued before the batch
+  // in hand runs, so that its latency hides behind that batch
+  const bool claim = nbat > nwarps;
+  uint32_t b = gw;
+  while (b < nbat) {
+    uint32_t nx = 0;
+    if (claim && (threadIdx.x & 31) == 0) nx = nwarps + atomicAdd(&st->sbatch_taken, 1u);
+    short_batch(c, ws, V, S.u.wb[warp], S.owner[warp], ws.sbatch[b]);
+    if (!claim) break;
+    b = __shfl_sync(0xffffffffu, nx, 0);
+  }
 }
 
 void launch_bpe_engine(const Call& call, const Workspace& w, const DevVocab& v, int n_sms, cudaStream_t s) {

@@ -108,12 +108,17 @@ struct DevStatus {
   uint32_t emit_done;              // K5 CTAs finished
   unsigned long long n_ids;
   unsigned long long sfrag_count;  // short fragments queued
-  uint32_t sbatch_count, sbatch_taken;  // warp batches of short fragments
-  uint32_t wide_count, wide_taken;      // fragments of 33..B_CAP bytes
-  uint32_t long_count, long_taken;      // longer fragments
+  uint32_t sbatch_count;           // warp batches of short fragments
+  uint32_t wide_count;             // fragments of 33..B_CAP bytes
+  uint32_t long_count, long_taken; // longer fragments
+  // warp batches claimed by K3b's warps beyond their first one: many warps
+  // add to it while the grid engine waits at its barriers, so each has a
+  // line of its own
+  alignas(128) uint32_t sbatch_taken;
   // the grid engine of K3b: its barrier (arrivals, generation), the flag a
   // CTA sets when it gave up waiting, and per sweep whether a pair merges
-  uint32_t gb_count, gb_gen, g_abort, g_any[3];
+  alignas(128) uint32_t gb_count;
+  uint32_t gb_gen, g_abort, g_any[3];
 };
 static_assert(sizeof(DevStatus) % 16 == 0, "the group totals follow the status");
 
