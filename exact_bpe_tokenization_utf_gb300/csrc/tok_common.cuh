@@ -105,7 +105,7 @@ struct DevStatus {
   // cleared before every call, together with the group totals that follow
   // the status in its allocation (one memset)
   int32_t code;
-  uint32_t emit_done;              // K5 CTAs finished
+  uint32_t pad0;
   unsigned long long n_ids;
   unsigned long long sfrag_count;  // short fragments queued
   uint32_t sbatch_count;           // warp batches of short fragments

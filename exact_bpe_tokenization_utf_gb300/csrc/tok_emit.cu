@@ -51,6 +51,34 @@ __device__ void write_user_status(const Call& c, const DevStatus* st) {
   c.user_status[3] = 0;
 }
 
+// The end of an encode, one thread: an inconsistency the thread found (a
+// bug upstream), recorded for the host path and stored in the caller's status
+// at once; and, by the last chunk's thread 0, the number of ids, the offsets
+// of the items that start at the text end and the rest of the caller's
+// status, written without waiting for the other CTAs: the boundary kernel set
+// the status code to OK before any stage ran, and the code only ever changes
+// to an error (the earlier kernels' errors are final when this kernel
+// starts, this kernel's are stored by the thread that finds them), so a late
+// store of the code cannot hide an error.
+__device__ __noinline__ void emit_tail(const Call& c, DevStatus* st, bool bug, bool last, unsigned long long n_ids) {
+  if (bug) {
+    set_error(st, ST_EINTERNAL);
+    if (c.user_status) c.user_status[0] = ST_EINTERNAL;
+  }
+  if (!last) return;
+  st->n_ids = n_ids;
+  if (c.item_off) {
+    for (int k = c.n_items; k >= 0 && c.item[k] >= c.n; --k) c.item_off[k] = (long long)n_ids;
+  }
+  if (!c.user_status) return;
+  const long long eo = err_offset(c.epoch, st->err_off);
+  const long long code = eo >= 0 ? (long long)ST_EUTF8 : (long long)st->code;
+  if (code != ST_OK) c.user_status[0] = code;
+  c.user_status[1] = (long long)n_ids;
+  c.user_status[2] = eo;
+  c.user_status[3] = 0;
+}
+
 }  // namespace
 
 // block-wide exclusive sum of v and the sum of u over the CTA, in one pass
@@ -99,7 +127,7 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
   __shared__ int big_a[MAX_BIG], big_k[MAX_BIG], big_o[MAX_BIG];
   __shared__ int scan[B_THREADS / 32];
   __shared__ unsigned long long scan64[B_THREADS / 32];
-  __shared__ int s_item, s_nbig, s_last;
+  __shared__ int s_item, s_nbig;
   const int tid = threadIdx.x, T = B_THREADS;
   // a programmatic dependent of the engine kernel: wait for its writes
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -133,12 +161,13 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
   // end); anything else would be a bug upstream, reported instead of
   // written out of bounds
   int cn[4] = {cnt4.x, cnt4.y, cnt4.z, cnt4.w};
+  bool bug = false;
   int ids = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     if (!((mine >> q) & 1u)) { cn[q] = 0; continue; }
     if (cn[q] < 1 || cn[q] > c.n - (r0 + q0 + q)) {
-      set_error(st, ST_EINTERNAL);
+      bug = true;
       cn[q] = 0;
     }
     ids += cn[q];
@@ -147,7 +176,7 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
   unsigned long long base = 0;  // ids before this chunk
   int o = block_excl_sum_and_total(ids, part, &total, &base, scan, scan64);
   if ((uint32_t)total != my_total) {  // the counts disagree with the chunk total: a bug upstream
-    if (tid == 0) set_error(st, ST_EINTERNAL);
+    bug |= tid == 0;
     total = 0;
   }
   // ids in text order: fragments of up to 8 ids by their thread, longer ones
@@ -184,7 +213,7 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
           big_k[bi] = k;
           big_o[bi] = o;
         } else {
-          set_error(st, ST_EINTERNAL);
+          bug = true;
         }
       }
       o += k;
@@ -236,24 +265,9 @@ __global__ void __launch_bounds__(B_THREADS, OFFS ? 10 : 16) k_emit(Call c, Work
     }
   }
   // the CTA of the last chunk knows the number of ids (the ids before it and
-  // its own); the last CTA to finish completes the status
-  __syncthreads();
-  if (tid == 0) {
-    if (chunk == nch - 1) st->n_ids = base + (unsigned long long)total;
-    __threadfence();
-    s_last = atomicAdd(&st->emit_done, 1u) == (uint32_t)(nch - 1);
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    const unsigned long long n_ids = *(volatile unsigned long long*)&st->n_ids;
-    if (tid == 0) {
-      if (c.item_off) {
-        for (int k = c.n_items; k >= 0 && c.item[k] >= c.n; --k) c.item_off[k] = (long long)n_ids;
-      }
-      write_user_status(c, st);
-    }
-  }
+  // its own) and completes the status (emit_tail)
+  const bool last = chunk == nch - 1 && tid == 0;
+  if (bug || last) emit_tail(c, st, bug, last, base + (unsigned long long)total);
 }
 
 // empty input: reset the status and report zero ids

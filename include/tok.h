@@ -162,7 +162,8 @@ int tok_encode_batch(tok_handle* h, const uint8_t* const* texts, const uint64_t*
  * `stream` (a cudaStream_t of the handle's device; NULL = the CUDA default
  * stream) without any host synchronisation.
  * d_text: device, len bytes.  d_ids: device, cap >= len int32 (required).
- * d_status: device int64[4], written when the chain finishes:
+ * d_status: device int64[4], valid once the chain has finished (read it
+ * after synchronising with `stream`):
  *   [0] = TOK_OK or a negative code, [1] = number of ids,
  *   [2] = offset of the first malformed UTF-8 sequence (or -1), [3] = reserved.
  * Returns TOK_EINVAL / TOK_EBUF / TOK_ENOMEM / TOK_ECUDA for launch-time
