@@ -418,6 +418,61 @@ def test_device_entry_points(pkg):
     assert d_ids[:int(off_h[-1])].cpu().numpy().tolist() == ids_h.tolist()
 
 
+def test_device_status_whatever_it_held_before(pkg):
+    # the caller's status buffer holds garbage, then an earlier call's error:
+    # after each call it holds exactly this call's result (the boundary
+    # kernel sets the code, the emit kernel's last chunk completes the rest)
+    import torch
+    from oracle.utf8 import decode_utf8
+    v, tok = pair(pkg, "cl100k_session_100k", PATTERN_CL100K)
+    stream = torch.cuda.current_stream().cuda_stream
+    good = textgen.agentic_session(120_000, 21).encode()
+    small = textgen.agentic_session(3_000, 22).encode()
+    bad = good[:70_001] + b"\xff" + good[70_001:]
+    with pytest.raises(Utf8Error) as e:
+        decode_utf8(bad)
+    bad_at = e.value.offset
+    n = len(bad)
+    d_text = torch.empty(n, dtype=torch.uint8, device="cuda")
+    d_ids = torch.empty(n, dtype=torch.int32, device="cuda")
+    d_st = torch.tensor([-77, 123456789, 42, 99], dtype=torch.int64, device="cuda")
+
+    def put(data):
+        if data:
+            d_text[:len(data)] = torch.frombuffer(bytearray(data), dtype=torch.uint8).cuda()
+
+    def run(data):
+        put(data)
+        tok.encode_device(d_text.data_ptr(), len(data), d_ids.data_ptr(), n, d_st.data_ptr(), stream)
+        torch.cuda.synchronize()
+        return d_st.cpu().tolist()
+
+    for data in (good, small):
+        d_st.copy_(torch.tensor([-77, 123456789, 42, 99]))
+        want = encode(data, v, PATTERN_CL100K)
+        assert run(data) == [pkg.TOK_OK, len(want), -1, 0]
+        assert d_ids[:len(want)].cpu().tolist() == want
+    st = run(bad)
+    assert st[0] == pkg.TOK_EUTF8 and st[2] == bad_at
+    assert run(good) == [pkg.TOK_OK, len(encode(good, v, PATTERN_CL100K)), -1, 0]
+    st = run(bad)
+    assert st[0] == pkg.TOK_EUTF8 and st[2] == bad_at
+    assert run(b"") == [pkg.TOK_OK, 0, -1, 0]
+    # a batch after an error, its status buffer full of garbage
+    items = [good[:40_000], b"", good[40_000:]]
+    starts = torch.tensor(np.cumsum([0] + [len(x) for x in items]).astype(np.int64)).cuda()
+    d_off = torch.full((len(items) + 1,), -5, dtype=torch.int64, device="cuda")
+    run(bad)
+    put(good)
+    d_st.copy_(torch.tensor([-77, 123456789, 42, 99]))
+    tok.encode_batch_device(d_text.data_ptr(), len(good), starts.data_ptr(), len(items), d_ids.data_ptr(), n,
+                            d_off.data_ptr(), d_st.data_ptr(), stream)
+    torch.cuda.synchronize()
+    ids_h, off_h = tok.encode_batch(items)
+    assert d_st.cpu().tolist() == [pkg.TOK_OK, int(off_h[-1]), -1, 0]
+    assert d_off.cpu().tolist() == off_h.tolist()
+
+
 # --- o200k-style pattern --------------------------------------------------------
 
 def test_o200k_style_encode_matches_oracle(pkg, oracle_pool):
