@@ -209,7 +209,7 @@ int tok_pretokenize_batch(tok_handle* h, const uint8_t* const* texts, const uint
  * callers that cannot allocate device memory (code inside another framework's
  * memory pool or arena, code that must not trigger the device-wide
  * synchronisation cudaMalloc/cudaFree can cause, hosts with a fixed memory
- * budget).  The paper has no counterpart: it is an integration entry point of
+ * budget).  TokTier describes no such call: it is an integration entry point of
  * this library, not a step of the method.
  * Needs no handle and allocates nothing: its scratch (the status block the
  * boundary kernel writes) lives in a fixed __device__ array of this library
