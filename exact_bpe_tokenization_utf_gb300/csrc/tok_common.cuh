@@ -170,7 +170,7 @@ struct Call {
   int grid_ctas;              // K3b CTAs that run the grid engine (0: none)
   uint32_t grid_extra;        // arrivals a grid barrier waits for beyond grid_ctas (0; a test sets 1)
   unsigned long long wait_ns; // limit of a device-side wait, in ns of the global timer
-  Prefetch pf[4];             // whole-token table, token bytes, merge table, byte-pair bits
+  Prefetch pf[4];             // whole-token table, its tail words, merge table, byte-pair bits
 };
 
 // The first malformed UTF-8 byte of a call, as one word that atomicMax keeps
@@ -235,7 +235,7 @@ __device__ __forceinline__ unsigned long long merge_lookup(const DevVocab& v, ui
 
 // Token whose bytes equal s[0..len) and whose own bytes encode to itself,
 // or -1.  The hash only selects the first slot; the length and the first 8
-// bytes are compared in the entry, the rest against the token bytes.  Split
+// bytes are compared in the entry, the rest against the token's tail words.  Split
 // in parts so that a thread can issue the first probes of several strings
 // before it waits for any: whole_first_slot gives the first slot of a hash,
 // whole_lookup_at finishes from the loaded first entry.
